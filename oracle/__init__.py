@@ -1,0 +1,60 @@
+"""Plain CPU oracle for exact attention (test infrastructure only).
+
+This package is test infrastructure.  It is a slow, deliberately simple float64
+restatement of what the attention path computes, written so that a reader can
+check it against the pages by eye:
+
+* ``attention``  -- the textbook definition O = softmax(scale * Q K^T [+causal]) V,
+  the per-row logsumexp, and the analytic backward (dQ, dK, dV).  Source of the
+  definition: "FlashAttention-2 (DE)", section "Hintergrund: Das Attention-Problem
+  in Transformern" (standard self-attention, O(N^2) time and memory), and the
+  exactness claim in the article's lead ("exakt identisch ... ohne
+  Genauigkeitsverlust") and in "Leistung und Effizienz" ("exakt und
+  deterministisch").  The tiled method reaches this same result, so the oracle is
+  the definition itself, never an online or tiled softmax.
+* ``brute``      -- a scalar triple-loop twin of ``attention`` for tiny inputs.
+* ``fp8``        -- the FP8 input preparation: random-sign Walsh-Hadamard rotation
+  of Q and K (incoherent processing) and per-tile block quantisation to OCP e4m3.
+  Source: "FlashAttention-Skalierung, Multi-GPU-Training und
+  Gewichtsquantisierung", section 1, bullet "Unterstützung geringer
+  FP8-Präzision".
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The product
+path (``io_aware_exact_fwd_gb300``) never imports it, and this package imports
+nothing from the product path.  Every function here is pinned by CPU tests
+against closed forms, invariants, brute force or library special cases; none is
+"parity unpinned".
+"""
+
+from .attention import (
+    attention_forward,
+    attention_forward_rows,
+    attention_backward,
+)
+from .brute import attention_forward_brute
+from .fp8 import (
+    sylvester_hadamard,
+    fwht_f32,
+    e4m3_encode,
+    e4m3_decode,
+    e4m3_round,
+    fp8_prepare,
+    fp8_dequantize,
+    E4M3_MAX,
+)
+
+__all__ = [
+    "attention_forward",
+    "attention_forward_rows",
+    "attention_backward",
+    "attention_forward_brute",
+    "sylvester_hadamard",
+    "fwht_f32",
+    "e4m3_encode",
+    "e4m3_decode",
+    "e4m3_round",
+    "fp8_prepare",
+    "fp8_dequantize",
+    "E4M3_MAX",
+]

@@ -1,0 +1,165 @@
+"""Pins of the FP8 preparation oracle: Hadamard rotation, e4m3 rounding, tile scales."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import (
+    E4M3_MAX,
+    attention_forward,
+    e4m3_decode,
+    e4m3_encode,
+    e4m3_round,
+    fp8_dequantize,
+    fp8_prepare,
+    fwht_f32,
+    sylvester_hadamard,
+)
+from synth import normal_qkv, outlier_qkv, rotation_signs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.mark.parametrize("d", [1, 2, 8, 64, 128])
+def test_hadamard_is_orthogonal_up_to_d(d):
+    h = sylvester_hadamard(d)
+    assert set(np.unique(h)) <= {-1.0, 1.0}
+    np.testing.assert_array_equal(h @ h.T, d * np.eye(d))
+    s = rotation_signs(d, seed=3).numpy().astype(np.float64)
+    m = np.diag(s) @ h / np.sqrt(d)
+    assert np.abs(m @ m.T - np.eye(d)).max() < 1e-12
+
+
+def test_hadamard_known_small_case():
+    np.testing.assert_array_equal(sylvester_hadamard(4), np.array(
+        [[1, 1, 1, 1], [1, -1, 1, -1], [1, 1, -1, -1], [1, -1, -1, 1]], dtype=np.float64))
+
+
+def test_rotation_preserves_scores():
+    x = normal_qkv(1, 1, 32, 64, seed=31)
+    q, k = x["q"].numpy().astype(np.float64)[0, 0], x["k"].numpy().astype(np.float64)[0, 0]
+    s = rotation_signs(64, seed=31).numpy().astype(np.float64)
+    m = np.diag(s) @ sylvester_hadamard(64) / 8.0
+    np.testing.assert_allclose((q @ m) @ (k @ m).T, q @ k.T, rtol=0, atol=1e-12)
+
+
+def test_same_seed_same_signs():
+    a, b, c = rotation_signs(128, 5), rotation_signs(128, 5), rotation_signs(128, 6)
+    assert torch.equal(a, b) and not torch.equal(a, c)
+    assert set(a.tolist()) <= {-1, 1}
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwht_matches_matrix_product_within_fp32_rounding(d):
+    x = outlier_qkv(1, 2, 96, d, seed=32)["q"].numpy()
+    s = rotation_signs(d, seed=32).numpy()
+    fast = fwht_f32(x, s).astype(np.float64)
+    exact = x.astype(np.float64) @ (np.diag(s.astype(np.float64)) @ sylvester_hadamard(d))
+    # Each of the log2(d) butterfly stages rounds once: |err| <= log2(d) * 2^-24 * sum|x|.
+    bound = np.log2(d) * 2.0 ** -24 * np.abs(x.astype(np.float64)).sum(axis=-1, keepdims=True)
+    assert (np.abs(fast - exact) <= bound * 1.0001).all()
+
+
+def test_e4m3_golden_values_and_rounding():
+    g = json.load(open(os.path.join(GOLDEN, "e4m3_codes.json")))
+    for item in g["values_by_definition"]:
+        assert int(e4m3_encode(np.array([item["value"]]))[0]) == item["code"], item
+        assert float(e4m3_decode(np.array([item["code"]], dtype=np.uint8))[0]) == item["value"], item
+    for item in g["rounding_by_definition"]:
+        assert int(e4m3_encode(np.array([item["input"]]))[0]) == item["code"], item
+
+
+def test_e4m3_all_codes_round_trip():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = e4m3_decode(codes)
+    finite = ~np.isnan(vals)
+    assert np.nanmax(vals) == E4M3_MAX and np.nanmin(vals) == -E4M3_MAX
+    np.testing.assert_array_equal(e4m3_encode(vals[finite]), codes[finite])
+    assert set(codes[~finite].tolist()) == {0x7F, 0xFF}
+    # Values strictly increase with the code within the positive half.
+    pos = vals[:0x7F]
+    assert (np.diff(pos) > 0).all()
+
+
+def test_e4m3_ties_to_even_everywhere():
+    vals = e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))  # 0 .. 448, ascending
+    mids = (vals[:-1] + vals[1:]) / 2
+    got = e4m3_encode(mids)
+    lo, hi = np.arange(0, 0x7E), np.arange(1, 0x7F)
+    expect = np.where(lo % 2 == 0, lo, hi)
+    np.testing.assert_array_equal(got, expect.astype(np.uint8))
+
+
+def test_e4m3_saturates():
+    x = np.array([448.0, 449.0, 480.0, 1e30, -500.0, -448.0])
+    np.testing.assert_array_equal(e4m3_round(x), [448, 448, 448, 448, -448, -448])
+
+
+def test_e4m3_agrees_with_torch_cast_in_range():
+    rng = np.random.default_rng(7)
+    x = np.concatenate([
+        rng.uniform(-448, 448, 20000),
+        rng.standard_normal(20000),
+        rng.uniform(-0.02, 0.02, 20000),          # subnormal and small normal range
+    ]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(e4m3_encode(x), ref)
+
+
+def test_fp8_prepare_tiles_scales_and_error_bounds():
+    d, N = 128, 200                       # 4 tiles, the last one ragged (8 rows)
+    x = outlier_qkv(1, 2, N, d, seed=33)
+    s = rotation_signs(d, seed=33).numpy()
+    out = fp8_prepare(x["q"], x["k"], x["v"], s)
+    assert out["sq"].shape == (1, 2, 4) and out["q8"].dtype == np.uint8
+    qr = fwht_f32(x["q"].numpy(), s).astype(np.float64)
+    for name, ref in (("q", qr), ("v", x["v"].numpy().astype(np.float64))):
+        codes, sig = out[name + "8"], out["s" + name]
+        deq = fp8_dequantize(codes, sig)
+        for t in range(4):
+            blk = ref[..., t * 64:(t + 1) * 64, :]
+            amax = np.abs(blk).max(axis=(-2, -1))
+            np.testing.assert_allclose(sig[..., t], amax / 448.0, rtol=2 ** -23)
+            # Every tile reaches the top code in magnitude (its amax maps to 448).
+            assert (np.abs(e4m3_decode(codes[..., t * 64:(t + 1) * 64, :])).max(axis=(-2, -1)) == 448).all()
+            err = np.abs(deq[..., t * 64:(t + 1) * 64, :] - blk)
+            # 3 mantissa bits: relative error <= 2^-4 for normals, absolute <= 2^-10 * sigma for subnormals.
+            bound = np.maximum(np.abs(blk) * 2.0 ** -4, 2.0 ** -10 * sig[..., t][..., None, None]) * 1.001
+            assert (err <= bound).all()
+
+
+def test_fp8_prepare_zero_tile():
+    z = torch.zeros(1, 1, 64, 64)
+    out = fp8_prepare(z, z, z, np.ones(64))
+    assert (out["q8"] == 0).all() and (out["sq"] == 1).all() and (out["sv"] == 1).all()
+
+
+def _rel_rmse(o, ref):
+    return np.sqrt(((o - ref) ** 2).mean()) / np.sqrt((ref ** 2).mean())
+
+
+def test_fp8_input_quantisation_error_floor():
+    # Attention on the dequantised e4m3 inputs is the best any FP8 kernel of this
+    # design can reach before P is rounded.  Its error against exact attention on
+    # the unquantised inputs follows the e4m3 rounding model: 3 mantissa bits give
+    # a relative rounding error of about 2^-3/sqrt(12)/1.53 ~ 2.4% RMS per
+    # element, so V alone contributes ~2.4% and the two score factors ~3.4%
+    # (sqrt(2) * 2.4%).  The floor therefore lies between 3% and 10% here, which is
+    # why a relative RMSE bound of 3e-2 against the unquantised inputs cannot be met.
+    d, N = 128, 256
+    x = outlier_qkv(1, 2, N, d, seed=34)
+    s = rotation_signs(d, seed=34).numpy()
+    out = fp8_prepare(x["q"], x["k"], x["v"], s)
+    qd = fp8_dequantize(out["q8"], out["sq"])
+    kd = fp8_dequantize(out["k8"], out["sk"])
+    vd = fp8_dequantize(out["v8"], out["sv"])
+    scale = d ** -0.5
+    o_ref, _ = attention_forward(x["q"], x["k"], x["v"], scale, False)
+    # Rotated operands: (Q M)(K M)^T = d * Q K^T for the unnormalised M = diag(s) H.
+    o_q, _ = attention_forward(qd, kd, vd, scale / d, False)
+    o_v, _ = attention_forward(x["q"], x["k"], vd, scale, False)
+    assert 0.015 < _rel_rmse(o_v, o_ref) < 0.035
+    assert 0.03 < _rel_rmse(o_q, o_ref) < 0.10
