@@ -1,0 +1,339 @@
+"""Throughput of the exact-attention hot path on GB300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (the configuration the headline metric is quoted on): bf16 attention,
+B=4, H=16, N=2048, d=128, scale 1/sqrt(d), non-causal, inputs N(0,1) from seed 2.
+One step = one pass of the hot path over that batch: the forward kernel
+(fa_fwd).  TFLOP/s counts 4*B*H*N^2*d per forward.
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
+torch.cuda.synchronize() on both sides.  L2 (129 MB) is flushed before every
+step by writing a 256 MB buffer outside the per-step CUDA-event pairs; device
+time is the sum of the per-step event pairs on the launching stream, max over
+ranks.  `e2e` repeats the step through the same public call with the inputs in
+pinned host memory: the H2D copies of Q, K, V, the kernel and the D2H copies of
+O and LSE are all inside its timed region.
+
+Under torchrun (N > 1) every rank runs the same independent replica (the heads
+shard with no exchange, so there is no collective on the data path) and rank 0
+prints the aggregate.  `--impl reference` times the float64 CPU oracle on a
+bounded row sample of the same workload instead (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = {"workload": "bf16 attention forward, B=4 H=16 N=2048 d=128, non-causal, scale=1/sqrt(d)",
+            "B": 4, "H": 16, "N": 2048, "d": 128, "causal": False, "seed": 2}
+METRIC = "attention fwd/bwd TFLOP/s on 1 GB300 and % of dense BF16/FP8 tensor peak"
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def fwd_flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"bf16_tflops": j.get("bf16_tflops"), "bf16_tflops_sustained": j.get("bf16_tflops_sustained"),
+                "hbm_gbs": j.get("hbm_gbs"), "source": "measured"}
+    return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def run_ours(args):
+    import torch
+
+    import io_aware_exact_fwd_gb300 as fa
+    from synth import normal_qkv
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    fa.load_library()
+    w = WORKLOAD
+    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
+    scale = d ** -0.5
+    x = normal_qkv(B, H, N, d, w["seed"] + rank)
+    q, k, v = (x[n].to(torch.bfloat16).cuda() for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    launches_per_step = 1
+
+    def step():
+        fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    fa.fa_sync_check()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop() if sampler else None
+    fa.fa_sync_check()
+    per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dev_ms = sum(per_step)
+    if world > 1:
+        t = torch.tensor([dev_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        dev_ms = float(t.item())
+    flops_step = fwd_flops(B, H, N, d, causal)
+    ms_per_step = dev_ms / args.steps
+    value = flops_step * args.steps * world / (dev_ms * 1e-3) / 1e12
+
+    # End to end through the public call: pinned host inputs in, O and LSE back out.
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        fa.fa_fwd(dq, dk, dv, o=o, lse=lse, causal=causal, scale=scale)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    fa.fa_sync_check()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return None
+
+    peaks = load_peaks()
+    peak = peaks["bf16_tflops"]
+    kernel_tflops = flops_step / (ms_per_step * 1e-3) / 1e12
+    roofline = {
+        "bound": "tensor", "kernel": "fwd_bf16_kernel<128,false>", "achieved": round(kernel_tflops, 1),
+        "peak": peak, "peak_source": f"{peaks['source']} bf16_tflops (burst, cuBLAS)", "unit": "TFLOP/s",
+        "frac": round(kernel_tflops / peak, 4), "traffic": args.traffic,
+        "algorithmic_flops_per_launch": flops_step,
+    }
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(seconds=args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(WORKLOAD, l2="flushed before every step (256 MB write, outside the timed event pairs)",
+                       parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "frac_of_peak": round(value / world / peak, 4),
+        "roofline": roofline,
+        "e2e": {"value": round(flops_step / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed_region": round(t_wall, 3),
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line
+
+
+def cpu_baseline(seconds: float = 10.0):
+    """The float64 oracle, as it stands, on a bounded row sample of the workload."""
+    import numpy as np
+
+    from oracle import attention_forward_rows
+    from synth import normal_qkv
+
+    w = WORKLOAD
+    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
+    x = normal_qkv(1, 2, N, d, w["seed"])
+    import torch
+
+    q, k, v = (x[n].to(torch.bfloat16).to(torch.float64).numpy() for n in ("q", "k", "v"))
+    rows_per_call = 256
+    done_rows, t0 = 0, time.perf_counter()
+    h = 0
+    while time.perf_counter() - t0 < seconds:
+        r0 = (done_rows // rows_per_call * rows_per_call) % N
+        rows = np.arange(r0, min(N, r0 + rows_per_call))
+        attention_forward_rows(q[0, h % 2], k[0, h % 2], v[0, h % 2], d ** -0.5, causal, rows)
+        done_rows += len(rows)
+        h += 1
+    dt = time.perf_counter() - t0
+    flops = 4.0 * done_rows * N * d / (2 if causal else 1)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done_rows} query rows x {N} keys of 2 heads (d={d}) in {dt:.1f} s, float64 numpy, "
+                      f"BLAS threads = {cores}"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import numpy as np
+    import torch
+
+    from oracle import attention_forward_rows
+    from synth import normal_qkv
+
+    w = WORKLOAD
+    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
+    x = normal_qkv(1, 2, N, d, w["seed"])
+    q, k, v = (x[n].to(torch.bfloat16).to(torch.float64).numpy() for n in ("q", "k", "v"))
+    rows_per_step = 64
+
+    def step(i):
+        r0 = (i * rows_per_step) % N
+        rows = np.arange(r0, min(N, r0 + rows_per_step))
+        attention_forward_rows(q[0, i % 2], k[0, i % 2], v[0, i % 2], d ** -0.5, causal, rows)
+        return len(rows)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    rows = 0
+    for i in range(args.steps):
+        rows += step(i)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * rows * N * d / (2 if causal else 1)
+    value = flops / dt / 1e12
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(WORKLOAD),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_per_step} query rows x {N} keys of one head per step"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture of this kernel version")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,118 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library (libfa.so).
+ *
+ * What it computes.  For every batch b and head h, with Q, K, V the N x d
+ * matrices of that (b, h):
+ *
+ *     O   = softmax(scale * Q K^T  [+ causal mask]) V
+ *     LSE = per-row natural-log logsumexp of the scaled (masked) scores
+ *
+ * exactly as standard self-attention defines it ("FlashAttention-2 (DE)",
+ * section "Hintergrund: Das Attention-Problem in Transformern"), but computed
+ * tile by tile with an online softmax so that the N x N score matrix is never
+ * materialised ("FlashAttention-2 (DE)", same section, "IO-Awareness" and
+ * "Tiling"; "FlashAttention-Skalierung, Multi-GPU-Training und
+ * Gewichtsquantisierung", section 1, FlashAttention-2 bullets).  The result is
+ * the standard one up to floating-point rounding ("exakt identisch ... ohne
+ * Genauigkeitsverlust", lead of "FlashAttention-2 (DE)").
+ *
+ * Conventions shared by every call:
+ *  - Tensors are dense, row-major [B, H, N, d] ("BHND": each head is one N x d
+ *    matrix, d contiguous).  LSE is [B, H, N] float32.  No strides are taken.
+ *  - Causal: key j is visible to query i iff j <= i (0-based, same N for
+ *    queries and keys).  Masked scores are excluded (weight exactly 0).
+ *  - scale must be finite and > 0 (the usual value is 1/sqrt(d)).
+ *  - d must be 64 or 128.  N >= 1 is arbitrary (no multiple-of-128 rule).
+ *  - All pointers are DEVICE pointers owned by the caller, on the current CUDA
+ *    device, and must stay valid until the work queued on `stream` finishes.
+ *    The library never allocates device memory in these calls and keeps no
+ *    reference to the pointers after the call returns.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *    asynchronous with respect to the host: they validate, enqueue and return.
+ *  - Every call is thread-safe.
+ *  - Errors: validation happens synchronously, before anything is enqueued;
+ *    a nonzero status means nothing was launched.  Errors detected by a kernel
+ *    while it runs (a bounded wait that expired) are reported by the next
+ *    fa_sync_check() on that device.  No C++ exception crosses this ABI.
+ *  - B * H * N == 0 is a no-op returning FA_OK (pointers may then be NULL).
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, causal not 0/1, scale not finite and > 0 */
+  FA_ERR_UNSUPPORTED = 2,  /* d not 64/128, sizes beyond the kernel's index range, or not an sm_103 GPU */
+  FA_ERR_MISALIGNED = 3,   /* a tensor pointer not 16-byte aligned (LSE: 4-byte) */
+  FA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, tensor-map encoding, ...) */
+  FA_ERR_TIMEOUT = 5,      /* a kernel gave up on a bounded wait; its outputs are undefined */
+  FA_ERR_WORKSPACE = 6     /* caller workspace missing or smaller than required */
+} fa_status;
+
+/* Static, human-readable text for a status code (never NULL). */
+FA_API const char* fa_strerror(int status);
+
+/* Library ABI version: (major << 16) | minor. */
+FA_API int fa_version(void);
+
+/*
+ * fa_fwd -- bf16 forward pass.
+ *   q, k, v : const bf16 [B, H, N, d]  (inputs)
+ *   o       : bf16 [B, H, N, d]        (output, fully overwritten)
+ *   lse     : float [B, H, N]          (output: ln sum_j exp(scale * q_i . k_j) over visible j)
+ * Numerics: scores accumulate in fp32 on the tensor cores; P is rounded to
+ * bf16 for the P V product; the running sum, the final 1/l and LSE are fp32;
+ * O is rounded to bf16 once at the end.  The result is bitwise reproducible
+ * run to run for the same inputs, sizes and device.
+ * Returns FA_OK or an error above (synchronous validation / launch failure).
+ */
+FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           int causal, float scale, fa_stream_t stream);
+
+/*
+ * fa_sync_check -- synchronise `stream`, then report device-detected errors.
+ * Returns FA_ERR_CUDA if the stream or a prior launch failed, FA_ERR_TIMEOUT
+ * if any kernel of this library on the current device expired a bounded wait
+ * since the last check (the word is then cleared), else FA_OK.
+ */
+FA_API int fa_sync_check(fa_stream_t stream);
+
+/*
+ * Last device error word observed by fa_sync_check on the current device:
+ * 0, or 0x80000000 | site, where site names the wait that expired (role in
+ * bits 8..11: 1 = TMA producer, 2 = MMA issuer, 3 = softmax/epilogue).
+ */
+FA_API unsigned int fa_last_error_site(void);
+
+/*
+ * Test hooks (process-wide, not thread-safe; meant for the test-suite only).
+ * fa_debug_set_wait_limit_ns: deadline of every bounded in-kernel wait
+ *   (default 2e9 ns).  0 restores the default.
+ * fa_debug_set_fault: 0 = none; 1 = the forward kernel's TMA producer
+ *   withholds K block 1 so that the MMA warp's bounded wait expires (needs
+ *   N > 128).  Faults are injected on the host side of the pipeline only: no
+ *   trap, no invalid address, no unbounded wait.
+ */
+FA_API void fa_debug_set_wait_limit_ns(unsigned long long ns);
+FA_API void fa_debug_set_fault(int fault);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

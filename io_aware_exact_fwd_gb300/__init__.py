@@ -1,0 +1,158 @@
+"""GB300 (sm_103a) exact attention: thin Python binding over the C ABI of libfa.so.
+
+Every function here has the name of the C entry point it calls (include/fa.h)
+and only marshals arguments: it checks dtypes, shapes and devices of torch
+tensors, passes their device pointers and the current CUDA stream, and raises
+``FAError`` on a nonzero status.  All arithmetic runs in the library's CUDA
+kernels; there is no fallback.  If libfa.so is missing, importing the binding
+still works but every call raises, so a missing build is never silent.
+
+PyTorch is used only as device-memory and stream plumbing.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "FAError", "load_library", "library_path", "fa_fwd", "fa_sync_check", "fa_strerror",
+    "fa_version", "fa_last_error_site", "fa_debug_set_wait_limit_ns", "fa_debug_set_fault",
+    "STATUS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "lib", "libfa.so")
+_lib = None
+
+STATUS = {
+    0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
+    4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_WORKSPACE",
+}
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = STATUS.get(status, str(status))
+        if _lib is not None:
+            msg += ": " + _lib.fa_strerror(status).decode()
+        super().__init__(f"{where}: {msg}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libfa.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"{_LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_strerror.restype = ctypes.c_char_p
+    lib.fa_strerror.argtypes = [i]
+    lib.fa_version.restype = i
+    lib.fa_version.argtypes = []
+    lib.fa_fwd.restype = i
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.fa_sync_check.restype = i
+    lib.fa_sync_check.argtypes = [vp]
+    lib.fa_last_error_site.restype = ctypes.c_uint
+    lib.fa_last_error_site.argtypes = []
+    lib.fa_debug_set_wait_limit_ns.restype = None
+    lib.fa_debug_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.fa_debug_set_fault.restype = None
+    lib.fa_debug_set_fault.argtypes = [i]
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise FAError(status, where)
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else ctypes.c_void_p(0)
+
+
+def _check_bhnd(name, t, shape, dtype):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous ([B, H, N, d] row-major)")
+
+
+def fa_fwd(q, k, v, o=None, lse=None, causal: bool = False, scale: float | None = None, stream=None):
+    """bf16 attention forward: returns (o, lse).
+
+    q, k, v: bf16 CUDA tensors [B, H, N, d], contiguous.  ``o`` (bf16 [B,H,N,d]) and
+    ``lse`` (fp32 [B,H,N]) are allocated if not given.  ``scale`` defaults to 1/sqrt(d).
+    """
+    import torch
+
+    lib = load_library()
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_bhnd(name, t, (B, H, N, d), torch.bfloat16)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_bhnd("o", o, (B, H, N, d), torch.bfloat16)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, N]")
+    if scale is None:
+        scale = d ** -0.5
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
+                        float(scale), _stream_handle(stream))
+    _check(st, "fa_fwd")
+    return o, lse
+
+
+def fa_sync_check(stream=None):
+    """Synchronise the stream and raise FAError if a kernel reported an error."""
+    lib = load_library()
+    _check(lib.fa_sync_check(_stream_handle(stream)), "fa_sync_check")
+
+
+def fa_strerror(status: int) -> str:
+    return load_library().fa_strerror(status).decode()
+
+
+def fa_version() -> int:
+    return load_library().fa_version()
+
+
+def fa_last_error_site() -> int:
+    return load_library().fa_last_error_site()
+
+
+def fa_debug_set_wait_limit_ns(ns: int):
+    load_library().fa_debug_set_wait_limit_ns(int(ns))
+
+
+def fa_debug_set_fault(fault: int):
+    load_library().fa_debug_set_fault(int(fault))

@@ -1,0 +1,195 @@
+// C ABI of libfa.so: argument validation, tensor-map encoding, dispatch to the
+// kernels, and the device error word that bounded in-kernel waits report to.
+// Declarations and the contract of every entry point: include/fa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+// One error word per device (a __device__ variable is instantiated on every
+// device that loads this module).  Kernels receive its address as a plain
+// pointer; the address is looked up once per device with the device current.
+static __device__ unsigned int g_fa_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+
+struct DeviceState {
+  bool ready = false;
+  unsigned int* err_word = nullptr;
+  int cc = 0;  // major * 10 + minor
+  unsigned int last_site = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_fault{0};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Resolves per-device state (error word address, compute capability) once.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FA_ERR_CUDA;
+    s.cc = major * 10 + minor;
+    if (s.cc != 103) {
+      *out = &s;
+      return FA_ERR_UNSUPPORTED;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_error_word) != cudaSuccess) return FA_ERR_CUDA;
+    s.err_word = static_cast<unsigned int*>(p);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return FA_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    s.ready = true;
+  }
+  *out = &s;
+  return s.cc == 103 ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+fa::DebugKnobs knobs() {
+  fa::DebugKnobs k;
+  k.wait_limit_ns = g_wait_ns.load();
+  k.fault = g_fault.load();
+  return k;
+}
+
+// Shared validation of the attention-shaped calls.  Returns FA_OK, a status,
+// or -1 meaning "valid, but empty: nothing to do".
+int validate_shape(int B, int H, int N, int d, int causal, float scale) {
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0) return -1;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long nqt = (static_cast<long long>(N) + fa::kBlockQ - 1) / fa::kBlockQ;
+  // Grid size (units of work) and element counts must stay inside int / TMA ranges.
+  if (bh * nqt > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (bh * N > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+}  // namespace
+
+namespace fa {
+
+cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int cols,
+                         int rows, int depth, int box_cols, int box_rows) {
+  if (!g_encode) return cudaErrorInitializationError;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(depth)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * elem_bytes,
+                                 static_cast<cuuint64_t>(cols) * elem_bytes * static_cast<cuuint64_t>(rows)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace fa
+
+extern "C" {
+
+const char* fa_strerror(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported (head dim, size or device)";
+    case FA_ERR_MISALIGNED: return "misaligned pointer";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "kernel wait timed out";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int fa_version(void) { return (0 << 16) | 1; }
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int causal,
+           float scale, fa_stream_t stream) {
+  const int vs = validate_shape(B, H, N, d, causal, scale);
+  if (vs < 0) return FA_OK;
+  if (vs != FA_OK) return vs;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  const int st = device_state(&ds);
+  if (st != FA_OK) return st;
+  fa::FwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.err_word = ds->err_word;
+  a.dbg = knobs();
+  return fa::launch_fwd_bf16(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_sync_check(fa_stream_t stream) {
+  DeviceState* ds = nullptr;
+  const int st = device_state(&ds);
+  if (st != FA_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, ds->err_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(ds->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    ds->last_site = word;
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+unsigned int fa_last_error_site(void) {
+  DeviceState* ds = nullptr;
+  if (device_state(&ds) != FA_OK || !ds) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  return ds->last_site;
+}
+
+void fa_debug_set_wait_limit_ns(unsigned long long ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs); }
+
+void fa_debug_set_fault(int fault) { g_fault.store(fault); }
+
+}  // extern "C"

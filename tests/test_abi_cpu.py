@@ -1,0 +1,92 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared
+symbol, and rejects bad arguments synchronously with the documented status."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session")
+def lib():
+    import io_aware_exact_fwd_gb300 as fa
+
+    if not os.path.exists(fa.library_path()):
+        from io_aware_exact_fwd_gb300 import _build
+
+        _build.build()
+    return fa.load_library()
+
+
+def _declared_symbols():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^FA_API\s+[^;(]*?\b(fa_\w+)\s*\(", src, re.M)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_symbols()
+    assert "fa_fwd" in names and "fa_sync_check" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_and_version(lib):
+    import io_aware_exact_fwd_gb300 as fa
+
+    for code in range(0, 7):
+        assert fa.fa_strerror(code)
+    assert fa.fa_strerror(99) == "unknown status"
+    assert fa.fa_version() >= 1
+
+
+FAKE = 0x10000  # 16-byte aligned fake device address: never dereferenced on these paths
+
+
+def _fwd(lib, B=1, H=1, N=128, d=64, causal=0, scale=0.125, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE):
+    vp = ctypes.c_void_p
+    return lib.fa_fwd(vp(q), vp(k), vp(v), vp(o), vp(lse), B, H, N, d, causal, scale, vp(0))
+
+
+def test_forward_validation_statuses(lib):
+    assert _fwd(lib, B=-1) == 1
+    assert _fwd(lib, N=-5) == 1
+    assert _fwd(lib, causal=2) == 1
+    for s in (0.0, -0.1, float("nan"), float("inf")):
+        assert _fwd(lib, scale=s) == 1
+    assert _fwd(lib, d=96) == 2
+    assert _fwd(lib, d=256) == 2
+    assert _fwd(lib, q=0) == 1
+    assert _fwd(lib, lse=0) == 1
+    assert _fwd(lib, o=FAKE + 8) == 3
+    assert _fwd(lib, lse=FAKE + 2) == 3
+    # Empty problems are valid no-ops, even with NULL pointers.
+    assert _fwd(lib, B=0, q=0, k=0, v=0, o=0, lse=0) == 0
+    assert _fwd(lib, N=0, q=0, k=0, v=0, o=0, lse=0) == 0
+    # Sizes beyond the kernel's index range are refused before any device work.
+    assert _fwd(lib, B=1 << 16, H=1 << 16, N=128) == 2
+
+
+def test_binding_raises_without_gpu_work(lib):
+    import torch
+
+    import io_aware_exact_fwd_gb300 as fa
+
+    with pytest.raises(TypeError):
+        fa.fa_fwd(torch.zeros(1, 1, 8, 64), torch.zeros(1, 1, 8, 64), torch.zeros(1, 1, 8, 64))
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "io_aware_exact_fwd_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, fn), encoding="utf-8").read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", src, re.M), fn
+                assert "oracle/" not in src, fn
