@@ -56,6 +56,36 @@ def load_peaks():
             "source": "fallback"}
 
 
+def profile_traffic(profile: str, source: str):
+    """DRAM bytes per launch from a committed ncu summary, or None.
+
+    The summary records the sha256 prefix of the kernel source it was captured
+    from; if that source has changed since, the counters no longer describe the
+    kernel and None is returned.
+    """
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", profile)
+    if not os.path.exists(path):
+        return None
+    meta = {}
+    for line in open(path):
+        if ":" in line and not line.startswith(("|", "#", " ")):
+            key, _, val = line.partition(":")
+            meta[key.strip()] = val.strip()
+    want = meta.get("kernel_source_sha256_16")
+    src = os.path.join(ROOT, meta.get("kernel_source", source))
+    if not want or not os.path.exists(src):
+        return None
+    have = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if have != want:
+        return None
+    try:
+        return float(meta["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
         os.environ.get("LOCAL_RANK", "0"))
@@ -64,7 +94,7 @@ def dist_env():
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -83,6 +113,9 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    def mark(self, which: str):
+        setattr(self, which, time.time())
+
     def stop(self):
         if self.proc is None:
             return None
@@ -94,11 +127,17 @@ class ClockSampler:
         self.fh.close()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+
+        t0, t1 = getattr(self, "t0", None), getattr(self, "t1", None)
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if t0 is not None and t1 is not None and not (t0 <= ts <= t1):
+                    continue  # outside the timed region
                 sm.append(float(parts[1]))
                 mx.append(float(parts[2]))
             except ValueError:
@@ -154,12 +193,16 @@ def run_ours(args):
         sampler.start()
         time.sleep(0.3)
     t_wall0 = time.perf_counter()
+    if sampler:
+        sampler.mark("t0")
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
         step()
         ends[i].record(stream)
     torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t1")
     t_wall = time.perf_counter() - t_wall0
     clocks = sampler.stop() if sampler else None
     fa.fa_sync_check()
@@ -214,7 +257,10 @@ def run_ours(args):
     roofline = {
         "bound": "tensor", "kernel": "fwd_bf16_kernel<128,false>", "achieved": round(kernel_tflops, 1),
         "peak": peak, "peak_source": f"{peaks['source']} bf16_tflops (burst, cuBLAS)", "unit": "TFLOP/s",
-        "frac": round(kernel_tflops / peak, 4), "traffic": args.traffic,
+        "frac": round(kernel_tflops / peak, 4),
+        "traffic": args.traffic if args.traffic is not None else profile_traffic(
+            "fwd_bf16_B4H16N2048d128.md", "io_aware_exact_fwd_gb300/csrc/fa_fwd.cu"),
+        "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
         "algorithmic_flops_per_launch": flops_step,
     }
     cpu = None
@@ -319,7 +365,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -85,6 +85,38 @@ FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* l
            int causal, float scale, fa_stream_t stream);
 
 /*
+ * fa_bwd_workspace_size -- bytes of device workspace fa_bwd needs for these
+ * sizes (0 if the sizes are invalid or unsupported).  The workspace holds an
+ * fp32 dQ accumulator [B, H, N, d] and two fp32 vectors of B*H*roundup(N, 64).
+ */
+FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * fa_bwd -- bf16 backward pass of fa_fwd, d = 128.
+ * The gradient follows from the chain rule applied to the definition above
+ * (the pages give the forward only): with P = softmax(scale * Q K^T [+mask]),
+ *     dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,
+ *     dS = P * (dP - D),  dQ = scale * dS K,  dK = scale * dS^T Q.
+ * P is recomputed from `lse` (as written by fa_fwd for the same q, k, scale,
+ * causal); the N x N matrices are never stored.
+ *   q, k, v, o, dout : const bf16 [B, H, N, d]   (o, lse: the forward's outputs)
+ *   lse              : const float [B, H, N]
+ *   dq, dk, dv       : bf16 [B, H, N, d]          (outputs, fully overwritten)
+ *   workspace        : device memory of at least fa_bwd_workspace_size(...)
+ *                      bytes, 256-byte aligned, owned by the caller; its
+ *                      contents on entry do not matter and are scratch after.
+ * Numerics: fp32 accumulation on the tensor cores; P and dS are rounded to
+ * bf16 as MMA operands; dQ accumulates across key blocks with fp32 atomic adds,
+ * so dQ may differ in the last bits from run to run (dK, dV do not).
+ * Errors: as fa_fwd; additionally FA_ERR_UNSUPPORTED for d != 128 and
+ * FA_ERR_WORKSPACE for a missing or short workspace; the workspace must be
+ * 256-byte aligned (FA_ERR_MISALIGNED otherwise).
+ */
+FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
+                  int causal, float scale, fa_stream_t stream);
+
+/*
  * fa_sync_check -- synchronise `stream`, then report device-detected errors.
  * Returns FA_ERR_CUDA if the stream or a prior launch failed, FA_ERR_TIMEOUT
  * if any kernel of this library on the current device expired a bounded wait

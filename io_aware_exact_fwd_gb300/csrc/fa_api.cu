@@ -163,6 +163,49 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   return fa::launch_fwd_bf16(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (validate_shape(B, H, N, d, 0, 1.f) != FA_OK || d != 128) return 0;
+  return fa::bwd_workspace_layout(B, H, N, d).total;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
+           void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d, int causal, float scale,
+           fa_stream_t stream) {
+  const int vs = validate_shape(B, H, N, d, causal, scale);
+  if (vs < 0) return FA_OK;
+  if (vs != FA_OK) return vs;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!workspace) return FA_ERR_WORKSPACE;
+  if (ws_bytes < fa::bwd_workspace_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
+    return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  const int st = device_state(&ds);
+  if (st != FA_OK) return st;
+  fa::BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.workspace = workspace;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.err_word = ds->err_word;
+  a.dbg = knobs();
+  return fa::launch_bwd_bf16(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_sync_check(fa_stream_t stream) {
   DeviceState* ds = nullptr;
   const int st = device_state(&ds);

@@ -1,0 +1,528 @@
+// Exact attention backward, bf16, d = 128, for sm_103a.
+//
+// The pages describe only the forward ("FlashAttention-2 (DE)", "Hintergrund";
+// "FlashAttention-Skalierung ...", section 1).  The backward follows from the
+// chain rule applied to the same definition, recomputing P from the forward's
+// per-row logsumexp instead of storing the N x N matrix (the same IO-aware
+// idea applied to the gradient):
+//
+//   P_ij  = exp(scale * q_i . k_j - LSE_i)            (0 where masked)
+//   dV    = P^T dO          dP = dO V^T
+//   D_i   = sum_c dO_ic O_ic = sum_j P_ij dP_ij
+//   dS    = P * (dP - D)    dQ = scale * dS K          dK = scale * dS^T Q
+//
+// Three launches on one stream:
+//  1. bwd_preprocess: D_i, LSE_i * log2(e) (padded rows get +inf so their P is
+//     exactly 0), and zeroing of the fp32 dQ accumulator.
+//  2. bwd_main: one CTA per (128-key block, head), the K/V-outer loop order.
+//     K_j, V_j stay in shared memory; Q_i, dO_i (64 query rows), LSE_i and D_i
+//     stream through a TMA ring.  Per query block, tcgen05 MMAs compute
+//     S^T = K Q_i^T and dP^T = V dO_i^T into TMEM (keys on TMEM lanes, so one
+//     thread owns one key row), four warps form P^T and dS^T in registers and
+//     write them back to TMEM as bf16 (A operands of dV += P^T dO_i and
+//     dK += dS^T Q_i) and to shared memory (B operand of dQ_i^T = K^T dS^T).
+//     dQ_i^T lands over the consumed S^T buffer; four more warps (one d-row
+//     per thread) add it into the fp32 accumulator with coalesced reductions.
+//     TMEM: dV, dK (128 columns each) + S^T, dP^T double-buffered (64 each).
+//  3. bwd_dq_convert: dQ = bf16(scale * dQacc).
+#include <math.h>
+
+#include "fa_device.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBkB = 128;       // keys per CTA
+constexpr int kBqB = 64;        // query rows per inner step
+constexpr int kThreads = 384;   // 0-3 compute, 4-7 dQ reduction, 8 TMA, 9 MMA, 10-11 spare
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+constexpr int kStages = 3;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+// Launch budget 168 x 384 registers: compute warpgroup 224 (two 64-wide score
+// rows live), dQ warpgroup keeps 168, control warpgroup (TMA, MMA) gives back to 112.
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kRegsCompute = 224;
+constexpr uint32_t kRegsControl = 112;
+static_assert(128 * (kRegsCompute + kLaunchRegs + kRegsControl) <= kLaunchRegs * kThreads, "register split");
+
+enum : uint32_t {
+  kSiteBLoad = 0x111,
+  kSiteBMmaKV = 0x211,
+  kSiteBMmaQ = 0x212,
+  kSiteBMmaC = 0x213,
+  kSiteBMmaDq = 0x214,
+  kSiteBComp = 0x311,
+  kSiteBDq = 0x312,
+  kSiteBEpi = 0x313,
+};
+
+struct BwdCfg {
+  static constexpr int kKVBox = kBkB * 64 * 2;          // 16 KB: 128 rows x 128 B
+  static constexpr int kKVTile = kBkB * kD * 2;         // 32 KB
+  static constexpr int kQBox = kBqB * 64 * 2;           // 8 KB: 64 rows x 128 B
+  static constexpr int kQTile = kBqB * kD * 2;          // 16 KB
+  static constexpr int kStageQ = 0;
+  static constexpr int kStageDO = kQTile;
+  static constexpr int kStageL = 2 * kQTile;            // 64 floats
+  static constexpr int kStageD = 2 * kQTile + 256;      // 64 floats
+  static constexpr int kStageTx = 2 * kQTile + 512;     // bytes landing per stage
+  static constexpr int kStageBytes = 34816;             // kStageTx rounded up to 1024
+  static constexpr int kDsBytes = kBkB * kBqB * 2;      // 16 KB: 128 key rows x 128 B
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKVTile;
+  static constexpr int kRingOff = 2 * kKVTile;
+  static constexpr int kDsOff = kRingOff + kStages * kStageBytes;
+  static constexpr int kBarOff = kDsOff + 2 * kDsBytes;
+  // kv, full[S], empty[S], sdp[2], comp[2], dqf[2], dqe[2], dkv, epi, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  // TMEM columns
+  static constexpr uint32_t kColDV = 0, kColDK = 128;
+  static __device__ __forceinline__ uint32_t col_s(int b) { return 256u + 64u * b; }
+  static __device__ __forceinline__ uint32_t col_dp(int b) { return 384u + 64u * b; }
+};
+static_assert(BwdCfg::kStageTx <= BwdCfg::kStageBytes, "stage layout");
+static_assert(BwdCfg::kSmemBytes <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ bool warp_wait_b(uint64_t* bar, uint32_t parity, const WaitCtl& wc, uint32_t site) {
+  const bool ok = mbar_wait(bar, parity, wc, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Stage the 128 x 128 fp32 accumulator row of this thread as bf16 into a
+// 128-byte-swizzled [128 rows][64 cols] x 2 TMA box pair.
+__device__ __forceinline__ void stage_row_bf16(uint32_t taddr_row, uint8_t* boxes, int row, float mul) {
+#pragma unroll 1
+  for (int c = 0; c < kD / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(taddr_row + c * 32, o);
+    tmem_ld_wait32(o);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * mul, __uint_as_float(o[2 * i + 1]) * mul);
+    uint8_t* box = boxes + (c / 2) * BwdCfg::kKVBox + row * 128;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int chunk = (c % 2) * 4 + q4;
+      *reinterpret_cast<uint4*>(box + ((chunk ^ (row & 7)) * 16)) =
+          make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+    }
+  }
+}
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                    const float* __restrict__ lse2, const float* __restrict__ dvec, float* __restrict__ dq_acc,
+                    int N, int Npad, int BH, int nkb, float scale, float scale_log2, unsigned int* err_word,
+                    unsigned long long wait_ns) {
+  using C = BwdCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem + C::kKOff;
+  uint8_t* sV = smem + C::kVOff;
+  uint8_t* sRing = smem + C::kRingOff;
+  uint8_t* sDs = smem + C::kDsOff;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* bar_kv = bars;
+  uint64_t* bar_full = bars + 1;
+  uint64_t* bar_empty = bar_full + kStages;
+  uint64_t* bar_sdp = bar_empty + kStages;  // [2]
+  uint64_t* bar_comp = bar_sdp + 2;         // [2]
+  uint64_t* bar_dqf = bar_comp + 2;         // [2] dQ^T ready in TMEM
+  uint64_t* bar_dqe = bar_dqf + 2;          // [2] dQ^T read out of TMEM
+  uint64_t* bar_dkv = bar_dqe + 2;
+  uint64_t* bar_epi = bar_dkv + 1;
+  uint64_t* bar_drain = bar_epi + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int kb, bh;
+  if (CAUSAL) {  // key blocks near the start see the most query blocks: issue them first
+    kb = static_cast<int>(blockIdx.x) / BH;
+    bh = static_cast<int>(blockIdx.x) % BH;
+  } else {
+    kb = static_cast<int>(blockIdx.x) % nkb;
+    bh = static_cast<int>(blockIdx.x) / nkb;
+  }
+  const int nqb = (N + kBqB - 1) / kBqB;
+  const int i0 = CAUSAL ? (kb * kBkB) / kBqB : 0;
+  const int n = nqb - i0;  // >= 1: query row kb*128 < N exists
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_sdp[b], 1);
+      mbar_init(&bar_comp[b], 4);
+      mbar_init(&bar_dqf[b], 1);
+      mbar_init(&bar_dqe[b], 4);
+    }
+    mbar_init(bar_dkv, 1);
+    mbar_init(bar_epi, 4);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, err_word, wait_ns};
+  const float* lse2_h = lse2 + static_cast<size_t>(bh) * Npad;
+  const float* dvec_h = dvec + static_cast<size_t>(bh) * Npad;
+
+  if (warp >= 8) {
+   regs_decrease<kRegsControl>();
+   if (warp == kWarpLoad) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_kv, 2 * C::kKVTile);
+      for (int b = 0; b < 2; ++b) {
+        tma_load_3d(sK + b * C::kKVBox, &tm_k, bar_kv, b * 64, kb * kBkB, bh);
+        tma_load_3d(sV + b * C::kKVBox, &tm_v, bar_kv, b * 64, kb * kBkB, bh);
+      }
+      int issued = 0;
+      for (int it = 0; it < n; ++it) {
+        const int slot = it % kStages;
+        if (!mbar_wait(&bar_empty[slot], ((it / kStages) & 1) ^ 1, wc, kSiteBLoad)) break;
+        const int i = i0 + it;
+        uint8_t* st = sRing + slot * C::kStageBytes;
+        mbar_arrive_expect_tx(&bar_full[slot], C::kStageTx);
+        for (int b = 0; b < 2; ++b) {
+          tma_load_3d(st + C::kStageQ + b * C::kQBox, &tm_q, &bar_full[slot], b * 64, i * kBqB, bh);
+          tma_load_3d(st + C::kStageDO + b * C::kQBox, &tm_do, &bar_full[slot], b * 64, i * kBqB, bh);
+        }
+        bulk_load(st + C::kStageL, lse2_h + i * kBqB, kBqB * 4, &bar_full[slot]);
+        bulk_load(st + C::kStageD, dvec_h + i * kBqB, kBqB * 4, &bar_full[slot]);
+        ++issued;
+      }
+      if (issued < n) {  // aborted: let the copies already in flight land
+        mbar_wait_drain(bar_kv, 0, wait_ns);
+        for (int t = max(0, issued - kStages); t < issued; ++t)
+          mbar_wait_drain(&bar_full[t % kStages], (t / kStages) & 1, wait_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_sdp = idesc_bf16_f32(kBkB, kBqB, 0, 0);   // keys x queries, K = d
+      constexpr uint32_t idesc_dkv = idesc_bf16_f32(kBkB, kD, 0, 1);     // keys x d, K = queries
+      constexpr uint32_t idesc_dq = idesc_bf16_f32(kD, kBqB, 1, 1);      // d x queries, K = keys
+      const uint64_t k_kmaj = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t v_kmaj = sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t k_mn = sdesc_sw128(smem_u32(sK), C::kKVBox, 1024);
+      const uint64_t ring_kmaj = sdesc_sw128(smem_u32(sRing), 16, 1024);
+      const uint64_t ring_mn = sdesc_sw128(smem_u32(sRing), C::kQBox, 1024);
+      const uint64_t ds_mn = sdesc_sw128(smem_u32(sDs), 16, 1024);
+      bool ok = mbar_wait(bar_kv, 0, wc, kSiteBMmaKV);
+
+      // S^T = K Q_i^T and dP^T = V dO_i^T for local step `it` into buffer it & 1.
+      auto issue_sdp = [&](int it) -> bool {
+        const int slot = it % kStages;
+        const int b = it & 1;
+        if (!mbar_wait(&bar_full[slot], (it / kStages) & 1, wc, kSiteBMmaQ)) return false;
+        if (it >= 2 && !mbar_wait(&bar_dqe[b], ((it - 2) >> 1) & 1, wc, kSiteBMmaDq)) return false;
+        tc_fence_after();
+        const uint32_t st = slot * C::kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
+          const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
+          mma_bf16_ss(tmem + C::col_s(b), sdesc_add(k_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageQ + offb),
+                      idesc_sdp, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
+          const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
+          mma_bf16_ss(tmem + C::col_dp(b), sdesc_add(v_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageDO + offb),
+                      idesc_sdp, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_sdp[b]);
+        return true;
+      };
+
+      if (ok) ok = issue_sdp(0);
+      for (int it = 0; ok && it < n; ++it) {
+        const int b = it & 1;
+        const int slot = it % kStages;
+        if (it + 1 < n && !(ok = issue_sdp(it + 1))) break;
+        if (!(ok = mbar_wait(&bar_comp[b], (it >> 1) & 1, wc, kSiteBMmaC))) break;
+        tc_fence_after();
+        const uint32_t st = slot * C::kStageBytes;
+        // dV += P^T dO_i ; dK += dS^T Q_i   (A from TMEM, B MN-major: 16 query rows per MMA)
+#pragma unroll
+        for (int kk = 0; kk < kBqB / 16; ++kk)
+          mma_bf16_ts(tmem + C::kColDV, tmem + C::col_s(b) + kk * 8,
+                      sdesc_add(ring_mn, st + C::kStageDO + kk * 2048), idesc_dkv, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kBqB / 16; ++kk)
+          mma_bf16_ts(tmem + C::kColDK, tmem + C::col_dp(b) + kk * 8,
+                      sdesc_add(ring_mn, st + C::kStageQ + kk * 2048), idesc_dkv, (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar_empty[slot]);
+        // dQ_i^T = K^T dS^T : A = K MN-major (d contiguous), B = dS^T rows of 64 queries; 16 keys per MMA.
+#pragma unroll
+        for (int kk = 0; kk < kBkB / 16; ++kk)
+          mma_bf16_ss(tmem + C::col_s(b), sdesc_add(k_mn, kk * 2048), sdesc_add(ds_mn, b * C::kDsBytes + kk * 2048),
+                      idesc_dq, kk > 0 ? 1u : 0u);
+        mma_commit(&bar_dqf[b]);
+      }
+      if (ok) mma_commit(bar_dkv);
+      mma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0, wait_ns);
+    }
+    __syncwarp();
+   }
+  } else if (warp < 4) {
+    regs_increase<kRegsCompute>();
+    // ------------------------------------- P and dS (one key row per thread)
+    const int row = threadIdx.x;
+    const int key = kb * kBkB + row;
+    const bool key_valid = key < N;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    bool ok = true;
+    for (int it = 0; it < n; ++it) {
+      const int b = it & 1;
+      const int slot = it % kStages;
+      const int i = i0 + it;
+      if (!(ok = warp_wait_b(&bar_sdp[b], (it >> 1) & 1, wc, kSiteBComp))) break;
+      if (!(ok = warp_wait_b(&bar_full[slot], (it / kStages) & 1, wc, kSiteBComp))) break;
+      tc_fence_after();
+      uint32_t s[2][32], dp[2][32];
+      tmem_ld32(trow + C::col_s(b), s[0]);
+      tmem_ld32(trow + C::col_s(b) + 32, s[1]);
+      tmem_ld32(trow + C::col_dp(b), dp[0]);
+      tmem_ld32(trow + C::col_dp(b) + 32, dp[1]);
+      tmem_ld_wait32(s[0]);
+      tmem_ld_wait32(s[1]);
+      tmem_ld_wait32(dp[0]);
+      tmem_ld_wait32(dp[1]);
+      const uint8_t* st = sRing + slot * C::kStageBytes;
+      const float4* l4 = reinterpret_cast<const float4*>(st + C::kStageL);
+      const float4* d4 = reinterpret_cast<const float4*>(st + C::kStageD);
+      const bool diag = CAUSAL && (i * kBqB < kb * kBkB + kBkB);  // some query in this block precedes a key
+      uint8_t* ds_row = sDs + b * C::kDsBytes + row * 128;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t ppk[16], dpk[16];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const float4 lv = l4[h * 8 + g];
+          const float4 dv = d4[h * 8 + g];
+          const float lz[4] = {lv.x, lv.y, lv.z, lv.w};
+          const float dz[4] = {dv.x, dv.y, dv.z, dv.w};
+          float p[4], ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = g * 4 + e;
+            const int q = i * kBqB + h * 32 + c;
+            float pe = ex2_approx(fmaf(__uint_as_float(s[h][c]), scale_log2, -lz[e]));
+            const bool masked = !key_valid || (diag && key > q);
+            pe = masked ? 0.f : pe;
+            p[e] = pe;
+            ds[e] = pe * (__uint_as_float(dp[h][c]) - dz[e]);
+          }
+          ppk[2 * g] = pack_bf16x2(p[0], p[1]);
+          ppk[2 * g + 1] = pack_bf16x2(p[2], p[3]);
+          dpk[2 * g] = pack_bf16x2(ds[0], ds[1]);
+          dpk[2 * g + 1] = pack_bf16x2(ds[2], ds[3]);
+        }
+        tmem_st16(trow + C::col_s(b) + h * 16, ppk);
+        tmem_st16(trow + C::col_dp(b) + h * 16, dpk);
+        // dS row into shared memory, 128-byte swizzle: chunk ch holds queries 8ch..8ch+7.
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int ch = h * 4 + c4;
+          *reinterpret_cast<uint4*>(ds_row + ((ch ^ (row & 7)) * 16)) =
+              make_uint4(dpk[4 * c4], dpk[4 * c4 + 1], dpk[4 * c4 + 2], dpk[4 * c4 + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_comp[b]);
+    }
+    // ---------------------------------------------------------- dK, dV epilogue
+    if (ok) ok = warp_wait_b(bar_dkv, 0, wc, kSiteBEpi);
+    if (ok) {
+      tc_fence_after();
+      stage_row_bf16(trow + C::kColDV, sV, row, 1.f);
+      stage_row_bf16(trow + C::kColDK, sK, row, scale);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_epi);
+      if (threadIdx.x == 0 && mbar_wait(bar_epi, 0, wc, kSiteBEpi)) {
+        for (int b = 0; b < 2; ++b) {
+          tma_store_3d(&tm_dv, sV + b * C::kKVBox, b * 64, kb * kBkB, bh);
+          tma_store_3d(&tm_dk, sK + b * C::kKVBox, b * 64, kb * kBkB, bh);
+        }
+        tma_store_commit_and_wait_read();
+      }
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // -------------------------------- dQ reduction (one d-row of dQ^T per thread)
+    const int dcol = threadIdx.x - 128;
+    const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    for (int it = 0; it < n; ++it) {
+      const int b = it & 1;
+      if (!warp_wait_b(&bar_dqf[b], (it >> 1) & 1, wc, kSiteBDq)) break;
+      tc_fence_after();
+      uint32_t v[2][32];
+      tmem_ld32(trow + C::col_s(b), v[0]);
+      tmem_ld32(trow + C::col_s(b) + 32, v[1]);
+      tmem_ld_wait32(v[0]);
+      tmem_ld_wait32(v[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_dqe[b]);
+      const int q0 = (i0 + it) * kBqB;
+      float* dst = dq_acc + (static_cast<size_t>(bh) * N + q0) * kD + dcol;
+      const int lim = min(kBqB, N - q0);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (h * 32 + c < lim) atomicAdd(dst + static_cast<size_t>(h * 32 + c) * kD, __uint_as_float(v[h][c]));
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// D_i = sum_c dO_ic O_ic ; LSE2_i = LSE_i * log2(e) (rows >= N: D = 0, LSE2 = +inf);
+// dQacc rows < N are zeroed.  16 threads per row, 8 elements each.
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
+                                                             const __nv_bfloat16* __restrict__ dout,
+                                                             const float* __restrict__ lse, float* __restrict__ dvec,
+                                                             float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                             int N, int Npad, long long rows_pad) {
+  const long long r = static_cast<long long>(blockIdx.x) * 16 + (threadIdx.x >> 4);
+  const int t = threadIdx.x & 15;
+  if (r >= rows_pad) return;
+  const long long bh = r / Npad;
+  const int nrow = static_cast<int>(r - bh * Npad);
+  float acc = 0.f;
+  if (nrow < N) {
+    const size_t base = (static_cast<size_t>(bh) * N + nrow) * kD + t * 8;
+    const uint4 ov = *reinterpret_cast<const uint4*>(o + base);
+    const uint4 gv = *reinterpret_cast<const uint4*>(dout + base);
+    const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
+    const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 a = __bfloat1622float2(op[e]);
+      const float2 g = __bfloat1622float2(gp[e]);
+      acc = fmaf(a.x, g.x, acc);
+      acc = fmaf(a.y, g.y, acc);
+    }
+    float4* z = reinterpret_cast<float4*>(dq_acc + base);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int m = 8; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m, 16);
+  if (t == 0) {
+    dvec[r] = nrow < N ? acc : 0.f;
+    lse2[r] = nrow < N ? lse[static_cast<size_t>(bh) * N + nrow] * kLog2e : INFINITY;
+  }
+}
+
+// dQ = bf16(scale * dQacc), 8 elements per thread.
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ dq_acc,
+                                                             __nv_bfloat16* __restrict__ dq, float scale,
+                                                             long long n8) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * idx];
+  const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * idx + 1];
+  uint4 out;
+  out.x = pack_bf16x2(a.x * scale, a.y * scale);
+  out.y = pack_bf16x2(a.z * scale, a.w * scale);
+  out.z = pack_bf16x2(b.x * scale, b.y * scale);
+  out.w = pack_bf16x2(b.z * scale, b.w * scale);
+  reinterpret_cast<uint4*>(dq)[idx] = out;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
+  BwdWorkspace w{};
+  const size_t bh = static_cast<size_t>(B) * H;
+  const size_t npad = (static_cast<size_t>(N) + kBqB - 1) / kBqB * kBqB;
+  w.npad = static_cast<int>(npad);
+  w.off_dq = 0;
+  w.off_d = align256(bh * N * d * sizeof(float));
+  w.off_lse2 = w.off_d + align256(bh * npad * sizeof(float));
+  w.total = w.off_lse2 + align256(bh * npad * sizeof(float));
+  return w;
+}
+
+cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg;
+  const int BH = a.B * a.H;
+  const BwdWorkspace w = bwd_workspace_layout(a.B, a.H, a.N, a.d);
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  float* dq_acc = reinterpret_cast<float*>(ws + w.off_dq);
+  float* dvec = reinterpret_cast<float*>(ws + w.off_d);
+  float* lse2 = reinterpret_cast<float*>(ws + w.off_lse2);
+  cudaError_t e;
+
+  const long long rows_pad = static_cast<long long>(BH) * w.npad;
+  bwd_preprocess_kernel<<<static_cast<unsigned>((rows_pad + 15) / 16), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, dvec, lse2, dq_acc,
+      a.N, w.npad, rows_pad);
+  if ((e = cudaGetLastError())) return e;
+
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  if ((e = make_tmap_3d(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBqB))) return e;
+  if ((e = make_tmap_3d(&tdo, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBqB))) return e;
+  if ((e = make_tmap_3d(&tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBkB))) return e;
+  if ((e = make_tmap_3d(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBkB))) return e;
+  if ((e = make_tmap_3d(&tdk, a.dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBkB))) return e;
+  if ((e = make_tmap_3d(&tdv, a.dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBkB))) return e;
+  auto kern = a.causal ? bwd_main_kernel<true> : bwd_main_kernel<false>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes))) return e;
+  // The register split assumes the block launches with kLaunchRegs per thread.
+  cudaFuncAttributes fattr;
+  if ((e = cudaFuncGetAttributes(&fattr, kern))) return e;
+  if (static_cast<uint32_t>(fattr.numRegs) < kLaunchRegs) return cudaErrorInvalidConfiguration;
+  const int nkb = (a.N + kBkB - 1) / kBkB;
+  kern<<<static_cast<unsigned>(nkb * BH), kThreads, C::kSmemBytes, stream>>>(
+      tq, tk, tv, tdo, tdk, tdv, lse2, dvec, dq_acc, a.N, w.npad, BH, nkb, a.scale, a.scale * kLog2e, a.err_word,
+      a.dbg.wait_limit_ns);
+  if ((e = cudaGetLastError())) return e;
+
+  const long long n8 = static_cast<long long>(BH) * a.N * kD / 8;
+  bwd_dq_convert_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
+      dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.scale, n8);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -3,27 +3,30 @@
 // Method ("FlashAttention-Skalierung, Multi-GPU-Training und
 // Gewichtsquantisierung", section 1; "FlashAttention-2 (DE)", sections
 // "Hintergrund" and "Technische Architektur und Funktionsprinzipien"): the
-// N x N score matrix is never materialised.  Each CTA owns one block of 128
-// query rows (outer loop over Q blocks) and streams the K/V blocks of its head
-// through shared memory (inner loop), keeping a running row maximum m and row
-// sum l (online softmax).  The single division by l happens once, after the
-// inner loop.
+// N x N score matrix is never materialised.  Each CTA owns query rows of one
+// head (outer loop over Q blocks, parallel over the sequence as well as over
+// batch and heads) and streams the K/V blocks of that head through shared
+// memory (inner loop), keeping a running row maximum m and row sum l (online
+// softmax).  The single division by l happens once, after the inner loop.
 //
 // GB300 mapping of the pages' ideas:
-//  * TMA copies (asynchronous copy unit, FlashAttention-3 bullet "Asynchrone
-//    Datenübertragung") move Q once and K_j, V_j through a ring of
-//    shared-memory slots guarded by full/empty mbarriers.
-//  * Warp specialisation (bullet "Warp-Spezialisierung"): warp 4 issues TMA,
-//    one thread of warp 5 issues tcgen05 MMAs, warps 0-3 run the softmax (one
-//    thread per query row = one TMEM lane), so the exponentials of block j
-//    overlap the tensor-core work of blocks j-1 (P V) and j+1 (Q K^T).
-//  * S = Q K_j^T accumulates in TMEM (two buffers, alternating); P is written
-//    back over its own S buffer as packed bf16 and fed to the P V MMA straight
-//    from TMEM, so P never touches shared memory.
-//  * The O accumulator stays in TMEM for the whole inner loop.  It is rescaled
-//    only when a row maximum grows by more than 2^8 ("rescale as late as
-//    possible"): until then exponentials are taken against the stale maximum,
-//    which keeps O and l consistent and the final O/l exact.
+//  * TMA copies ("Asynchrone Datenübertragung (TMA)") move the Q tiles once and
+//    K_j, V_j through a ring of shared-memory slots guarded by full/empty
+//    mbarriers.
+//  * Warp specialisation ("Warp-Spezialisierung"): warp 8 issues TMA, one thread
+//    of warp 9 issues tcgen05 MMAs, and two softmax warpgroups (warps 0-3 and
+//    4-7, one thread per query row = one TMEM lane) each own one of the CTA's
+//    two 128-row query tiles.  While one warpgroup exponentiates its scores the
+//    tensor core runs the other tile's P V and Q K^T ("Nahtloses Interleaving von
+//    Operationen" on the FlashAttention-3 page: matmul and softmax overlap).
+//  * Per tile, S = Q K_j^T accumulates in TMEM; P is written back over S as packed
+//    bf16 and feeds the P V MMA straight from TMEM, so P never touches shared
+//    memory.  TMEM holds S_a, S_b (128 columns each) and O_a, O_b (d columns
+//    each): all 512 columns at d = 128.
+//  * The O accumulators stay in TMEM for the whole inner loop.  O is rescaled only
+//    when a row maximum grows by more than 2^8 ("rescale only at the very end"
+//    taken one step further): until then exponentials are taken against the
+//    stale maximum, which keeps O and l consistent and the final O/l exact.
 //
 // Every mbarrier wait is bounded (see fa_device.cuh); on expiry the CTA sets a
 // device error word, drains its own in-flight copies, frees TMEM and exits.
@@ -35,9 +38,18 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 192;          // warps 0-3 softmax + epilogue, warp 4 TMA, warp 5 MMA
-constexpr int kWarpLoad = 4;
-constexpr int kWarpMma = 5;
+constexpr int kTiles = 2;                       // query tiles per CTA
+constexpr int kRowsPerCta = kTiles * kBlockQ;   // 256 query rows
+constexpr int kThreads = 384;                   // warps 0-7 softmax (2 groups), 8 TMA, 9 MMA, 10-11 spare
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+// Launch budget: 168 registers x 384 threads.  Softmax warpgroups take 216 each
+// (128 live scores per thread), the TMA/MMA warpgroup gives back down to 72:
+// 2 x 128 x 216 + 128 x 72 = 168 x 384.
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsControl = 72;
+constexpr uint32_t kRegsNeeded = 2 * 128 * kRegsSoftmax + 128 * kRegsControl;
+static_assert(kRegsNeeded <= 65536, "register split exceeds the SM register file");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: stale-max exponentials stay <= 256
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -59,17 +71,16 @@ struct FwdCfg {
   static constexpr int kBoxes = D / kBoxCols;
   static constexpr int kBoxBytes = kBlockK * kBoxCols * 2;  // 16 KB: 128 rows x 128 bytes
   static constexpr int kTileBytes = kBlockK * D * 2;        // one Q, K or V tile
-  static constexpr int kSlots = D == 128 ? 5 : 8;
-  static constexpr int kQOff = 0;
-  static constexpr int kRingOff = kTileBytes;
+  static constexpr int kSlots = D == 128 ? 4 : 8;
+  static constexpr int kQOff = 0;                           // Q_a, Q_b
+  static constexpr int kRingOff = kTiles * kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
-  // q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], o_done[2], epi, drain
-  static constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 2 + 1 + 1;
+  // q_full[2], full[kSlots], empty[kSlots], s_full[2], p_full[2], o_done[2], epi[2], drain
+  static constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
-  static constexpr uint32_t kColSBase = 0;  // S buffer b occupies columns [128*b, 128*b + 128)
-  static constexpr uint32_t kColO = 256;
-  static __device__ __forceinline__ uint32_t col_s(int b) { return kColSBase + 128u * static_cast<uint32_t>(b); }
+  static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * static_cast<uint32_t>(t); }
+  static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + D * static_cast<uint32_t>(t); }
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc, uint32_t site) {
@@ -77,11 +88,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
+// Number of K/V blocks query tile t of work unit u attends to (0 if the tile is past N).
+template <bool CAUSAL>
+__device__ __forceinline__ int kv_blocks(int u, int t, int N) {
+  const int row0 = u * kRowsPerCta + t * kBlockQ;
+  if (row0 >= N) return 0;
+  const int nkt_all = (N + kBlockK - 1) / kBlockK;
+  return CAUSAL ? min(row0 / kBlockK + 1, nkt_all) : nkt_all;
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    float* __restrict__ lse, int N, int BH, int nqt, float scale_log2, unsigned int* err_word,
+                    float* __restrict__ lse, int N, int BH, int nunits, float scale_log2, unsigned int* err_word,
                     unsigned long long wait_ns, int fault) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -89,44 +109,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem + C::kQOff;
   uint8_t* sRing = smem + C::kRingOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* bar_q = bars;
-  uint64_t* bar_full = bars + 1;
+  uint64_t* bar_q = bars;                    // [2]
+  uint64_t* bar_full = bars + 2;             // [kSlots]
   uint64_t* bar_empty = bar_full + C::kSlots;
-  uint64_t* bar_s = bar_empty + C::kSlots;
-  uint64_t* bar_p = bar_s + 2;
-  uint64_t* bar_o = bar_p + 2;
-  uint64_t* bar_epi = bar_o + 2;
-  uint64_t* bar_drain = bar_epi + 1;
+  uint64_t* bar_s = bar_empty + C::kSlots;   // [2] per tile: S ready
+  uint64_t* bar_p = bar_s + 2;               // [2] per tile: P written
+  uint64_t* bar_o = bar_p + 2;               // [2] per tile: last P V done
+  uint64_t* bar_epi = bar_o + 2;             // [2] per tile: O staged in shared memory
+  uint64_t* bar_drain = bar_epi + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work unit: (query block, head).  Causal blocks are issued heaviest first.
-  int qt, bh;
+  // Work unit: (256-row query block, head).  Causal blocks are issued heaviest first.
+  int u, bh;
   if (CAUSAL) {
-    qt = nqt - 1 - static_cast<int>(blockIdx.x) / BH;
+    u = nunits - 1 - static_cast<int>(blockIdx.x) / BH;
     bh = static_cast<int>(blockIdx.x) % BH;
   } else {
-    qt = static_cast<int>(blockIdx.x) % nqt;
-    bh = static_cast<int>(blockIdx.x) / nqt;
+    u = static_cast<int>(blockIdx.x) % nunits;
+    bh = static_cast<int>(blockIdx.x) / nunits;
   }
-  const int nkt_all = (N + kBlockK - 1) / kBlockK;
-  const int nkt = CAUSAL ? min(qt + 1, nkt_all) : nkt_all;
+  const int n_a = kv_blocks<CAUSAL>(u, 0, N);
+  const int n_b = kv_blocks<CAUSAL>(u, 1, N);
+  const int n_max = max(n_a, n_b);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(&bar_q[t], 1);
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_p[t], 4);
+      mbar_init(&bar_o[t], 1);
+      mbar_init(&bar_epi[t], 4);
+    }
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar_s[b], 1);
-      mbar_init(&bar_p[b], 4);
-      mbar_init(&bar_o[b], 1);
-    }
-    mbar_init(bar_epi, 4);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -144,14 +165,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, err_word, wait_ns};
 
-  if (warp == kWarpLoad) {
+  if (warp >= 8) {
+   // Control warpgroup: gives registers back to the softmax warpgroups.
+   regs_decrease<kRegsControl>();
+   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, C::kTileBytes);
+      const int nq[kTiles] = {n_a, n_b};
+      for (int t = 0; t < kTiles; ++t) {
+        if (nq[t] == 0) continue;
+        mbar_arrive_expect_tx(&bar_q[t], C::kTileBytes);
 #pragma unroll
-      for (int b = 0; b < C::kBoxes; ++b) tma_load_3d(sQ + b * C::kBoxBytes, &tm_q, bar_q, b * kBoxCols, qt * kBlockQ, bh);
-
-      // Ring order = MMA consumption order: K0, K1, V0, K2, V1, ..., K_{n-1}, V_{n-2}, V_{n-1}.
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_3d(sQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, &bar_q[t], b * kBoxCols,
+                      u * kRowsPerCta + t * kBlockQ, bh);
+      }
+      // Ring order = MMA first-use order: K0, V0, K1, V1, ...
       int issued = 0;
       bool ok = true;
       auto push = [&](const CUtensorMap* tm, int j) -> bool {
@@ -167,14 +196,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++issued;
         return true;
       };
-      for (int j = 0; ok && j < nkt; ++j) {
+      for (int j = 0; ok && j < n_max; ++j) {
         ok = push(&tm_k, j);
-        if (ok && j >= 1) ok = push(&tm_v, j - 1);
+        if (ok) ok = push(&tm_v, j);
       }
-      if (ok) ok = push(&tm_v, nkt - 1);
       if (!ok) {
-        // Drain: the last (up to kSlots) issued copies may still be landing in shared memory.
-        mbar_wait_drain(bar_q, 0, wait_ns);
+        // Drain: the Q tiles and the last (up to kSlots) issued copies may still be landing.
+        for (int t = 0; t < kTiles; ++t)
+          if (nq[t] > 0) mbar_wait_drain(&bar_q[t], 0, wait_ns);
         for (int t = max(0, issued - C::kSlots); t < issued; ++t)
           mbar_wait_drain(&bar_full[t % C::kSlots], (t / C::kSlots) & 1, wait_ns);
       }
@@ -187,82 +216,126 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockQ, D, 0, 1);
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t ring_addr = smem_u32(sRing);
-      int t = 0;
-      bool ok = mbar_wait(bar_q, 0, wc, kSiteMmaQ);
-      tc_fence_after();
+      const int nq[kTiles] = {n_a, n_b};
+      int item = 0;  // ring index of the next K or V block to consume
+      bool ok = true;
 
-      // O += P_jj V_jj : A = P from TMEM (K-major, 2 bf16 per column), B = V tile,
-      // MN-major (d contiguous): 8 key rows per 1024-byte swizzle atom (SBO),
-      // 64 d-columns per TMA box (LBO = one box).
-      auto pv = [&](int jj) -> bool {
-        const int sb = jj & 1;
-        if (!mbar_wait(&bar_p[sb], (jj >> 1) & 1, wc, kSiteMmaP)) return false;
-        const int slot = t % C::kSlots;
-        if (!mbar_wait(&bar_full[slot], (t / C::kSlots) & 1, wc, kSiteMmaV)) return false;
-        tc_fence_after();
-        const uint32_t vbase = ring_addr + slot * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBlockK / 16; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, C::kBoxBytes, 1024);
-          mma_bf16_ts(tmem + C::kColO, tmem + C::col_s(sb) + kk * 8, bdesc, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bar_o[sb]);
-        mma_commit(&bar_empty[slot]);
-        ++t;
-        return true;
-      };
+      // Base descriptors; every MMA operand below is one of these advanced by a
+      // compile-time byte offset (a single 32-bit add on the issuing thread).
+      const uint64_t qdesc = sdesc_sw128(q_addr, 16, 1024);          // K-major, SBO = 8 rows x 128 B
+      const uint64_t kdesc = sdesc_sw128(ring_addr, 16, 1024);       // K-major view of a ring slot
+      const uint64_t vdesc = sdesc_sw128(ring_addr, C::kBoxBytes, 1024);  // MN-major view, LBO = one box
 
-      for (int j = 0; ok && j < nkt; ++j) {
-        // S_j = Q K_j^T : both operands K-major (d contiguous), 16 d-columns per MMA.
-        const int slot = t % C::kSlots;
-        if (!mbar_wait(&bar_full[slot], (t / C::kSlots) & 1, wc, kSiteMmaK)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t kbase = ring_addr + slot * C::kTileBytes;
-        const uint32_t sb = j & 1;
+      // S_t = Q_t K^T : both operands K-major (d contiguous), 16 d-columns per MMA.
+      auto qk = [&](int t, int slot) {
+        const uint64_t qd = sdesc_add(qdesc, t * C::kTileBytes);
+        const uint64_t kd = sdesc_add(kdesc, slot * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-          mma_bf16_ss(tmem + C::col_s(sb), sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                      idesc_qk, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + C::col_s(t), sdesc_add(qd, off), sdesc_add(kd, off), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar_s[sb]);
-        mma_commit(&bar_empty[slot]);
-        ++t;
-        if (j >= 1) ok = pv(j - 1);
+        mma_commit(&bar_s[t]);
+      };
+      // O_t += P_t V : A = P from TMEM (2 bf16 per column), B = V tile, MN-major
+      // (d contiguous): 8 key rows per 1024-byte swizzle atom (SBO), 64 d-columns
+      // per TMA box (LBO = one box).
+      auto pv = [&](int t, int slot, bool accumulate) {
+        const uint64_t vd = sdesc_add(vdesc, slot * C::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBlockK / 16; ++kk)
+          mma_bf16_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, sdesc_add(vd, kk * 16 * 128), idesc_pv,
+                      (accumulate || kk > 0) ? 1u : 0u);
+      };
+
+      // Prologue: S_a = Q_a K_0^T, S_b = Q_b K_0^T.
+      {
+        const int slot = item % C::kSlots;
+        ok = mbar_wait(&bar_full[slot], (item / C::kSlots) & 1, wc, kSiteMmaK);
+        for (int t = 0; ok && t < kTiles; ++t) {
+          if (nq[t] == 0) continue;
+          ok = mbar_wait(&bar_q[t], 0, wc, kSiteMmaQ);
+          if (!ok) break;
+          tc_fence_after();
+          qk(t, slot);
+        }
+        if (ok) mma_commit(&bar_empty[slot]);
+        ++item;
       }
-      if (ok) pv(nkt - 1);
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int slot_v = item % C::kSlots;
+        ok = mbar_wait(&bar_full[slot_v], (item / C::kSlots) & 1, wc, kSiteMmaV);
+        ++item;
+        if (!ok) break;
+        const bool has_next = j + 1 < n_max;
+        const int slot_k = item % C::kSlots;
+        const uint32_t par_k = (item / C::kSlots) & 1;
+        if (has_next) ++item;
+        bool k_ready = false;
+        for (int t = 0; ok && t < kTiles; ++t) {
+          if (j >= nq[t]) continue;
+          ok = mbar_wait(&bar_p[t], j & 1, wc, kSiteMmaP);
+          if (!ok) break;
+          tc_fence_after();
+          pv(t, slot_v, j > 0);
+          if (j + 1 == nq[t]) mma_commit(&bar_o[t]);
+          if (j + 1 < nq[t]) {
+            if (!k_ready) {
+              ok = mbar_wait(&bar_full[slot_k], par_k, wc, kSiteMmaK);
+              if (!ok) break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            qk(t, slot_k);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bar_empty[slot_v]);
+        if (has_next) {
+          if (!k_ready) {  // no tile needed K_{j+1} (cannot happen for n_max > j + 1, kept for safety)
+            ok = mbar_wait(&bar_full[slot_k], par_k, wc, kSiteMmaK);
+            if (!ok) break;
+          }
+          mma_commit(&bar_empty[slot_k]);
+        }
+      }
       // Every issued MMA must finish before TMEM is released.
       mma_commit(bar_drain);
       mbar_wait_drain(bar_drain, 0, wait_ns);
     }
     __syncwarp();
+   }
   } else {
-    // ------------------------------------------------ softmax warps (0..3)
-    const int row = threadIdx.x;  // tile row == TMEM lane
-    const int qrow = qt * kBlockQ + row;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    regs_increase<kRegsSoftmax>();
+    // -------------------------------------------- softmax warpgroups (0-3, 4-7)
+    const int t = warp >> 2;                 // query tile of this warpgroup
+    const int row = threadIdx.x & 127;       // tile row == TMEM lane
+    const int qrow0 = u * kRowsPerCta + t * kBlockQ;
+    const int qrow = qrow0 + row;
+    const int nkt = t == 0 ? n_a : n_b;
+    const int diag = qrow0 / kBlockK;        // K/V block on this tile's diagonal
+    const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t col_s = C::col_s(t);
+    const uint32_t col_o = C::col_o(t);
+    const float2 c2 = make_float2(scale_log2, scale_log2);
     float m_used = -INFINITY;  // running maximum in log2 units (possibly stale, see header)
     float l = 0.f;
     bool ok = true;
 
     for (int j = 0; j < nkt; ++j) {
-      const int sb = j & 1;
-      if (!warp_wait(&bar_s[sb], (j >> 1) & 1, wc, kSiteSoftS)) {
+      if (!warp_wait(&bar_s[t], j & 1, wc, kSiteSoftS)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t r[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(trow + C::col_s(sb) + c * 32, r[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld32(trow + col_s + c * 32, r[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait32(r[c]);
 
       const int kbase = j * kBlockK;
-      const bool need_mask = (kbase + kBlockK > N) || (CAUSAL && j == qt);
+      const bool need_mask = (kbase + kBlockK > N) || (CAUSAL && j == diag);
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -283,106 +356,99 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx[c] = fmaxf(a, __uint_as_float(r[c][31]));
       }
       const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      const float m_tile = rmax * scale_log2;
-      const float m_new = fmaxf(m_used, m_tile);
+      const float m_new = fmaxf(m_used, rmax * scale_log2);
 
       if (j == 0) {
         m_used = (m_new == -INFINITY) ? 0.f : m_new;
       } else {
         const bool need = m_new > m_used + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
-          // O must hold P_{j-1} V_{j-1} before it is rescaled.
-          const int pj = j - 1;
-          if (!warp_wait(&bar_o[pj & 1], (pj >> 1) & 1, wc, kSiteSoftO)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+          // O_t already holds P V up to block j-1: Q K_j^T was issued after that P V.
           float alpha = 1.f;
           if (need) {
             alpha = ex2_approx(m_used - m_new);
             m_used = m_new;
           }
           l *= alpha;
+          const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
-            tmem_ld32(trow + C::kColO + c * 32, o);
+            tmem_ld32(trow + col_o + c * 32, o);
             tmem_ld_wait32(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(trow + C::kColO + c * 32, o);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+              o[i] = __float_as_uint(v.x);
+              o[i + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(trow + col_o + c * 32, o);
           }
           tmem_st_wait();
         }
       }
 
-      // P = exp2(S * scale * log2(e) - m), packed to bf16 pairs over the S buffer.
-      const float neg_m = -m_used;
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = exp2(S * scale * log2(e) - m), packed to bf16 pairs over the S buffer:
+      // keys 32c..32c+31 become TMEM columns 16c..16c+15 of this tile's S region.
+      const float2 nm2 = make_float2(-m_used, -m_used);
+      float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * i]), scale_log2, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * i + 1]), scale_log2, neg_m));
-          part[c] += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          const float2 x =
+              __ffma2_rn(make_float2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), c2, nm2);
+          const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          part[i & 1] = __fadd2_rn(part[i & 1], p);
+          pk[i] = pack_bf16x2(p.x, p.y);
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) r[c][i] = pk[i];
+        tmem_st16(trow + col_s + c * 16, pk);
       }
-      l += (part[0] + part[1]) + (part[2] + part[3]);
-      // r[0][0..15], r[1][0..15], ... hold 64 packed columns; gather into two stores of 32.
-      uint32_t st0[32], st1[32];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        st0[i] = r[0][i];
-        st0[16 + i] = r[1][i];
-        st1[i] = r[2][i];
-        st1[16 + i] = r[3][i];
-      }
-      tmem_st32(trow + C::col_s(sb), st0);
-      tmem_st32(trow + C::col_s(sb) + 32, st1);
+      const float2 ps = __fadd2_rn(part[0], part[1]);
+      l += ps.x + ps.y;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_p[sb]);
+      if (lane == 0) mbar_arrive(&bar_p[t]);
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && nkt >= 2) ok = warp_wait(&bar_o[(nkt - 2) & 1], ((nkt - 2) >> 1) & 1, wc, kSiteSoftO);
-    if (ok) ok = warp_wait(&bar_o[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1, wc, kSiteSoftO);
-    if (ok) {
+    if (ok && nkt > 0) ok = warp_wait(&bar_o[t], 0, wc, kSiteSoftO);
+    if (ok && nkt > 0) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      // O row -> bf16 -> the Q staging area (free: every Q K^T MMA has completed),
-      // laid out exactly as the 128-byte-swizzled TMA box expects.
+      const float2 il2 = make_float2(inv_l, inv_l);
+      // O row -> bf16 -> this tile's Q staging area (free: its last Q K^T MMA has
+      // completed), laid out exactly as the 128-byte-swizzled TMA box expects.
+      uint8_t* sQt = sQ + t * C::kTileBytes;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(trow + C::kColO + c * 32, o);
+        tmem_ld32(trow + col_o + c * 32, o);
         tmem_ld_wait32(o);
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        uint8_t* box = sQ + (c / 2) * C::kBoxBytes + row * 128;
+        for (int i = 0; i < 16; ++i) {
+          const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2);
+          pk[i] = pack_bf16x2(v.x, v.y);
+        }
+        uint8_t* box = sQt + (c / 2) * C::kBoxBytes + row * 128;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int chunk = (c % 2) * 4 + q4;
-          uint4 val = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          const uint4 val = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
           *reinterpret_cast<uint4*>(box + ((chunk ^ (row & 7)) * 16)) = val;
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_epi);
+      if (lane == 0) mbar_arrive(&bar_epi[t]);
       if (qrow < N) lse[static_cast<size_t>(bh) * N + qrow] = (m_used + log2f(l)) * kLn2;
-      if (threadIdx.x == 0 && mbar_wait(bar_epi, 0, wc, kSiteEpi)) {
+      if (row == 0 && mbar_wait(&bar_epi[t], 0, wc, kSiteEpi)) {
 #pragma unroll
-        for (int b = 0; b < C::kBoxes; ++b) tma_store_3d(&tm_o, sQ + b * C::kBoxBytes, b * kBoxCols, qt * kBlockQ, bh);
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_store_3d(&tm_o, sQt + b * C::kBoxBytes, b * kBoxCols, qrow0, bh);
         tma_store_commit_and_wait_read();
       }
     }
@@ -410,10 +476,15 @@ cudaError_t launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
   auto kern = fwd_bf16_kernel<D, CAUSAL>;
   // Per device and idempotent; cheap enough to repeat on every launch.
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes))) return e;
-  const int nqt = (a.N + kBlockQ - 1) / kBlockQ;
+  // setmaxnreg.inc can only draw on the registers the block was launched with; a
+  // build that allocated fewer per thread than the split assumes would stall.
+  cudaFuncAttributes fattr;
+  if ((e = cudaFuncGetAttributes(&fattr, kern))) return e;
+  if (static_cast<uint32_t>(fattr.numRegs) * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+  const int nunits = (a.N + kRowsPerCta - 1) / kRowsPerCta;
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  dim3 grid(static_cast<unsigned>(nqt * BH));
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a.lse, a.N, BH, nqt, scale_log2, a.err_word,
+  dim3 grid(static_cast<unsigned>(nunits * BH));
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a.lse, a.N, BH, nunits, scale_log2, a.err_word,
                                                    a.dbg.wait_limit_ns, a.dbg.fault);
   return cudaGetLastError();
 }

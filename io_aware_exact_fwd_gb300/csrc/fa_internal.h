@@ -38,6 +38,36 @@ struct FwdArgs {
 // Forward launcher (fa_fwd.cu).  Returns a cudaError_t.
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream);
 
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  void* workspace;
+  int B, H, N, d;
+  int causal;
+  float scale;
+  unsigned int* err_word;
+  DebugKnobs dbg;
+};
+
+// Workspace of the backward: fp32 dQ accumulator [BH, N, d], then D and
+// LSE * log2(e), each [BH, npad] with npad = N rounded up to 64.  Every region
+// starts on a 256-byte boundary.
+struct BwdWorkspace {
+  size_t off_dq, off_d, off_lse2, total;
+  int npad;
+};
+BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d);
+
+// Backward launcher (fa_bwd.cu): preprocess, main, dQ convert on `stream`.
+cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream);
+
 // Encodes a 3-D tiled tensor map over a [BH, N, cols] row-major tensor with
 // `elem_bytes`-byte elements, box {box_cols, box_rows, 1}, 128-byte swizzle.
 // Implemented in fa_api.cu (driver entry point resolved once).
