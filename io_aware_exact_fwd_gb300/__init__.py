@@ -16,7 +16,8 @@ import ctypes
 import os
 
 __all__ = [
-    "FAError", "load_library", "library_path", "fa_fwd", "fa_sync_check", "fa_strerror",
+    "FAError", "load_library", "library_path", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_sync_check",
+    "fa_strerror",
     "fa_version", "fa_last_error_site", "fa_debug_set_wait_limit_ns", "fa_debug_set_fault",
     "STATUS",
 ]
@@ -60,6 +61,10 @@ def load_library():
     lib.fa_version.argtypes = []
     lib.fa_fwd.restype = i
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, f, vp]
     lib.fa_sync_check.restype = i
     lib.fa_sync_check.argtypes = [vp]
     lib.fa_last_error_site.restype = ctypes.c_uint
@@ -130,6 +135,45 @@ def fa_fwd(q, k, v, o=None, lse=None, causal: bool = False, scale: float | None 
                         float(scale), _stream_handle(stream))
     _check(st, "fa_fwd")
     return o, lse
+
+
+def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    """Bytes of device workspace fa_bwd needs (0 if unsupported)."""
+    return int(load_library().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, workspace=None, causal: bool = False,
+           scale: float | None = None, stream=None):
+    """bf16 attention backward (d = 128): returns (dq, dk, dv).
+
+    q, k, v, o, do: bf16 CUDA tensors [B, H, N, d]; lse: fp32 [B, H, N] from fa_fwd
+    with the same causal/scale.  Outputs are allocated if not given; the
+    workspace (uint8 CUDA tensor of fa_bwd_workspace_size bytes) too.
+    """
+    import torch
+
+    lib = load_library()
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_bhnd(name, t, (B, H, N, d), torch.bfloat16)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, N]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_bhnd(name, t, (B, H, N, d), torch.bfloat16)
+    need = int(lib.fa_bwd_workspace_size(B, H, N, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if scale is None:
+        scale = d ** -0.5
+    with torch.cuda.device(q.device):
+        st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                        _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, N, d,
+                        int(bool(causal)), float(scale), _stream_handle(stream))
+    _check(st, "fa_bwd")
+    return dq, dk, dv
 
 
 def fa_sync_check(stream=None):

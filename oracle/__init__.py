@@ -31,6 +31,7 @@ from .attention import (
     attention_forward,
     attention_forward_rows,
     attention_backward,
+    attention_backward_sampled,
 )
 from .brute import attention_forward_brute
 from .fp8 import (
@@ -48,6 +49,7 @@ __all__ = [
     "attention_forward",
     "attention_forward_rows",
     "attention_backward",
+    "attention_backward_sampled",
     "attention_forward_brute",
     "sylvester_hadamard",
     "fwht_f32",

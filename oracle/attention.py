@@ -126,3 +126,46 @@ def attention_backward(q, k, v, do, scale: float, causal: bool, row_chunk: int =
                 dq[b, h, rows] = scale * (ds @ k[b, h])
                 dk[b, h] += scale * (ds.T @ q[b, h, rows])
     return dq, dk, dv
+
+
+def attention_backward_sampled(q_head, k_head, v_head, do_head, scale: float, causal: bool, rows, keys,
+                               row_chunk: int = 1024):
+    """Exact dQ at selected query rows and dK, dV at selected keys of ONE head.
+
+    The same definition as :func:`attention_backward`, evaluated element by
+    element: LSE_i and D_i = sum_j P_ij dP_ij are formed for every row (in row
+    chunks, from complete rows of S), then
+      dQ_i = scale * sum_j P_ij (dP_ij - D_i) k_j      for i in rows
+      dV_j = sum_i P_ij dO_i                            for j in keys
+      dK_j = scale * sum_i P_ij (dP_ij - D_i) q_i       for j in keys
+    with P_ij = exp(scale q_i.k_j - LSE_i) (0 where masked) and dP_ij = dO_i . v_j.
+    Returns (dQ[len(rows), d], dK[len(keys), d], dV[len(keys), d]).
+    """
+    q, k, v, g = (_as_f64(t) for t in (q_head, k_head, v_head, do_head))
+    N = q.shape[0]
+    rows = np.asarray(rows, dtype=np.int64)
+    keys = np.asarray(keys, dtype=np.int64)
+    lse = np.empty(N)
+    dsum = np.empty(N)
+    for r0 in range(0, N, row_chunk):
+        rr = np.arange(r0, min(N, r0 + row_chunk))
+        s = _scores(q[rr], k, rr, scale, causal)
+        p, m, l = _softmax_rows(s)
+        lse[rr] = m + np.log(l)
+        dsum[rr] = (p * (g[rr] @ v.T)).sum(axis=1)
+    # rows of P for dQ
+    s = _scores(q[rows], k, rows, scale, causal)
+    p = np.exp(s - lse[rows][:, None])
+    ds = p * (g[rows] @ v.T - dsum[rows][:, None])
+    dq = scale * (ds @ k)
+    # columns of P for dK, dV
+    allr = np.arange(N)
+    sc = scale * (q @ k[keys].T)                          # [N, len(keys)]
+    if causal:
+        sc = np.where(keys[None, :] > allr[:, None], -np.inf, sc)
+    pc = np.exp(sc - lse[:, None])
+    dpc = g @ v[keys].T
+    dsc = pc * (dpc - dsum[:, None])
+    dv = pc.T @ g
+    dk = scale * (dsc.T @ q)
+    return dq, dk, dv

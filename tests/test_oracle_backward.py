@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import attention_backward, attention_forward
+from oracle import attention_backward, attention_backward_sampled, attention_forward
 from synth import normal_qkv
 
 
@@ -83,3 +83,17 @@ def test_causal_last_key_gets_gradient_only_from_last_query():
     p_last = np.exp(scale * q[0, 0, -1] @ k[0, 0, -1] - lse[0, 0, -1])
     _, _, dv = attention_backward(q, k, v, g, scale, True)
     np.testing.assert_allclose(dv[0, 0, -1], p_last * g[0, 0, -1], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_backward_equals_full_backward(causal):
+    x = normal_qkv(1, 1, 150, 16, seed=26, with_do=True)
+    q, k, v, g = (x[n].numpy().astype(np.float64) for n in ("q", "k", "v", "do"))
+    dq, dk, dv = attention_backward(q, k, v, g, 0.45, causal)
+    rows = [0, 1, 77, 149]
+    keys = [0, 64, 148, 149]
+    sq, sk, sv = attention_backward_sampled(q[0, 0], k[0, 0], v[0, 0], g[0, 0], 0.45, causal, rows, keys,
+                                            row_chunk=37)
+    np.testing.assert_allclose(sq, dq[0, 0, rows], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sk, dk[0, 0, keys], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sv, dv[0, 0, keys], rtol=0, atol=1e-12)
