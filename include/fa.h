@@ -117,6 +117,34 @@ FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, co
                   int causal, float scale, fa_stream_t stream);
 
 /*
+ * fa_bwd_noalloc -- fa_bwd without a caller workspace; allocates nothing.
+ * The pages have no counterpart to this call: it exists for callers that
+ * cannot allocate device memory themselves (a plugin inside a host framework
+ * that owns all device memory and gives plugins no allocator, or a
+ * latency-critical loop where cudaMalloc, which may synchronise the device, is
+ * not allowed).  The caller still passes every input and output exactly as for
+ * fa_bwd; the scratch comes from one fixed buffer per device that the library
+ * holds from the moment it is first used on that device until the process
+ * exits (fa_bwd_noalloc_max_workspace() bytes, 64 MiB).
+ * Limits and behaviour:
+ *  - Sizes whose fa_bwd_workspace_size() exceeds that buffer are rejected with
+ *    FA_ERR_WORKSPACE before anything is launched (at d = 128 this admits about
+ *    B*H*N <= 127,000 rows); other errors are those of fa_bwd.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - The first call on a device looks up the buffer's device address for that
+ *    device; make that first call before any stream capture.
+ *  - Every call on a device shares the one buffer, which keeps the contents of
+ *    the last call (the kernels initialise what must start at zero).  Calls that
+ *    overlap on the GPU (e.g. on two streams at once) race on it: serialise them.
+ */
+FA_API int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                          float scale, fa_stream_t stream);
+
+/* Size in bytes of the fixed scratch buffer behind fa_bwd_noalloc (per device). */
+FA_API size_t fa_bwd_noalloc_max_workspace(void);
+
+/*
  * fa_sync_check -- synchronise `stream`, then report device-detected errors.
  * Returns FA_ERR_CUDA if the stream or a prior launch failed, FA_ERR_TIMEOUT
  * if any kernel of this library on the current device expired a bounded wait

@@ -16,7 +16,8 @@ import ctypes
 import os
 
 __all__ = [
-    "FAError", "load_library", "library_path", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_sync_check",
+    "FAError", "load_library", "library_path", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_noalloc",
+    "fa_bwd_noalloc_max_workspace", "fa_sync_check",
     "fa_strerror",
     "fa_version", "fa_last_error_site", "fa_debug_set_wait_limit_ns", "fa_debug_set_fault",
     "STATUS",
@@ -65,6 +66,10 @@ def load_library():
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, f, vp]
+    lib.fa_bwd_noalloc.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.fa_bwd_noalloc_max_workspace.restype = ctypes.c_size_t
+    lib.fa_bwd_noalloc_max_workspace.argtypes = []
     lib.fa_sync_check.restype = i
     lib.fa_sync_check.argtypes = [vp]
     lib.fa_last_error_site.restype = ctypes.c_uint
@@ -174,6 +179,37 @@ def fa_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, workspace=None, causa
                         int(bool(causal)), float(scale), _stream_handle(stream))
     _check(st, "fa_bwd")
     return dq, dk, dv
+
+
+def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal: bool = False, scale: float | None = None,
+                   stream=None):
+    """fa_bwd for callers that cannot allocate device memory: no workspace argument.
+
+    The library supplies the scratch from a fixed per-device buffer of
+    fa_bwd_noalloc_max_workspace() bytes (larger problems raise FAError with
+    FA_ERR_WORKSPACE).  The caller passes every input and output tensor; this
+    function allocates nothing.  Calls that overlap on the GPU share that buffer
+    and must be serialised.
+    """
+    import torch
+
+    lib = load_library()
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_bhnd(name, t, (B, H, N, d), torch.bfloat16)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, N]")
+    if scale is None:
+        scale = d ** -0.5
+    with torch.cuda.device(q.device):
+        st = lib.fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                                _ptr(dv), B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+    _check(st, "fa_bwd_noalloc")
+    return dq, dk, dv
+
+
+def fa_bwd_noalloc_max_workspace() -> int:
+    return int(load_library().fa_bwd_noalloc_max_workspace())
 
 
 def fa_sync_check(stream=None):
