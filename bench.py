@@ -3,9 +3,12 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Workload (the configuration the headline metric is quoted on): bf16 attention,
-B=4, H=16, N=2048, d=128, scale 1/sqrt(d), non-causal, inputs N(0,1) from seed 2.
-One step = one pass of the hot path over that batch: the forward kernel
-(fa_fwd).  TFLOP/s counts 4*B*H*N^2*d per forward.
+B=4, H=16, N=2048, d=128, scale 1/sqrt(d), non-causal, Q, K, V, dO ~ N(0,1) from
+seed 2.  One step = one pass of the whole bf16 hot path over that batch: the
+forward (fa_fwd) and the backward's three stages (fa_bwd_prep, fa_bwd_main,
+fa_bwd_dq), four launches.  TFLOP/s counts 4*B*H*N^2*d per forward and 2.5 times
+that per backward.  Each stage is bracketed by its own CUDA events, which give
+the per-kernel rooflines.
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides.  L2 (129 MB) is flushed before every
@@ -13,7 +16,7 @@ step by writing a 256 MB buffer outside the per-step CUDA-event pairs; device
 time is the sum of the per-step event pairs on the launching stream, max over
 ranks.  `e2e` repeats the step through the same public call with the inputs in
 pinned host memory: the H2D copies of Q, K, V, the kernel and the D2H copies of
-O and LSE are all inside its timed region.
+O, LSE, dQ, dK and dV are all inside its timed region.
 
 Under torchrun (N > 1) every rank runs the same independent replica (the heads
 shard with no exchange, so there is no collective on the data path) and rank 0
@@ -34,7 +37,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = {"workload": "bf16 attention forward, B=4 H=16 N=2048 d=128, non-causal, scale=1/sqrt(d)",
+WORKLOAD = {"workload": "bf16 attention forward + backward, B=4 H=16 N=2048 d=128, non-causal, scale=1/sqrt(d)",
             "B": 4, "H": 16, "N": 2048, "d": 128, "causal": False, "seed": 2}
 METRIC = "attention fwd/bwd TFLOP/s on 1 GB300 and % of dense BF16/FP8 tensor peak"
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -167,24 +170,30 @@ def run_ours(args):
     w = WORKLOAD
     B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
     scale = d ** -0.5
-    x = normal_qkv(B, H, N, d, w["seed"] + rank)
-    q, k, v = (x[n].to(torch.bfloat16).cuda() for n in ("q", "k", "v"))
+    x = normal_qkv(B, H, N, d, w["seed"] + rank, with_do=True)
+    q, k, v, g = (x[n].to(torch.bfloat16).cuda() for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
     lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
-    launches_per_step = 1
-
-    def step():
-        fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale)
+    stages = ("fwd", "bwd_prep", "bwd_main", "bwd_dq")
+    calls = {
+        "fwd": lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale),
+        "bwd_prep": lambda: fa.fa_bwd_prep(o, g, lse, ws),
+        "bwd_main": lambda: fa.fa_bwd_main(q, k, v, g, dk, dv, ws, causal=causal, scale=scale),
+        "bwd_dq": lambda: fa.fa_bwd_dq(ws, dq, scale=scale),
+    }
+    launches_per_step = 4
 
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        for st in stages:
+            calls[st]()
     fa.fa_sync_check()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(local) if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
@@ -197,40 +206,43 @@ def run_ours(args):
         sampler.mark("t0")
     for i in range(args.steps):
         flush.zero_()
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
+        ev[i][0].record(stream)
+        for j, st in enumerate(stages):
+            calls[st]()
+            ev[i][j + 1].record(stream)
     torch.cuda.synchronize()
     if sampler:
         sampler.mark("t1")
     t_wall = time.perf_counter() - t_wall0
     clocks = sampler.stop() if sampler else None
     fa.fa_sync_check()
-    per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    dev_ms = sum(per_step)
+    stage_ms = {st: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
+                for j, st in enumerate(stages)}
+    dev_ms = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps))
     if world > 1:
         t = torch.tensor([dev_ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         torch.distributed.barrier()
         dev_ms = float(t.item())
-    flops_step = fwd_flops(B, H, N, d, causal)
+    f_fwd = fwd_flops(B, H, N, d, causal)
+    flops_step = 3.5 * f_fwd
     ms_per_step = dev_ms / args.steps
     value = flops_step * args.steps * world / (dev_ms * 1e-3) / 1e12
 
-    # End to end through the public call: pinned host inputs in, O and LSE back out.
-    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    # End to end through the public calls: pinned host inputs in, every output back out.
+    hq, hk, hv, hg = (t.cpu().pin_memory() for t in (q, k, v, g))
+    outs = (o, lse, dq, dk, dv)
+    houts = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    dq_in, dk_in, dv_in, dg_in = (torch.empty_like(t) for t in (q, k, v, g))
     e2e_steps = max(3, min(args.steps, 50))
 
     def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        fa.fa_fwd(dq, dk, dv, o=o, lse=lse, causal=causal, scale=scale)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+        for dst, src in zip((dq_in, dk_in, dv_in, dg_in), (hq, hk, hv, hg)):
+            dst.copy_(src, non_blocking=True)
+        fa.fa_fwd(dq_in, dk_in, dv_in, o=o, lse=lse, causal=causal, scale=scale)
+        fa.fa_bwd(dq_in, dk_in, dv_in, o, dg_in, lse, dq, dk, dv, ws, causal=causal, scale=scale)
+        for dst, src in zip(houts, outs):
+            dst.copy_(src, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -243,8 +255,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     fa.fa_sync_check()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
+    d2h = sum(t.numel() * t.element_size() for t in houts)
 
     if rank != 0:
         if world > 1:
@@ -253,15 +265,49 @@ def run_ours(args):
 
     peaks = load_peaks()
     peak = peaks["bf16_tflops"]
-    kernel_tflops = flops_step / (ms_per_step * 1e-3) / 1e12
+    hbm = peaks["hbm_gbs"]
+    elems = B * H * N * d
+    npad = (N + 63) // 64 * 64
+    stage_info = {
+        "fwd": {"bound": "tensor", "flops": f_fwd, "bytes": 8 * elems + 4 * B * H * N,
+                "kernel": "fwd_bf16_kernel<128,false>", "profile": "fwd_bf16_B4H16N2048d128.md",
+                "source": "io_aware_exact_fwd_gb300/csrc/fa_fwd.cu"},
+        "bwd_prep": {"bound": "hbm", "flops": 2.0 * elems,
+                     "bytes": 4 * elems + 4 * B * H * N + 8 * B * H * npad + 4 * elems,
+                     "kernel": "bwd_preprocess_kernel"},
+        "bwd_main": {"bound": "tensor", "flops": 2.5 * f_fwd,
+                     "bytes": 10 * elems + 8 * B * H * npad + 4 * elems + 4 * elems,
+                     "kernel": "bwd_main_kernel<false>", "profile": "bwd_main_B4H16N2048d128.md",
+                     "source": "io_aware_exact_fwd_gb300/csrc/fa_bwd.cu"},
+        "bwd_dq": {"bound": "hbm", "flops": 0.0, "bytes": 4 * elems + 2 * elems, "kernel": "bwd_dq_convert_kernel"},
+    }
+    per_stage = {}
+    for st in stages:
+        info, ms = stage_info[st], stage_ms[st]
+        tf = info["flops"] / (ms * 1e-3) / 1e12
+        gbs = info["bytes"] / (ms * 1e-3) / 1e9
+        if info["bound"] == "tensor":
+            per_stage[st] = {"ms": round(ms, 5), "bound": "tensor", "achieved": round(tf, 1), "unit": "TFLOP/s",
+                             "frac": round(tf / peak, 4), "gbs": round(gbs, 1)}
+        else:
+            per_stage[st] = {"ms": round(ms, 5), "bound": "hbm", "achieved": round(gbs, 1), "unit": "GB/s",
+                             "frac": round(gbs / hbm, 4)}
+    dom = max(stages, key=lambda st: stage_ms[st])
+    di = stage_info[dom]
+    dom_ach = per_stage[dom]["achieved"]
+    dom_peak = peak if di["bound"] == "tensor" else hbm
+    traffic = None
+    if args.traffic is not None:
+        traffic = args.traffic
+    elif "profile" in di:
+        traffic = profile_traffic(di["profile"], di["source"])
     roofline = {
-        "bound": "tensor", "kernel": "fwd_bf16_kernel<128,false>", "achieved": round(kernel_tflops, 1),
-        "peak": peak, "peak_source": f"{peaks['source']} bf16_tflops (burst, cuBLAS)", "unit": "TFLOP/s",
-        "frac": round(kernel_tflops / peak, 4),
-        "traffic": args.traffic if args.traffic is not None else profile_traffic(
-            "fwd_bf16_B4H16N2048d128.md", "io_aware_exact_fwd_gb300/csrc/fa_fwd.cu"),
+        "bound": di["bound"], "kernel": di["kernel"], "achieved": dom_ach, "peak": dom_peak,
+        "peak_source": (f"{peaks['source']} bf16_tflops (burst, cuBLAS)" if di["bound"] == "tensor"
+                        else f"{peaks['source']} hbm_gbs (copy)"),
+        "unit": per_stage[dom]["unit"], "frac": round(dom_ach / dom_peak, 4), "traffic": traffic,
         "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
-        "algorithmic_flops_per_launch": flops_step,
+        "algorithmic_flops_per_launch": di["flops"], "algorithmic_bytes_per_launch": di["bytes"],
     }
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -271,9 +317,11 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(WORKLOAD, l2="flushed before every step (256 MB write, outside the timed event pairs)",
-                       parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+                       parallelism=f"replicas x{world}" if world > 1 else "single GPU",
+                       flops_per_step=flops_step),
         "frac_of_peak": round(value / world / peak, 4),
         "roofline": roofline,
+        "stages": per_stage,
         "e2e": {"value": round(flops_step / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -287,57 +335,59 @@ def run_ours(args):
     return line
 
 
-def cpu_baseline(seconds: float = 10.0):
-    """The float64 oracle, as it stands, on a bounded row sample of the workload."""
+def _oracle_step_sample(q, k, v, g, scale, causal, head, r0, rows_per_step):
+    """The oracle on one row block of one head: forward rows plus that block's backward share."""
     import numpy as np
 
-    from oracle import attention_forward_rows
+    from oracle import attention_backward_rows, attention_forward_rows
+
+    N = q.shape[2]
+    rows = np.arange(r0, min(N, r0 + rows_per_step))
+    attention_forward_rows(q[0, head], k[0, head], v[0, head], scale, causal, rows)
+    attention_backward_rows(q[0, head], k[0, head], v[0, head], g[0, head], scale, causal, rows)
+    return len(rows)
+
+
+def _oracle_inputs():
+    import torch
+
     from synth import normal_qkv
 
     w = WORKLOAD
-    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
-    x = normal_qkv(1, 2, N, d, w["seed"])
-    import torch
+    x = normal_qkv(1, 2, w["N"], w["d"], w["seed"], with_do=True)
+    return [x[n].to(torch.bfloat16).to(torch.float64).numpy() for n in ("q", "k", "v", "do")]
 
-    q, k, v = (x[n].to(torch.bfloat16).to(torch.float64).numpy() for n in ("q", "k", "v"))
+
+def cpu_baseline(seconds: float = 10.0):
+    """The float64 oracle, as it stands, on a bounded row sample of the workload (fwd + bwd)."""
+    w = WORKLOAD
+    N, d, causal = w["N"], w["d"], w["causal"]
+    q, k, v, g = _oracle_inputs()
     rows_per_call = 256
-    done_rows, t0 = 0, time.perf_counter()
-    h = 0
+    done_rows, t0, i = 0, time.perf_counter(), 0
     while time.perf_counter() - t0 < seconds:
-        r0 = (done_rows // rows_per_call * rows_per_call) % N
-        rows = np.arange(r0, min(N, r0 + rows_per_call))
-        attention_forward_rows(q[0, h % 2], k[0, h % 2], v[0, h % 2], d ** -0.5, causal, rows)
-        done_rows += len(rows)
-        h += 1
+        done_rows += _oracle_step_sample(q, k, v, g, d ** -0.5, causal, i % 2, (i * rows_per_call) % N,
+                                         rows_per_call)
+        i += 1
     dt = time.perf_counter() - t0
-    flops = 4.0 * done_rows * N * d / (2 if causal else 1)
+    flops = 3.5 * 4.0 * done_rows * N * d / (2 if causal else 1)
     cores = len(os.sched_getaffinity(0))
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done_rows} query rows x {N} keys of 2 heads (d={d}) in {dt:.1f} s, float64 numpy, "
-                      f"BLAS threads = {cores}"}
+            "sample": f"{done_rows} query rows x {N} keys (forward rows + their backward share) of 2 heads "
+                      f"(d={d}) in {dt:.1f} s, float64 numpy, BLAS threads = {cores}"}
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return None
-    import numpy as np
-    import torch
-
-    from oracle import attention_forward_rows
-    from synth import normal_qkv
-
     w = WORKLOAD
-    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
-    x = normal_qkv(1, 2, N, d, w["seed"])
-    q, k, v = (x[n].to(torch.bfloat16).to(torch.float64).numpy() for n in ("q", "k", "v"))
-    rows_per_step = 64
+    N, d, causal = w["N"], w["d"], w["causal"]
+    q, k, v, g = _oracle_inputs()
+    rows_per_step = 32
 
     def step(i):
-        r0 = (i * rows_per_step) % N
-        rows = np.arange(r0, min(N, r0 + rows_per_step))
-        attention_forward_rows(q[0, i % 2], k[0, i % 2], v[0, i % 2], d ** -0.5, causal, rows)
-        return len(rows)
+        return _oracle_step_sample(q, k, v, g, d ** -0.5, causal, i % 2, (i * rows_per_step) % N, rows_per_step)
 
     for i in range(args.warmup):
         step(i)
@@ -346,7 +396,7 @@ def run_reference(args):
     for i in range(args.steps):
         rows += step(i)
     dt = time.perf_counter() - t0
-    flops = 4.0 * rows * N * d / (2 if causal else 1)
+    flops = 3.5 * 4.0 * rows * N * d / (2 if causal else 1)
     value = flops / dt / 1e12
     cores = len(os.sched_getaffinity(0))
     line = {
@@ -355,7 +405,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": dict(WORKLOAD),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{rows_per_step} query rows x {N} keys of one head per step"},
+                         "sample": f"{rows_per_step} query rows x {N} keys of one head per step "
+                                   f"(forward rows + their backward share)"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -365,7 +416,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

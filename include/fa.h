@@ -117,6 +117,27 @@ FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, co
                   int causal, float scale, fa_stream_t stream);
 
 /*
+ * The three stages of fa_bwd, for callers that schedule or time them one by one.
+ * fa_bwd(...) is exactly fa_bwd_prep, fa_bwd_main, fa_bwd_dq in that order on
+ * one stream with one workspace; arguments mean what they mean for fa_bwd.
+ *
+ * fa_bwd_prep: D_i = sum_c dO_ic O_ic and LSE_i * log2(e) into the workspace
+ *   (rows padded to a multiple of 64: D = 0, LSE = +inf), and zeroes the fp32
+ *   dQ accumulator.  Bandwidth-bound.
+ * fa_bwd_main: the dK/dV-outer loop (per 128-key block: recompute P from LSE,
+ *   dV += P^T dO, dP = dO V^T, dS = P (dP - D), dK += dS^T Q, dQ += dS K into
+ *   the fp32 accumulator).  Writes dk, dv; needs the workspace fa_bwd_prep filled.
+ * fa_bwd_dq: dq = bf16(scale * accumulator).
+ */
+FA_API int fa_bwd_prep(const void* o, const void* dout, const float* lse, void* workspace, size_t ws_bytes, int B,
+                       int H, int N, int d, fa_stream_t stream);
+FA_API int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                       void* workspace, size_t ws_bytes, int B, int H, int N, int d, int causal, float scale,
+                       fa_stream_t stream);
+FA_API int fa_bwd_dq(const void* workspace, size_t ws_bytes, void* dq, int B, int H, int N, int d, float scale,
+                     fa_stream_t stream);
+
+/*
  * fa_bwd_noalloc -- fa_bwd without a caller workspace; allocates nothing.
  * The pages have no counterpart to this call: it exists for callers that
  * cannot allocate device memory themselves (a plugin inside a host framework

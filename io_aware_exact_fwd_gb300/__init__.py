@@ -17,7 +17,7 @@ import os
 
 __all__ = [
     "FAError", "load_library", "library_path", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_noalloc",
-    "fa_bwd_noalloc_max_workspace", "fa_sync_check",
+    "fa_bwd_noalloc_max_workspace", "fa_bwd_prep", "fa_bwd_main", "fa_bwd_dq", "fa_sync_check",
     "fa_strerror",
     "fa_version", "fa_last_error_site", "fa_debug_set_wait_limit_ns", "fa_debug_set_fault",
     "STATUS",
@@ -66,6 +66,12 @@ def load_library():
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, f, vp]
+    lib.fa_bwd_prep.restype = i
+    lib.fa_bwd_prep.argtypes = [vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, vp]
+    lib.fa_bwd_main.restype = i
+    lib.fa_bwd_main.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, f, vp]
+    lib.fa_bwd_dq.restype = i
+    lib.fa_bwd_dq.argtypes = [vp, ctypes.c_size_t, vp, i, i, i, i, f, vp]
     lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.fa_bwd_noalloc_max_workspace.restype = ctypes.c_size_t
@@ -179,6 +185,43 @@ def fa_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, workspace=None, causa
                         int(bool(causal)), float(scale), _stream_handle(stream))
     _check(st, "fa_bwd")
     return dq, dk, dv
+
+
+def _ws_bytes(workspace):
+    return workspace.numel() * workspace.element_size()
+
+
+def fa_bwd_prep(o, do, lse, workspace, stream=None):
+    """Backward stage 1: D = rowsum(dO * O), LSE * log2(e) and a zeroed dQ accumulator in `workspace`."""
+    lib = load_library()
+    B, H, N, d = o.shape
+    with __import__("torch").cuda.device(o.device):
+        st = lib.fa_bwd_prep(_ptr(o), _ptr(do), _ptr(lse), _ptr(workspace), _ws_bytes(workspace), B, H, N, d,
+                             _stream_handle(stream))
+    _check(st, "fa_bwd_prep")
+
+
+def fa_bwd_main(q, k, v, do, dk, dv, workspace, causal: bool = False, scale: float | None = None, stream=None):
+    """Backward stage 2: dK, dV and the fp32 dQ accumulator (needs fa_bwd_prep's workspace)."""
+    lib = load_library()
+    B, H, N, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    with __import__("torch").cuda.device(q.device):
+        st = lib.fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dk), _ptr(dv), _ptr(workspace),
+                             _ws_bytes(workspace), B, H, N, d, int(bool(causal)), float(scale),
+                             _stream_handle(stream))
+    _check(st, "fa_bwd_main")
+
+
+def fa_bwd_dq(workspace, dq, scale: float | None = None, stream=None):
+    """Backward stage 3: dq = bf16(scale * accumulator)."""
+    lib = load_library()
+    B, H, N, d = dq.shape
+    scale = d ** -0.5 if scale is None else scale
+    with __import__("torch").cuda.device(dq.device):
+        st = lib.fa_bwd_dq(_ptr(workspace), _ws_bytes(workspace), _ptr(dq), B, H, N, d, float(scale),
+                           _stream_handle(stream))
+    _check(st, "fa_bwd_dq")
 
 
 def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal: bool = False, scale: float | None = None,

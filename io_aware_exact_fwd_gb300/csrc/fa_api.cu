@@ -168,23 +168,36 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   return fa::bwd_workspace_layout(B, H, N, d).total;
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
-           void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d, int causal, float scale,
-           fa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Which tensors a backward stage reads or writes.
+enum BwdUse : unsigned {
+  kUseQKV = 1u, kUseO = 2u, kUseDout = 4u, kUseLse = 8u, kUseDq = 16u, kUseDkDv = 32u,
+};
+
+// Validation shared by fa_bwd and its three stages; fills `a` on success.
+int bwd_setup(fa::BwdArgs& a, unsigned use, const void* q, const void* k, const void* v, const void* o,
+              const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+              int B, int H, int N, int d, int causal, float scale) {
   const int vs = validate_shape(B, H, N, d, causal, scale);
-  if (vs < 0) return FA_OK;
+  if (vs < 0) return -1;
   if (vs != FA_OK) return vs;
   if (d != 128) return FA_ERR_UNSUPPORTED;
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (((use & kUseQKV) && (!q || !k || !v)) || ((use & kUseO) && !o) || ((use & kUseDout) && !dout) ||
+      ((use & kUseLse) && !lse) || ((use & kUseDq) && !dq) || ((use & kUseDkDv) && (!dk || !dv)))
+    return FA_ERR_INVALID_ARG;
   if (!workspace) return FA_ERR_WORKSPACE;
   if (ws_bytes < fa::bwd_workspace_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
-      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(workspace, 256))
-    return FA_ERR_MISALIGNED;
+  const bool al = (!(use & kUseQKV) || (aligned(q, 16) && aligned(k, 16) && aligned(v, 16))) &&
+                  (!(use & kUseO) || aligned(o, 16)) && (!(use & kUseDout) || aligned(dout, 16)) &&
+                  (!(use & kUseLse) || aligned(lse, 4)) && (!(use & kUseDq) || aligned(dq, 16)) &&
+                  (!(use & kUseDkDv) || (aligned(dk, 16) && aligned(dv, 16))) && aligned(workspace, 256);
+  if (!al) return FA_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
   const int st = device_state(&ds);
   if (st != FA_OK) return st;
-  fa::BwdArgs a;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -203,7 +216,54 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.scale = scale;
   a.err_word = ds->err_word;
   a.dbg = knobs();
-  return fa::launch_bwd_bf16(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return FA_OK;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
+           void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d, int causal, float scale,
+           fa_stream_t stream) {
+  fa::BwdArgs a;
+  const int st = bwd_setup(a, kUseQKV | kUseO | kUseDout | kUseLse | kUseDq | kUseDkDv, q, k, v, o, dout, lse, dq,
+                           dk, dv, workspace, ws_bytes, B, H, N, d, causal, scale);
+  if (st < 0) return FA_OK;
+  if (st != FA_OK) return st;
+  return status_of(fa::launch_bwd_bf16(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd_prep(const void* o, const void* dout, const float* lse, void* workspace, size_t ws_bytes, int B, int H,
+                int N, int d, fa_stream_t stream) {
+  fa::BwdArgs a;
+  const int st = bwd_setup(a, kUseO | kUseDout | kUseLse, nullptr, nullptr, nullptr, o, dout, lse, nullptr, nullptr,
+                           nullptr, workspace, ws_bytes, B, H, N, d, 0, 1.f);
+  if (st < 0) return FA_OK;
+  if (st != FA_OK) return st;
+  return status_of(fa::launch_bwd_prep(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv, void* workspace,
+                size_t ws_bytes, int B, int H, int N, int d, int causal, float scale, fa_stream_t stream) {
+  fa::BwdArgs a;
+  const int st = bwd_setup(a, kUseQKV | kUseDout | kUseDkDv, q, k, v, nullptr, dout, nullptr, nullptr, dk, dv,
+                           workspace, ws_bytes, B, H, N, d, causal, scale);
+  if (st < 0) return FA_OK;
+  if (st != FA_OK) return st;
+  return status_of(fa::launch_bwd_main(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd_dq(const void* workspace, size_t ws_bytes, void* dq, int B, int H, int N, int d, float scale,
+              fa_stream_t stream) {
+  fa::BwdArgs a;
+  const int st = bwd_setup(a, kUseDq, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr, nullptr,
+                           const_cast<void*>(workspace), ws_bytes, B, H, N, d, 0, scale);
+  if (st < 0) return FA_OK;
+  if (st != FA_OK) return st;
+  return status_of(fa::launch_bwd_dq(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int fa_sync_check(fa_stream_t stream) {

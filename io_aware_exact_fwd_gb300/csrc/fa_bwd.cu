@@ -484,22 +484,24 @@ BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
   return w;
 }
 
-cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  const BwdWorkspace w = bwd_workspace_layout(a.B, a.H, a.N, a.d);
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  const long long rows_pad = static_cast<long long>(BH) * w.npad;
+  bwd_preprocess_kernel<<<static_cast<unsigned>((rows_pad + 15) / 16), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
+      reinterpret_cast<float*>(ws + w.off_d), reinterpret_cast<float*>(ws + w.off_lse2),
+      reinterpret_cast<float*>(ws + w.off_dq), a.N, w.npad, rows_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg;
   const int BH = a.B * a.H;
   const BwdWorkspace w = bwd_workspace_layout(a.B, a.H, a.N, a.d);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  float* dq_acc = reinterpret_cast<float*>(ws + w.off_dq);
-  float* dvec = reinterpret_cast<float*>(ws + w.off_d);
-  float* lse2 = reinterpret_cast<float*>(ws + w.off_lse2);
   cudaError_t e;
-
-  const long long rows_pad = static_cast<long long>(BH) * w.npad;
-  bwd_preprocess_kernel<<<static_cast<unsigned>((rows_pad + 15) / 16), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, dvec, lse2, dq_acc,
-      a.N, w.npad, rows_pad);
-  if ((e = cudaGetLastError())) return e;
-
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if ((e = make_tmap_3d(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBqB))) return e;
   if ((e = make_tmap_3d(&tdo, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBqB))) return e;
@@ -515,14 +517,26 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream) {
   if (static_cast<uint32_t>(fattr.numRegs) < kLaunchRegs) return cudaErrorInvalidConfiguration;
   const int nkb = (a.N + kBkB - 1) / kBkB;
   kern<<<static_cast<unsigned>(nkb * BH), kThreads, C::kSmemBytes, stream>>>(
-      tq, tk, tv, tdo, tdk, tdv, lse2, dvec, dq_acc, a.N, w.npad, BH, nkb, a.scale, a.scale * kLog2e, a.err_word,
-      a.dbg.wait_limit_ns);
-  if ((e = cudaGetLastError())) return e;
+      tq, tk, tv, tdo, tdk, tdv, reinterpret_cast<const float*>(ws + w.off_lse2),
+      reinterpret_cast<const float*>(ws + w.off_d), reinterpret_cast<float*>(ws + w.off_dq), a.N, w.npad, BH, nkb,
+      a.scale, a.scale * kLog2e, a.err_word, a.dbg.wait_limit_ns);
+  return cudaGetLastError();
+}
 
-  const long long n8 = static_cast<long long>(BH) * a.N * kD / 8;
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream) {
+  const BwdWorkspace w = bwd_workspace_layout(a.B, a.H, a.N, a.d);
+  const float* dq_acc = reinterpret_cast<const float*>(static_cast<uint8_t*>(a.workspace) + w.off_dq);
+  const long long n8 = static_cast<long long>(a.B) * a.H * a.N * kD / 8;
   bwd_dq_convert_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
       dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.scale, n8);
   return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream) {
+  cudaError_t e;
+  if ((e = launch_bwd_prep(a, stream))) return e;
+  if ((e = launch_bwd_main(a, stream))) return e;
+  return launch_bwd_dq(a, stream);
 }
 
 }  // namespace fa

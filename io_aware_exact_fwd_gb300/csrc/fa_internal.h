@@ -65,7 +65,11 @@ struct BwdWorkspace {
 };
 BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d);
 
-// Backward launcher (fa_bwd.cu): preprocess, main, dQ convert on `stream`.
+// Backward launchers (fa_bwd.cu).  launch_bwd_bf16 = prep, main, dq in order on
+// `stream`; each stage reads only the BwdArgs fields it needs.
+cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream);
 
 // Encodes a 3-D tiled tensor map over a [BH, N, cols] row-major tensor with

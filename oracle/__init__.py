@@ -32,6 +32,7 @@ from .attention import (
     attention_forward_rows,
     attention_backward,
     attention_backward_sampled,
+    attention_backward_rows,
 )
 from .brute import attention_forward_brute
 from .fp8 import (
@@ -50,6 +51,7 @@ __all__ = [
     "attention_forward_rows",
     "attention_backward",
     "attention_backward_sampled",
+    "attention_backward_rows",
     "attention_forward_brute",
     "sylvester_hadamard",
     "fwht_f32",

@@ -169,3 +169,21 @@ def attention_backward_sampled(q_head, k_head, v_head, do_head, scale: float, ca
     dv = pc.T @ g
     dk = scale * (dsc.T @ q)
     return dq, dk, dv
+
+
+def attention_backward_rows(q_head, k_head, v_head, do_head, scale: float, causal: bool, rows):
+    """One row block's share of the backward of ONE head (the loop body of attention_backward).
+
+    For the query rows ``rows``: returns (dQ[rows], dK_part, dV_part), where dK_part
+    and dV_part are the contributions of those rows to dK and dV ([N, d] each);
+    summing the parts over any partition of the rows gives attention_backward's
+    dK and dV.
+    """
+    q, k, v, g = (_as_f64(t) for t in (q_head, k_head, v_head, do_head))
+    rows = np.asarray(rows, dtype=np.int64)
+    s = _scores(q[rows], k, rows, scale, causal)
+    p, _, _ = _softmax_rows(s)
+    gr = g[rows]
+    dp = gr @ v.T
+    ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+    return scale * (ds @ k), scale * (ds.T @ q[rows]), p.T @ gr

@@ -131,3 +131,19 @@ def test_backward_rejects_bad_arguments():
         fa.fa_bwd(q64, k64, v64, o64, g64, lse64)
     assert e.value.status == 2
     fa.fa_sync_check()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_staged_backward_equals_fa_bwd(causal):
+    # fa_bwd is fa_bwd_prep + fa_bwd_main + fa_bwd_dq on one stream.
+    q, k, v, g = _inputs(2, 2, 700, 128, 12)
+    o, lse = fa.fa_fwd(q, k, v, causal=causal)
+    ref = fa.fa_bwd(q, k, v, o, g, lse, causal=causal)
+    ws = torch.empty(fa.fa_bwd_workspace_size(2, 2, 700, 128), dtype=torch.uint8, device="cuda")
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    fa.fa_bwd_prep(o, g, lse, ws)
+    fa.fa_bwd_main(q, k, v, g, dk, dv, ws, causal=causal)
+    fa.fa_bwd_dq(ws, dq)
+    fa.fa_sync_check()
+    assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+    assert _rel_err(dq, ref[0].double().cpu().numpy()) <= 1e-2

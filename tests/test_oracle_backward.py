@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import attention_backward, attention_backward_sampled, attention_forward
+from oracle import attention_backward, attention_backward_rows, attention_backward_sampled, attention_forward
 from synth import normal_qkv
 
 
@@ -97,3 +97,19 @@ def test_sampled_backward_equals_full_backward(causal):
     np.testing.assert_allclose(sq, dq[0, 0, rows], rtol=0, atol=1e-12)
     np.testing.assert_allclose(sk, dk[0, 0, keys], rtol=0, atol=1e-12)
     np.testing.assert_allclose(sv, dv[0, 0, keys], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_block_parts_sum_to_full_backward(causal):
+    x = normal_qkv(1, 1, 90, 8, seed=27, with_do=True)
+    q, k, v, g = (x[n].numpy().astype(np.float64)[0, 0] for n in ("q", "k", "v", "do"))
+    dq, dk, dv = attention_backward(q[None, None], k[None, None], v[None, None], g[None, None], 0.6, causal)
+    sk, sv = np.zeros_like(k), np.zeros_like(v)
+    for r0 in (0, 31, 60):
+        rows = np.arange(r0, {0: 31, 31: 60, 60: 90}[r0])
+        pq, pk, pv = attention_backward_rows(q, k, v, g, 0.6, causal, rows)
+        np.testing.assert_allclose(pq, dq[0, 0, rows], rtol=0, atol=1e-12)
+        sk += pk
+        sv += pv
+    np.testing.assert_allclose(sk, dk[0, 0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sv, dv[0, 0], rtol=0, atol=1e-12)
