@@ -166,6 +166,57 @@ FA_API int fa_bwd_noalloc(const void* q, const void* k, const void* v, const voi
 FA_API size_t fa_bwd_noalloc_max_workspace(void);
 
 /*
+ * FP8 path ("FlashAttention-Skalierung, Multi-GPU-Training und
+ * Gewichtsquantisierung", section 1, "Unterstützung geringer FP8-Präzision":
+ * block quantisation plus multiplication of Q and K by a random orthogonal
+ * matrix before quantising).
+ *
+ * fa_fp8_workspace_size -- bytes of device workspace the FP8 path needs (0 if
+ *   the sizes are invalid).
+ * fa_fp8_workspace_offsets -- byte offsets of the regions inside that workspace,
+ *   written to offsets[0..7]: q8, k8, v8t, sq, sk, sv, then npad and ntiles.
+ *   q8, k8: e4m3 codes [B, H, N, d] (row-major); v8t: e4m3 codes of V transposed
+ *   [B, H, d, npad] (keys contiguous, npad = N rounded up to 128, padding zero);
+ *   sq, sk, sv: fp32 dequantisation scales [B, H, ntiles], ntiles = ceil(N/64).
+ *
+ * fa_fp8_prepare -- fill the workspace from q, k, v.
+ *   q, k, v   : const [B, H, N, d], fp32 (in_dtype = 0) or bf16 (in_dtype = 1)
+ *   signs     : const int8 [d] on the device: the rotation's random signs s
+ *               (an entry < 0 means -1, otherwise +1)
+ *   For Q and K, each row x becomes y = (x * s) H_d (H_d the Sylvester
+ *   Walsh-Hadamard matrix, entries +-1, so (QM)(KM)^T = d Q K^T with M = diag(s)
+ *   H_d; fa_fwd_fp8 folds the 1/d into its scale).  V rows are unchanged.  Then
+ *   per tile of 64 consecutive rows of one head: amax = max|y| (exact), codes =
+ *   e4m3(y * (448 / amax)) with round-to-nearest-even and saturation (OCP E4M3,
+ *   max 448), scale = amax / 448 (1 for an all-zero tile), so that
+ *   y ~= decode(code) * scale.  The transform is fp32 radix-2 butterflies with
+ *   spans 1, 2, ..., d/2; 448 / amax and amax / 448 are IEEE fp32 divisions.
+ *   Errors as fa_fwd; FA_ERR_WORKSPACE for a missing or short workspace;
+ *   FA_ERR_INVALID_ARG for in_dtype not 0/1 or a NULL signs pointer.
+ */
+FA_API size_t fa_fp8_workspace_size(int B, int H, int N, int d);
+FA_API int fa_fp8_workspace_offsets(int B, int H, int N, int d, size_t* offsets);
+FA_API int fa_fp8_prepare(const void* q, const void* k, const void* v, int in_dtype, const int8_t* signs,
+                          void* workspace, size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream);
+
+/*
+ * fa_fwd_fp8 -- FP8 forward from a workspace filled by fa_fp8_prepare (same
+ * B, H, N, d; d = 128).  Computes O = softmax(scale * Q K^T [+mask]) V and LSE
+ * like fa_fwd, with both matmuls on e4m3 operands (kind::f8f6f4 tensor cores,
+ * fp32 accumulation):
+ *   S = (scale / d) * sQ(row tile) * sK(key tile) * (codesQ . codesK^T)
+ *   (the rotation's H_d H_d^T = d I is undone by the 1/d);
+ *   P = exp(S - m) is multiplied by sV(key tile) / max_tiles sV and rounded to
+ *   e4m3 as the A operand of P V; O = acc * max sV / l, rounded to bf16 once.
+ *   The row sum l and LSE use the unrounded P.
+ *   o   : bf16 [B, H, N, d] (output)      lse : float [B, H, N] (output)
+ * Errors as fa_fwd; FA_ERR_UNSUPPORTED for d != 128; FA_ERR_WORKSPACE for a
+ * missing or short workspace (256-byte alignment required).
+ */
+FA_API int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* lse, int B, int H, int N, int d,
+                      int causal, float scale, fa_stream_t stream);
+
+/*
  * fa_sync_check -- synchronise `stream`, then report device-detected errors.
  * Returns FA_ERR_CUDA if the stream or a prior launch failed, FA_ERR_TIMEOUT
  * if any kernel of this library on the current device expired a bounded wait

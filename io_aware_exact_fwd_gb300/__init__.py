@@ -17,7 +17,8 @@ import os
 
 __all__ = [
     "FAError", "load_library", "library_path", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_noalloc",
-    "fa_bwd_noalloc_max_workspace", "fa_bwd_prep", "fa_bwd_main", "fa_bwd_dq", "fa_sync_check",
+    "fa_bwd_noalloc_max_workspace", "fa_bwd_prep", "fa_bwd_main", "fa_bwd_dq", "fa_fp8_workspace_size",
+    "fa_fp8_workspace_offsets", "fa_fp8_prepare", "fa_fwd_fp8", "fa_sync_check",
     "fa_strerror",
     "fa_version", "fa_last_error_site", "fa_debug_set_wait_limit_ns", "fa_debug_set_fault",
     "STATUS",
@@ -72,6 +73,14 @@ def load_library():
     lib.fa_bwd_main.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, f, vp]
     lib.fa_bwd_dq.restype = i
     lib.fa_bwd_dq.argtypes = [vp, ctypes.c_size_t, vp, i, i, i, i, f, vp]
+    lib.fa_fp8_workspace_size.restype = ctypes.c_size_t
+    lib.fa_fp8_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_fp8_workspace_offsets.restype = i
+    lib.fa_fp8_workspace_offsets.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa_fp8_prepare.restype = i
+    lib.fa_fp8_prepare.argtypes = [vp, vp, vp, i, vp, vp, ctypes.c_size_t, i, i, i, i, vp]
+    lib.fa_fwd_fp8.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp, ctypes.c_size_t, vp, vp, i, i, i, i, i, f, vp]
     lib.fa_bwd_noalloc.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.fa_bwd_noalloc_max_workspace.restype = ctypes.c_size_t
@@ -222,6 +231,66 @@ def fa_bwd_dq(workspace, dq, scale: float | None = None, stream=None):
         st = lib.fa_bwd_dq(_ptr(workspace), _ws_bytes(workspace), _ptr(dq), B, H, N, d, float(scale),
                            _stream_handle(stream))
     _check(st, "fa_bwd_dq")
+
+
+def fa_fp8_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().fa_fp8_workspace_size(B, H, N, d))
+
+
+def fa_fp8_workspace_offsets(B: int, H: int, N: int, d: int) -> dict:
+    """Byte offsets of the FP8 workspace regions (q8, k8, v8t, sq, sk, sv) plus npad and ntiles."""
+    arr = (ctypes.c_size_t * 8)()
+    _check(load_library().fa_fp8_workspace_offsets(B, H, N, d, arr), "fa_fp8_workspace_offsets")
+    keys = ("q8", "k8", "v8t", "sq", "sk", "sv", "npad", "ntiles")
+    return {kk: int(arr[i]) for i, kk in enumerate(keys)}
+
+
+def fa_fp8_prepare(q, k, v, signs, workspace=None, stream=None):
+    """Rotate Q, K and block-quantise Q, K, V to e4m3 into `workspace` (allocated if None); returns it.
+
+    q, k, v: fp32 or bf16 CUDA tensors [B, H, N, d]; signs: int8 CUDA tensor [d] (+-1).
+    """
+    import torch
+
+    lib = load_library()
+    B, H, N, d = q.shape
+    dt = q.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise TypeError("q, k, v must be float32 or bfloat16")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_bhnd(name, t, (B, H, N, d), dt)
+    if signs.dtype != torch.int8 or tuple(signs.shape) != (d,) or not signs.is_cuda:
+        raise ValueError("signs must be an int8 CUDA tensor of shape [d]")
+    if workspace is None:
+        workspace = torch.empty(max(fa_fp8_workspace_size(B, H, N, d), 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = lib.fa_fp8_prepare(_ptr(q), _ptr(k), _ptr(v), 1 if dt == torch.bfloat16 else 0, _ptr(signs),
+                                _ptr(workspace), _ws_bytes(workspace), B, H, N, d, _stream_handle(stream))
+    _check(st, "fa_fp8_prepare")
+    return workspace
+
+
+def fa_fwd_fp8(workspace, shape, o=None, lse=None, causal: bool = False, scale: float | None = None, stream=None):
+    """FP8 forward from a prepared workspace; shape = (B, H, N, d).  Returns (o bf16, lse fp32)."""
+    import torch
+
+    lib = load_library()
+    B, H, N, d = shape
+    dev = workspace.device
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    _check_bhnd("o", o, (B, H, N, d), torch.bfloat16)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, N]")
+    if scale is None:
+        scale = d ** -0.5
+    with torch.cuda.device(dev):
+        st = lib.fa_fwd_fp8(_ptr(workspace), _ws_bytes(workspace), _ptr(o), _ptr(lse), B, H, N, d,
+                            int(bool(causal)), float(scale), _stream_handle(stream))
+    _check(st, "fa_fwd_fp8")
+    return o, lse
 
 
 def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal: bool = False, scale: float | None = None,

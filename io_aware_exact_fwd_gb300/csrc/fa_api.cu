@@ -266,6 +266,83 @@ int fa_bwd_dq(const void* workspace, size_t ws_bytes, void* dq, int B, int H, in
   return status_of(fa::launch_bwd_dq(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t fa_fp8_workspace_size(int B, int H, int N, int d) {
+  if (validate_shape(B, H, N, d, 0, 1.f) != FA_OK) return 0;
+  return fa::fp8_layout(B, H, N, d).total;
+}
+
+int fa_fp8_workspace_offsets(int B, int H, int N, int d, size_t* offsets) {
+  if (!offsets) return FA_ERR_INVALID_ARG;
+  const int vs = validate_shape(B, H, N, d, 0, 1.f);
+  if (vs < 0) return FA_ERR_INVALID_ARG;
+  if (vs != FA_OK) return vs;
+  const fa::Fp8Layout l = fa::fp8_layout(B, H, N, d);
+  offsets[0] = l.off_q8;
+  offsets[1] = l.off_k8;
+  offsets[2] = l.off_v8t;
+  offsets[3] = l.off_sq;
+  offsets[4] = l.off_sk;
+  offsets[5] = l.off_sv;
+  offsets[6] = static_cast<size_t>(l.npad);
+  offsets[7] = static_cast<size_t>(l.ntiles);
+  return FA_OK;
+}
+
+int fa_fp8_prepare(const void* q, const void* k, const void* v, int in_dtype, const int8_t* signs, void* workspace,
+                   size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream) {
+  const int vs = validate_shape(B, H, N, d, 0, 1.f);
+  if (vs < 0) return FA_OK;
+  if (vs != FA_OK) return vs;
+  if (in_dtype != 0 && in_dtype != 1) return FA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !signs) return FA_ERR_INVALID_ARG;
+  if (!workspace) return FA_ERR_WORKSPACE;
+  if (ws_bytes < fa::fp8_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  const int st = device_state(&ds);
+  if (st != FA_OK) return st;
+  fa::Fp8PrepArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.in_bf16 = in_dtype;
+  a.signs = signs;
+  a.workspace = workspace;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  return fa::launch_fp8_prepare(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* lse, int B, int H, int N, int d, int causal,
+               float scale, fa_stream_t stream) {
+  const int vs = validate_shape(B, H, N, d, causal, scale);
+  if (vs < 0) return FA_OK;
+  if (vs != FA_OK) return vs;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!o || !lse) return FA_ERR_INVALID_ARG;
+  if (!workspace) return FA_ERR_WORKSPACE;
+  if (ws_bytes < fa::fp8_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
+  if (!aligned(o, 16) || !aligned(lse, 4) || !aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  const int st = device_state(&ds);
+  if (st != FA_OK) return st;
+  fa::FwdArgs a{};
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.err_word = ds->err_word;
+  a.dbg = knobs();
+  return fa::launch_fwd_fp8(a, workspace, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                                  : FA_ERR_CUDA;
+}
+
 int fa_sync_check(fa_stream_t stream) {
   DeviceState* ds = nullptr;
   const int st = device_state(&ds);

@@ -328,6 +328,16 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
+// Two e4m3 codes (round to nearest even, saturating at +-448) in the low 16
+// bits: `lo` in bits 0-7, `hi` in bits 8-15.
+__device__ __forceinline__ uint32_t e4m3x2_bits(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tmov.b16 %0, t;\n\t}"
+      : "=h"(r)
+      : "f"(lo), "f"(hi));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

@@ -1,0 +1,221 @@
+// FP8 input preparation for sm_103a: incoherent processing and block quantisation.
+//
+// "FlashAttention-Skalierung, Multi-GPU-Training und Gewichtsquantisierung",
+// section 1, bullet "Unterstützung geringer FP8-Präzision": FP8 tensor cores
+// double raw throughput; to keep outliers from destroying precision, small tiles
+// are scaled independently (block quantisation) and Q and K are multiplied by a
+// random orthogonal matrix before quantising (incoherent processing).
+//
+// Here (one CTA per 64-row tile of one head of Q, K or V):
+//  * Q and K rows are rotated by x -> (x * s) H_d, s the caller's +-1 signs and
+//    H_d the Sylvester Walsh-Hadamard matrix, as a radix-2 transform with
+//    butterfly spans 1, 2, ..., d/2 (each butterfly one fp32 add and one fp32
+//    subtract; spans below the per-thread width in registers, the rest across
+//    lanes with shuffles).  The 1/sqrt(d) normalisation of the orthogonal
+//    matrix is left to the attention kernel's score scale.  V is not rotated.
+//  * amax = max |x| over the tile (exact), inv = 448 / amax (one IEEE fp32
+//    division), codes = e4m3_rn_satfinite(x * inv), sigma = amax / 448
+//    (sigma = inv = 1 for an all-zero tile).
+//  * Q and K codes are written row-major [BH, N, d]; V codes transposed,
+//    [BH, d, npad] with keys contiguous (npad = N rounded up to 128, a whole
+//    attention key block), so that V is a K-major operand of the P V MMA.
+//    Keys >= N are zeros (a V-only block past the last tile writes zeros).
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "fa_device.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kTileRows = 64;
+constexpr int kPrepThreads = 256;  // 8 warps x 8 rows each
+
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %2, %1;\n\tmov.b16 %0, t;\n\t}" : "=h"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// Load 4 (d=128) or 2 (d=64) consecutive elements of one row as fp32.
+template <int D>
+__device__ __forceinline__ void load_row(const void* base, size_t elem0, int in_bf16, float (&x)[D / 32]) {
+  constexpr int E = D / 32;
+  if (in_bf16) {
+    const __nv_bfloat16* p = static_cast<const __nv_bfloat16*>(base) + elem0;
+    if (E == 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(p);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+      x[0] = a.x; x[1] = a.y; x[2 % E] = b.x; x[3 % E] = b.y;
+    } else {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+      x[0] = a.x; x[1 % E] = a.y;
+    }
+  } else {
+    const float* p = static_cast<const float*>(base) + elem0;
+    if (E == 4) {
+      const float4 a = *reinterpret_cast<const float4*>(p);
+      x[0] = a.x; x[1] = a.y; x[2 % E] = a.z; x[3 % E] = a.w;
+    } else {
+      const float2 a = *reinterpret_cast<const float2*>(p);
+      x[0] = a.x; x[1 % E] = a.y;
+    }
+  }
+}
+
+// In-place unnormalised Walsh-Hadamard transform of one row held as E = D/32
+// consecutive elements per lane (lane t holds elements E*t .. E*t+E-1).
+template <int D>
+__device__ __forceinline__ void fwht_row(float (&x)[D / 32], int lane) {
+  constexpr int E = D / 32;
+  // spans inside the lane
+#pragma unroll
+  for (int span = 1; span < E; span <<= 1) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      if ((i & span) == 0) {
+        const float a = x[i], b = x[i + span];
+        x[i] = a + b;
+        x[i + span] = a - b;
+      }
+    }
+  }
+  // spans across lanes: partner lane = lane ^ (span / E)
+#pragma unroll
+  for (int span = E; span < D; span <<= 1) {
+    const int m = span / E;
+    const bool upper = (lane & m) != 0;  // this lane holds the "b" half
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
+      x[i] = upper ? (other - x[i]) : (x[i] + other);
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* __restrict__ q,
+                                                                   const void* __restrict__ k,
+                                                                   const void* __restrict__ v, int in_bf16,
+                                                                   const int8_t* __restrict__ signs,
+                                                                   Fp8Layout lay, uint8_t* __restrict__ ws, int N) {
+  constexpr int E = D / 32;
+  constexpr int kRowsPerWarp = kTileRows / 8;
+  const int tile = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int which = blockIdx.z;  // 0 = Q, 1 = K, 2 = V
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const void* src = which == 0 ? q : (which == 1 ? k : v);
+  __shared__ float s_amax[8];
+  __shared__ uint8_t s_vt[D * kTileRows];  // V codes of this tile, transposed [d][64]
+
+  float sgn[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) sgn[i] = signs[E * lane + i] < 0 ? -1.f : 1.f;
+
+  float x[kRowsPerWarp][E];
+  float amax = 0.f;
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int row = tile * kTileRows + warp * kRowsPerWarp + r;
+    if (row < N) {
+      load_row<D>(src, (static_cast<size_t>(bh) * N + row) * D + E * lane, in_bf16, x[r]);
+      if (which < 2) {
+#pragma unroll
+        for (int i = 0; i < E; ++i) x[r][i] *= sgn[i];
+        fwht_row<D>(x[r], lane);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < E; ++i) x[r][i] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(x[r][i]));
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  if (lane == 0) s_amax[warp] = amax;
+  __syncthreads();
+  amax = s_amax[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_amax[w]);
+  const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+  const float sigma = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+
+  const int ntiles = lay.ntiles;
+  if (tile >= ntiles && which < 2) return;  // blocks past the last tile only pad V^T with zeros
+  if (threadIdx.x == 0 && tile < ntiles) {
+    float* sc = reinterpret_cast<float*>(ws + (which == 0 ? lay.off_sq : (which == 1 ? lay.off_sk : lay.off_sv)));
+    sc[static_cast<size_t>(bh) * ntiles + tile] = sigma;
+  }
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int lrow = warp * kRowsPerWarp + r;
+    const int row = tile * kTileRows + lrow;
+    uint8_t c[E];
+#pragma unroll
+    for (int i = 0; i < E; i += 2) {
+      const uint16_t two = e4m3x2(__fmul_rn(x[r][i], inv), __fmul_rn(x[r][i + 1], inv));
+      c[i] = static_cast<uint8_t>(two & 0xff);
+      c[i + 1] = static_cast<uint8_t>(two >> 8);
+    }
+    if (which < 2) {
+      if (row < N) {
+        uint8_t* dst = ws + (which == 0 ? lay.off_q8 : lay.off_k8) + (static_cast<size_t>(bh) * N + row) * D + E * lane;
+        if (E == 4)
+          *reinterpret_cast<uint32_t*>(dst) = c[0] | (c[1 % E] << 8) | (c[2 % E] << 16) | (c[3 % E] << 24);
+        else
+          *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(c[0] | (c[1 % E] << 8));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < E; ++i) s_vt[(E * lane + i) * kTileRows + lrow] = c[i];
+    }
+  }
+  if (which == 2) {
+    __syncthreads();
+    // [d][64] tile -> V^T rows: 64 contiguous key bytes per d-row (16 bytes per thread).
+    uint8_t* vt = ws + lay.off_v8t + static_cast<size_t>(bh) * D * lay.npad + static_cast<size_t>(tile) * kTileRows;
+    for (int idx = threadIdx.x; idx < D * 4; idx += kPrepThreads) {
+      const int drow = idx >> 2;
+      const int part = idx & 3;
+      *reinterpret_cast<uint4*>(vt + static_cast<size_t>(drow) * lay.npad + part * 16) =
+          *reinterpret_cast<const uint4*>(s_vt + drow * kTileRows + part * 16);
+    }
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+Fp8Layout fp8_layout(int B, int H, int N, int d) {
+  Fp8Layout l{};
+  const size_t bh = static_cast<size_t>(B) * H;
+  l.ntiles = (N + kTileRows - 1) / kTileRows;
+  l.npad = (N + 127) / 128 * 128;
+  l.off_q8 = 0;
+  l.off_k8 = align256(bh * N * d);
+  l.off_v8t = l.off_k8 + align256(bh * N * d);
+  l.off_sq = l.off_v8t + align256(bh * d * l.npad);
+  l.off_sk = l.off_sq + align256(bh * l.ntiles * 4);
+  l.off_sv = l.off_sk + align256(bh * l.ntiles * 4);
+  l.total = l.off_sv + align256(bh * l.ntiles * 4);
+  return l;
+}
+
+cudaError_t launch_fp8_prepare(const Fp8PrepArgs& a, cudaStream_t stream) {
+  const Fp8Layout lay = fp8_layout(a.B, a.H, a.N, a.d);
+  dim3 grid(static_cast<unsigned>(lay.npad / kTileRows), static_cast<unsigned>(a.B * a.H), 3);
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  if (a.d == 64)
+    fp8_prepare_kernel<64><<<grid, kPrepThreads, 0, stream>>>(a.q, a.k, a.v, a.in_bf16, a.signs, lay, ws, a.N);
+  else
+    fp8_prepare_kernel<128><<<grid, kPrepThreads, 0, stream>>>(a.q, a.k, a.v, a.in_bf16, a.signs, lay, ws, a.N);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -66,14 +66,21 @@ enum : uint32_t {
   kSiteEpi = 0x303,
 };
 
-template <int D>
+// FP8 selects the e4m3 variant: Q, K and V tiles of e4m3 codes (V transposed,
+// keys contiguous), kind::f8f6f4 MMAs, per-tile dequantisation scales folded
+// into the softmax, P quantised to e4m3 in TMEM, bf16 O.
+template <int D, bool FP8>
 struct FwdCfg {
-  static constexpr int kBoxes = D / kBoxCols;
-  static constexpr int kBoxBytes = kBlockK * kBoxCols * 2;  // 16 KB: 128 rows x 128 bytes
-  static constexpr int kTileBytes = kBlockK * D * 2;        // one Q, K or V tile
-  static constexpr int kSlots = D == 128 ? 4 : 8;
+  static constexpr int kRowBytes = D * (FP8 ? 1 : 2);       // one row of a Q, K or V tile
+  static constexpr int kBoxes = kRowBytes / 128;            // 128-byte-wide TMA boxes per row
+  static constexpr int kBoxBytes = kBlockK * 128;           // 16 KB: 128 rows x 128 bytes
+  static constexpr int kTileBytes = kBlockK * kRowBytes;    // one Q, K or V tile
+  static constexpr int kKSteps = kRowBytes / 32;            // MMA K-steps of 32 bytes over d
+  static constexpr int kQBytes = kBlockQ * D * 2;           // per query tile: Q, later the bf16 O staging
+  static constexpr int kOBoxes = D * 2 / 128;               // 128-byte boxes per bf16 O row
+  static constexpr int kSlots = kTileBytes == 32768 ? 4 : 8;
   static constexpr int kQOff = 0;                           // Q_a, Q_b
-  static constexpr int kRingOff = kTiles * kTileBytes;
+  static constexpr int kRingOff = kTiles * kQBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
   // q_full[2], full[kSlots], empty[kSlots], s_full[2], p_full[2], o_done[2], epi[2], drain
   static constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1;
@@ -97,13 +104,22 @@ __device__ __forceinline__ int kv_blocks(int u, int t, int N) {
   return CAUSAL ? min(row0 / kBlockK + 1, nkt_all) : nkt_all;
 }
 
-template <int D, bool CAUSAL>
+// Dequantisation scales of the FP8 variant (unused by the bf16 one): per
+// 64-row tile of each head, [BH, ntiles].
+struct Fp8Scales {
+  const float* sq;
+  const float* sk;
+  const float* sv;
+  int ntiles;
+};
+
+template <int D, bool CAUSAL, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
-    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    float* __restrict__ lse, int N, int BH, int nunits, float scale_log2, unsigned int* err_word,
-                    unsigned long long wait_ns, int fault) {
-  using C = FwdCfg<D>;
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               float* __restrict__ lse, int N, int BH, int nunits, float scale_log2, unsigned int* err_word,
+               unsigned long long wait_ns, int fault, Fp8Scales f8) {
+  using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::kQOff;
@@ -177,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bar_q[t], C::kTileBytes);
 #pragma unroll
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(sQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, &bar_q[t], b * kBoxCols,
+          tma_load_3d(sQ + t * C::kQBytes + b * C::kBoxBytes, &tm_q, &bar_q[t], b * kBoxCols,
                       u * kRowsPerCta + t * kBlockQ, bh);
       }
       // Ring order = MMA first-use order: K0, V0, K1, V1, ...
@@ -190,9 +206,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (fault == 1 && tm == &tm_k && j == 1) return false;  // test-only: K block 1 never arrives
         mbar_arrive_expect_tx(&bar_full[slot], C::kTileBytes);
         uint8_t* dst = sRing + slot * C::kTileBytes;
+        if (FP8 && tm == &tm_v) {
+          // V^T codes [d rows][keys]: one 128-key x d-row box at key offset j * 128.
+          tma_load_3d(dst, tm, &bar_full[slot], j * kBlockK, 0, bh);
+        } else {
 #pragma unroll
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(dst + b * C::kBoxBytes, tm, &bar_full[slot], b * kBoxCols, j * kBlockK, bh);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(dst + b * C::kBoxBytes, tm, &bar_full[slot], b * kBoxCols, j * kBlockK, bh);
+        }
         ++issued;
         return true;
       };
@@ -212,8 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockQ, kBlockK, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockQ, D, 0, 1);
+      constexpr uint32_t idesc_qk =
+          FP8 ? idesc_e4m3_f32(kBlockQ, kBlockK, 0, 0) : idesc_bf16_f32(kBlockQ, kBlockK, 0, 0);
+      constexpr uint32_t idesc_pv = FP8 ? idesc_e4m3_f32(kBlockQ, D, 0, 0) : idesc_bf16_f32(kBlockQ, D, 0, 1);
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t ring_addr = smem_u32(sRing);
       const int nq[kTiles] = {n_a, n_b};
@@ -224,16 +246,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // compile-time byte offset (a single 32-bit add on the issuing thread).
       const uint64_t qdesc = sdesc_sw128(q_addr, 16, 1024);          // K-major, SBO = 8 rows x 128 B
       const uint64_t kdesc = sdesc_sw128(ring_addr, 16, 1024);       // K-major view of a ring slot
-      const uint64_t vdesc = sdesc_sw128(ring_addr, C::kBoxBytes, 1024);  // MN-major view, LBO = one box
+      // bf16: V is MN-major (LBO = one box); FP8: V^T is K-major like K.
+      const uint64_t vdesc = sdesc_sw128(ring_addr, FP8 ? 16 : C::kBoxBytes, 1024);
 
       // S_t = Q_t K^T : both operands K-major (d contiguous), 16 d-columns per MMA.
       auto qk = [&](int t, int slot) {
-        const uint64_t qd = sdesc_add(qdesc, t * C::kTileBytes);
+        const uint64_t qd = sdesc_add(qdesc, t * C::kQBytes);
         const uint64_t kd = sdesc_add(kdesc, slot * C::kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < C::kKSteps; ++kk) {
           const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-          mma_bf16_ss(tmem + C::col_s(t), sdesc_add(qd, off), sdesc_add(kd, off), idesc_qk, kk > 0 ? 1u : 0u);
+          if constexpr (FP8)
+            mma_e4m3_ss(tmem + C::col_s(t), sdesc_add(qd, off), sdesc_add(kd, off), idesc_qk, kk > 0 ? 1u : 0u);
+          else
+            mma_bf16_ss(tmem + C::col_s(t), sdesc_add(qd, off), sdesc_add(kd, off), idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar_s[t]);
       };
@@ -242,10 +268,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // per TMA box (LBO = one box).
       auto pv = [&](int t, int slot, bool accumulate) {
         const uint64_t vd = sdesc_add(vdesc, slot * C::kTileBytes);
+        if constexpr (FP8) {
+          // A = P (e4m3, 4 per TMEM column), 32 keys per MMA; B = V^T K-major, 32 key bytes per step.
 #pragma unroll
-        for (int kk = 0; kk < kBlockK / 16; ++kk)
-          mma_bf16_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, sdesc_add(vd, kk * 16 * 128), idesc_pv,
-                      (accumulate || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBlockK / 32; ++kk)
+            mma_e4m3_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, sdesc_add(vd, kk * 32), idesc_pv,
+                        (accumulate || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kBlockK / 16; ++kk)
+            mma_bf16_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, sdesc_add(vd, kk * 16 * 128), idesc_pv,
+                        (accumulate || kk > 0) ? 1u : 0u);
+        }
       };
 
       // Prologue: S_a = Q_a K_0^T, S_b = Q_b K_0^T.
@@ -317,10 +351,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t col_s = C::col_s(t);
     const uint32_t col_o = C::col_o(t);
-    const float2 c2 = make_float2(scale_log2, scale_log2);
     float m_used = -INFINITY;  // running maximum in log2 units (possibly stale, see header)
     float l = 0.f;
     bool ok = true;
+    // FP8: the row's Q scale joins the score scale; V scales are folded into P
+    // relative to the head's largest V scale (so P stays <= 256 in e4m3) and
+    // undone in the epilogue.
+    float crow = scale_log2, inv_svmax = 1.f, svmax = 1.f;
+    const float* skh = nullptr;
+    const float* svh = nullptr;
+    if constexpr (FP8) {
+      const size_t hb = static_cast<size_t>(bh) * f8.ntiles;
+      skh = f8.sk + hb;
+      svh = f8.sv + hb;
+      float mxv = 0.f;
+      for (int i = lane; i < f8.ntiles; i += 32) mxv = fmaxf(mxv, svh[i]);
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) mxv = fmaxf(mxv, __shfl_xor_sync(0xffffffffu, mxv, m));
+      svmax = mxv;
+      inv_svmax = 1.f / mxv;
+      crow = scale_log2 * (qrow < N ? f8.sq[hb + qrow / 64] : 1.f);
+    }
 
     for (int j = 0; j < nkt; ++j) {
       if (!warp_wait(&bar_s[t], j & 1, wc, kSiteSoftS)) {
@@ -355,8 +406,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 1; i < 31; i += 2) a = max3(a, __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
         mx[c] = fmaxf(a, __uint_as_float(r[c][31]));
       }
-      const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      const float m_new = fmaxf(m_used, rmax * scale_log2);
+      // Per 64-key half h: multiplier c[h] of the raw score (FP8: times that key
+      // tile's K scale) and lg[h] = log2 of the V-scale fold of P (0 for bf16).
+      float ch[2] = {crow, crow}, lg[2] = {0.f, 0.f}, fv[2] = {1.f, 1.f};
+      if constexpr (FP8) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int kt = 2 * j + h;
+          if (kt < f8.ntiles) {
+            ch[h] = crow * skh[kt];
+            fv[h] = svh[kt] * inv_svmax;
+            lg[h] = __log2f(fv[h]);
+          }
+        }
+      }
+      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]) * ch[0], fmaxf(mx[2], mx[3]) * ch[1]);
+      const float m_new = fmaxf(m_used, m_tile);
 
       if (j == 0) {
         m_used = (m_new == -INFINITY) ? 0.f : m_new;
@@ -388,25 +453,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
-      // P = exp2(S * scale * log2(e) - m), packed to bf16 pairs over the S buffer:
-      // keys 32c..32c+31 become TMEM columns 16c..16c+15 of this tile's S region.
-      const float2 nm2 = make_float2(-m_used, -m_used);
+      // P = exp2(S * c - m) written back over the S buffer.  bf16: keys
+      // 32c..32c+31 become TMEM columns 16c..16c+15 (2 per column).  FP8: P * fv
+      // (the V-scale fold) as e4m3, 4 per column, keys 64h..64h+63 in columns
+      // 16h..16h+15.
       float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      uint32_t pk8[16];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
+        const int h = c >> 1;
+        const float2 c2 = make_float2(ch[h], ch[h]);
+        const float2 b2 = make_float2(lg[h] - m_used, lg[h] - m_used);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float2 x =
-              __ffma2_rn(make_float2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), c2, nm2);
+              __ffma2_rn(make_float2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), c2, b2);
           const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          part[i & 1] = __fadd2_rn(part[i & 1], p);
-          pk[i] = pack_bf16x2(p.x, p.y);
+          part[h] = __fadd2_rn(part[h], p);
+          if constexpr (FP8)
+            pk[i] = e4m3x2_bits(p.x, p.y);
+          else
+            pk[i] = pack_bf16x2(p.x, p.y);
         }
-        tmem_st16(trow + col_s + c * 16, pk);
+        if constexpr (FP8) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) pk8[(c & 1) * 8 + i] = pk[2 * i] | (pk[2 * i + 1] << 16);
+          if (c & 1) tmem_st16(trow + col_s + h * 16, pk8);
+        } else {
+          tmem_st16(trow + col_s + c * 16, pk);
+        }
       }
-      const float2 ps = __fadd2_rn(part[0], part[1]);
-      l += ps.x + ps.y;
+      // l counts the unscaled P: undo the V-scale fold of each half.
+      l += (part[0].x + part[0].y) / fv[0] + (part[1].x + part[1].y) / fv[1];
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -417,11 +496,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && nkt > 0) ok = warp_wait(&bar_o[t], 0, wc, kSiteSoftO);
     if (ok && nkt > 0) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = svmax / l;  // svmax = 1 for bf16
       const float2 il2 = make_float2(inv_l, inv_l);
       // O row -> bf16 -> this tile's Q staging area (free: its last Q K^T MMA has
       // completed), laid out exactly as the 128-byte-swizzled TMA box expects.
-      uint8_t* sQt = sQ + t * C::kTileBytes;
+      uint8_t* sQt = sQ + t * C::kQBytes;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -447,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (qrow < N) lse[static_cast<size_t>(bh) * N + qrow] = (m_used + log2f(l)) * kLn2;
       if (row == 0 && mbar_wait(&bar_epi[t], 0, wc, kSiteEpi)) {
 #pragma unroll
-        for (int b = 0; b < C::kBoxes; ++b)
+        for (int b = 0; b < C::kOBoxes; ++b)
           tma_store_3d(&tm_o, sQt + b * C::kBoxBytes, b * kBoxCols, qrow0, bh);
         tma_store_commit_and_wait_read();
       }
@@ -463,17 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
-cudaError_t launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
-  using C = FwdCfg<D>;
-  const int BH = a.B * a.H;
-  CUtensorMap tq, tk, tv, to;
+template <int D, bool CAUSAL, bool FP8>
+cudaError_t launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                          float* lse, int N, int BH, float scale_log2, unsigned int* err_word, const DebugKnobs& dbg,
+                          const Fp8Scales& f8, cudaStream_t stream) {
+  using C = FwdCfg<D, FP8>;
   cudaError_t e;
-  if ((e = make_tmap_3d(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockQ))) return e;
-  if ((e = make_tmap_3d(&tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockK))) return e;
-  if ((e = make_tmap_3d(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockK))) return e;
-  if ((e = make_tmap_3d(&to, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockQ))) return e;
-  auto kern = fwd_bf16_kernel<D, CAUSAL>;
+  auto kern = fwd_kernel<D, CAUSAL, FP8>;
   // Per device and idempotent; cheap enough to repeat on every launch.
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes))) return e;
   // setmaxnreg.inc can only draw on the registers the block was launched with; a
@@ -481,12 +556,44 @@ cudaError_t launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
   cudaFuncAttributes fattr;
   if ((e = cudaFuncGetAttributes(&fattr, kern))) return e;
   if (static_cast<uint32_t>(fattr.numRegs) * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
-  const int nunits = (a.N + kRowsPerCta - 1) / kRowsPerCta;
-  const float scale_log2 = a.scale * 1.4426950408889634f;
+  const int nunits = (N + kRowsPerCta - 1) / kRowsPerCta;
   dim3 grid(static_cast<unsigned>(nunits * BH));
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, a.lse, a.N, BH, nunits, scale_log2, a.err_word,
-                                                   a.dbg.wait_limit_ns, a.dbg.fault);
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, lse, N, BH, nunits, scale_log2, err_word,
+                                                   dbg.wait_limit_ns, dbg.fault, f8);
   return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  CUtensorMap tq, tk, tv, to;
+  cudaError_t e;
+  if ((e = make_tmap_3d(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockQ))) return e;
+  if ((e = make_tmap_3d(&tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockK))) return e;
+  if ((e = make_tmap_3d(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockK))) return e;
+  if ((e = make_tmap_3d(&to, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockQ))) return e;
+  return launch_kernel<D, CAUSAL, false>(tq, tk, tv, to, a.lse, a.N, BH, a.scale * 1.4426950408889634f, a.err_word,
+                                         a.dbg, Fp8Scales{nullptr, nullptr, nullptr, 0}, stream);
+}
+
+template <bool CAUSAL>
+cudaError_t launch_fwd_fp8_impl(const FwdArgs& a, const void* workspace, cudaStream_t stream) {
+  constexpr int D = 128;
+  const int BH = a.B * a.H;
+  const Fp8Layout lay = fp8_layout(a.B, a.H, a.N, D);
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  CUtensorMap tq, tk, tv, to;
+  cudaError_t e;
+  if ((e = make_tmap_3d(&tq, ws + lay.off_q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D, a.N, BH, 128, kBlockQ))) return e;
+  if ((e = make_tmap_3d(&tk, ws + lay.off_k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D, a.N, BH, 128, kBlockK))) return e;
+  if ((e = make_tmap_3d(&tv, ws + lay.off_v8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, lay.npad, D, BH, kBlockK, D)))
+    return e;
+  if ((e = make_tmap_3d(&to, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockQ))) return e;
+  const Fp8Scales f8{reinterpret_cast<const float*>(ws + lay.off_sq), reinterpret_cast<const float*>(ws + lay.off_sk),
+                     reinterpret_cast<const float*>(ws + lay.off_sv), lay.ntiles};
+  // Scores of the rotated operands are d times the plain ones: fold 1/d into the scale.
+  const float scale_log2 = a.scale * 1.4426950408889634f / static_cast<float>(D);
+  return launch_kernel<D, CAUSAL, true>(tq, tk, tv, to, a.lse, a.N, BH, scale_log2, a.err_word, a.dbg, f8, stream);
 }
 
 }  // namespace
@@ -494,6 +601,10 @@ cudaError_t launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream) {
   if (a.d == 64) return a.causal ? launch_fwd_impl<64, true>(a, stream) : launch_fwd_impl<64, false>(a, stream);
   return a.causal ? launch_fwd_impl<128, true>(a, stream) : launch_fwd_impl<128, false>(a, stream);
+}
+
+cudaError_t launch_fwd_fp8(const FwdArgs& a, const void* workspace, cudaStream_t stream) {
+  return a.causal ? launch_fwd_fp8_impl<true>(a, workspace, stream) : launch_fwd_fp8_impl<false>(a, workspace, stream);
 }
 
 }  // namespace fa

@@ -72,6 +72,32 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream);
 
+// Workspace of the FP8 path (written by fa_fp8_prepare, read by fa_fwd_fp8):
+// e4m3 codes of the rotated Q and K, row-major [BH, N, d]; e4m3 codes of V
+// transposed [BH, d, npad] (keys contiguous, npad = N rounded up to 128); fp32
+// dequantisation scales per 64-row tile [BH, ntiles] for Q, K, V.  Every region
+// starts on a 256-byte boundary.
+struct Fp8Layout {
+  size_t off_q8, off_k8, off_v8t, off_sq, off_sk, off_sv, total;
+  int ntiles, npad;
+};
+Fp8Layout fp8_layout(int B, int H, int N, int d);
+
+// FP8 forward launcher (fa_fwd.cu): reads the prepared workspace (q, k, v of
+// FwdArgs unused), writes bf16 O and fp32 LSE; d = 128.
+cudaError_t launch_fwd_fp8(const FwdArgs& a, const void* workspace, cudaStream_t stream);
+
+struct Fp8PrepArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int in_bf16;             // 0: fp32 inputs, 1: bf16 inputs
+  const int8_t* signs;     // [d], the sign of each entry is used
+  void* workspace;
+  int B, H, N, d;
+};
+cudaError_t launch_fp8_prepare(const Fp8PrepArgs& a, cudaStream_t stream);
+
 // Encodes a 3-D tiled tensor map over a [BH, N, cols] row-major tensor with
 // `elem_bytes`-byte elements, box {box_cols, box_rows, 1}, 128-byte swizzle.
 // Implemented in fa_api.cu (driver entry point resolved once).
