@@ -4,11 +4,14 @@
 
 Workload (the configuration the headline metric is quoted on): bf16 attention,
 B=4, H=16, N=2048, d=128, scale 1/sqrt(d), non-causal, Q, K, V, dO ~ N(0,1) from
-seed 2.  One step = one pass of the whole bf16 hot path over that batch: the
-forward (fa_fwd) and the backward's three stages (fa_bwd_prep, fa_bwd_main,
-fa_bwd_dq), four launches.  TFLOP/s counts 4*B*H*N^2*d per forward and 2.5 times
-that per backward.  Each stage is bracketed by its own CUDA events, which give
-the per-kernel rooflines.
+seed 2.  One step = one pass of the whole hot path over that batch, six
+launches: the bf16 forward (fa_fwd), the backward's three stages (fa_bwd_prep,
+fa_bwd_main, fa_bwd_dq), and the FP8 path on the same Q, K, V (fa_fp8_prepare
+with seeded rotation signs, fa_fwd_fp8).  TFLOP/s counts 4*B*H*N^2*d per forward
+(bf16 or FP8) and 2.5 times that per backward.  `frac_of_peak` is the time the
+step's work would take at the measured peaks (bf16 FLOPs at the bf16 peak, FP8
+FLOPs at twice it, the nominal ratio) over the measured time.  Each stage is
+bracketed by its own CUDA events, which give the per-kernel rooflines.
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides.  L2 (129 MB) is flushed before every
@@ -158,7 +161,7 @@ def run_ours(args):
     import torch
 
     import io_aware_exact_fwd_gb300 as fa
-    from synth import normal_qkv
+    from synth import normal_qkv, rotation_signs
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -176,16 +179,22 @@ def run_ours(args):
     lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    ws8 = torch.empty(fa.fa_fp8_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    signs = rotation_signs(d, w["seed"]).cuda()
+    o8 = torch.empty_like(q)
+    lse8 = torch.empty_like(lse)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
-    stages = ("fwd", "bwd_prep", "bwd_main", "bwd_dq")
+    stages = ("fwd", "bwd_prep", "bwd_main", "bwd_dq", "fp8_prep", "fwd_fp8")
     calls = {
         "fwd": lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale),
         "bwd_prep": lambda: fa.fa_bwd_prep(o, g, lse, ws),
         "bwd_main": lambda: fa.fa_bwd_main(q, k, v, g, dk, dv, ws, causal=causal, scale=scale),
         "bwd_dq": lambda: fa.fa_bwd_dq(ws, dq, scale=scale),
+        "fp8_prep": lambda: fa.fa_fp8_prepare(q, k, v, signs, ws8),
+        "fwd_fp8": lambda: fa.fa_fwd_fp8(ws8, (B, H, N, d), o=o8, lse=lse8, causal=causal, scale=scale),
     }
-    launches_per_step = 4
+    launches_per_step = 6
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -225,22 +234,25 @@ def run_ours(args):
         torch.distributed.barrier()
         dev_ms = float(t.item())
     f_fwd = fwd_flops(B, H, N, d, causal)
-    flops_step = 3.5 * f_fwd
+    flops_step = 4.5 * f_fwd  # bf16 forward + backward (2.5x) + FP8 forward
     ms_per_step = dev_ms / args.steps
     value = flops_step * args.steps * world / (dev_ms * 1e-3) / 1e12
 
     # End to end through the public calls: pinned host inputs in, every output back out.
     hq, hk, hv, hg = (t.cpu().pin_memory() for t in (q, k, v, g))
-    outs = (o, lse, dq, dk, dv)
-    houts = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
     dq_in, dk_in, dv_in, dg_in = (torch.empty_like(t) for t in (q, k, v, g))
     e2e_steps = max(3, min(args.steps, 50))
+
+    outs = (o, lse, dq, dk, dv, o8, lse8)
+    houts = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
 
     def e2e_step():
         for dst, src in zip((dq_in, dk_in, dv_in, dg_in), (hq, hk, hv, hg)):
             dst.copy_(src, non_blocking=True)
         fa.fa_fwd(dq_in, dk_in, dv_in, o=o, lse=lse, causal=causal, scale=scale)
         fa.fa_bwd(dq_in, dk_in, dv_in, o, dg_in, lse, dq, dk, dv, ws, causal=causal, scale=scale)
+        fa.fa_fp8_prepare(dq_in, dk_in, dv_in, signs, ws8)
+        fa.fa_fwd_fp8(ws8, (B, H, N, d), o=o8, lse=lse8, causal=causal, scale=scale)
         for dst, src in zip(houts, outs):
             dst.copy_(src, non_blocking=True)
 
@@ -280,22 +292,26 @@ def run_ours(args):
                      "kernel": "bwd_main_kernel<false>", "profile": "bwd_main_B4H16N2048d128.md",
                      "source": "io_aware_exact_fwd_gb300/csrc/fa_bwd.cu"},
         "bwd_dq": {"bound": "hbm", "flops": 0.0, "bytes": 4 * elems + 2 * elems, "kernel": "bwd_dq_convert_kernel"},
+        "fp8_prep": {"bound": "hbm", "flops": 0.0, "bytes": 3 * 2 * elems + 3 * elems, "kernel": "fp8_prepare_kernel<128>"},
+        "fwd_fp8": {"bound": "tensor_fp8", "flops": f_fwd, "bytes": 3 * elems + 2 * elems + 4 * B * H * N,
+                    "kernel": "fwd_kernel<128,false,fp8>"},
     }
     per_stage = {}
     for st in stages:
         info, ms = stage_info[st], stage_ms[st]
         tf = info["flops"] / (ms * 1e-3) / 1e12
         gbs = info["bytes"] / (ms * 1e-3) / 1e9
-        if info["bound"] == "tensor":
-            per_stage[st] = {"ms": round(ms, 5), "bound": "tensor", "achieved": round(tf, 1), "unit": "TFLOP/s",
-                             "frac": round(tf / peak, 4), "gbs": round(gbs, 1)}
+        if info["bound"] in ("tensor", "tensor_fp8"):
+            pk = peak if info["bound"] == "tensor" else 2.0 * peak
+            per_stage[st] = {"ms": round(ms, 5), "bound": info["bound"], "achieved": round(tf, 1),
+                             "unit": "TFLOP/s", "frac": round(tf / pk, 4), "peak": pk, "gbs": round(gbs, 1)}
         else:
             per_stage[st] = {"ms": round(ms, 5), "bound": "hbm", "achieved": round(gbs, 1), "unit": "GB/s",
                              "frac": round(gbs / hbm, 4)}
     dom = max(stages, key=lambda st: stage_ms[st])
     di = stage_info[dom]
     dom_ach = per_stage[dom]["achieved"]
-    dom_peak = peak if di["bound"] == "tensor" else hbm
+    dom_peak = {"tensor": peak, "tensor_fp8": 2.0 * peak, "hbm": hbm}[di["bound"]]
     traffic = None
     if args.traffic is not None:
         traffic = args.traffic
@@ -303,8 +319,9 @@ def run_ours(args):
         traffic = profile_traffic(di["profile"], di["source"])
     roofline = {
         "bound": di["bound"], "kernel": di["kernel"], "achieved": dom_ach, "peak": dom_peak,
-        "peak_source": (f"{peaks['source']} bf16_tflops (burst, cuBLAS)" if di["bound"] == "tensor"
-                        else f"{peaks['source']} hbm_gbs (copy)"),
+        "peak_source": {"tensor": f"{peaks['source']} bf16_tflops (burst, cuBLAS)",
+                        "tensor_fp8": f"2 x {peaks['source']} bf16_tflops (FP8/BF16 nominal ratio)",
+                        "hbm": f"{peaks['source']} hbm_gbs (copy)"}[di["bound"]],
         "unit": per_stage[dom]["unit"], "frac": round(dom_ach / dom_peak, 4), "traffic": traffic,
         "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
         "algorithmic_flops_per_launch": di["flops"], "algorithmic_bytes_per_launch": di["bytes"],
@@ -319,7 +336,7 @@ def run_ours(args):
         "config": dict(WORKLOAD, l2="flushed before every step (256 MB write, outside the timed event pairs)",
                        parallelism=f"replicas x{world}" if world > 1 else "single GPU",
                        flops_per_step=flops_step),
-        "frac_of_peak": round(value / world / peak, 4),
+        "frac_of_peak": round((3.5 * f_fwd / peak + f_fwd / (2.0 * peak)) / 1e12 / (ms_per_step * 1e-3), 4),
         "roofline": roofline,
         "stages": per_stage,
         "e2e": {"value": round(flops_step / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
@@ -351,7 +368,7 @@ def _oracle_step_sample(q, k, v, g, scale, causal, head, r0, rows_per_step):
 def _oracle_inputs():
     import torch
 
-    from synth import normal_qkv
+    from synth import normal_qkv, rotation_signs
 
     w = WORKLOAD
     x = normal_qkv(1, 2, w["N"], w["d"], w["seed"], with_do=True)
