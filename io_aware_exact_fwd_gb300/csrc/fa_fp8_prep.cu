@@ -95,6 +95,18 @@ __device__ __forceinline__ void fwht_row(float (&x)[D / 32], int lane) {
   }
 }
 
+// Block-wide max of a per-thread value (8 warps).
+__device__ __forceinline__ float block_amax(float amax, float* s_amax, int warp, int lane) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  if (lane == 0) s_amax[warp] = amax;
+  __syncthreads();
+  amax = s_amax[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_amax[w]);
+  return amax;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* __restrict__ q,
                                                                    const void* __restrict__ k,
@@ -103,58 +115,97 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
                                                                    Fp8Layout lay, uint8_t* __restrict__ ws, int N) {
   constexpr int E = D / 32;
   constexpr int kRowsPerWarp = kTileRows / 8;
+  constexpr int kVtPitch = kTileRows + 4;  // 17 words per d-row: byte stores of 32 lanes hit 32 banks
   const int tile = blockIdx.x;
   const int bh = blockIdx.y;
   const int which = blockIdx.z;  // 0 = Q, 1 = K, 2 = V
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const void* src = which == 0 ? q : (which == 1 ? k : v);
+  const int ntiles = lay.ntiles;
   __shared__ float s_amax[8];
-  __shared__ uint8_t s_vt[D * kTileRows];  // V codes of this tile, transposed [d][64]
+  __shared__ __align__(16) uint8_t s_vt[D * kVtPitch];  // V codes of this tile, transposed [d][64 (+4)]
 
+  float x[kRowsPerWarp][E];
+  if (which == 2) {
+    // ------------------------------------------------ V: no rotation, transposed out
+    // Lane l holds columns l, l + 32, ... of each row (coalesced loads).
+    float amax = 0.f;
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const int row = tile * kTileRows + warp * kRowsPerWarp + r;
+#pragma unroll
+      for (int m = 0; m < E; ++m) {
+        float val = 0.f;
+        if (row < N) {
+          const size_t e = (static_cast<size_t>(bh) * N + row) * D + lane + 32 * m;
+          val = in_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(v)[e]) : static_cast<const float*>(v)[e];
+        }
+        x[r][m] = val;
+        amax = fmaxf(amax, fabsf(val));
+      }
+    }
+    amax = block_amax(amax, s_amax, warp, lane);
+    const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+    const float sigma = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    if (threadIdx.x == 0 && tile < ntiles)
+      reinterpret_cast<float*>(ws + lay.off_sv)[static_cast<size_t>(bh) * ntiles + tile] = sigma;
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const int lrow = warp * kRowsPerWarp + r;
+#pragma unroll
+      for (int m = 0; m < E; m += 2) {
+        const uint16_t two = e4m3x2(__fmul_rn(x[r][m], inv), __fmul_rn(x[r][m + 1], inv));
+        s_vt[(lane + 32 * m) * kVtPitch + lrow] = static_cast<uint8_t>(two & 0xff);
+        s_vt[(lane + 32 * (m + 1)) * kVtPitch + lrow] = static_cast<uint8_t>(two >> 8);
+      }
+    }
+    __syncthreads();
+    // [d][64] tile -> V^T rows of 64 contiguous key bytes, 4 bytes per store.
+    uint8_t* vt = ws + lay.off_v8t + static_cast<size_t>(bh) * D * lay.npad + static_cast<size_t>(tile) * kTileRows;
+    for (int idx = threadIdx.x; idx < D * (kTileRows / 4); idx += kPrepThreads) {
+      const int drow = idx / (kTileRows / 4);
+      const int word = idx % (kTileRows / 4);
+      *reinterpret_cast<uint32_t*>(vt + static_cast<size_t>(drow) * lay.npad + word * 4) =
+          *reinterpret_cast<const uint32_t*>(s_vt + drow * kVtPitch + word * 4);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------ Q, K: rotate, then quantise
+  if (tile >= ntiles) return;  // blocks past the last tile exist only to pad V^T
   float sgn[E];
 #pragma unroll
   for (int i = 0; i < E; ++i) sgn[i] = signs[E * lane + i] < 0 ? -1.f : 1.f;
-
-  float x[kRowsPerWarp][E];
+  const void* src = which == 0 ? q : k;
   float amax = 0.f;
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r) {
     const int row = tile * kTileRows + warp * kRowsPerWarp + r;
     if (row < N) {
       load_row<D>(src, (static_cast<size_t>(bh) * N + row) * D + E * lane, in_bf16, x[r]);
-      if (which < 2) {
-#pragma unroll
-        for (int i = 0; i < E; ++i) x[r][i] *= sgn[i];
-        fwht_row<D>(x[r], lane);
-      }
     } else {
 #pragma unroll
       for (int i = 0; i < E; ++i) x[r][i] = 0.f;
     }
-#pragma unroll
-    for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(x[r][i]));
-  }
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-  if (lane == 0) s_amax[warp] = amax;
-  __syncthreads();
-  amax = s_amax[0];
-#pragma unroll
-  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_amax[w]);
-  const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
-  const float sigma = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-
-  const int ntiles = lay.ntiles;
-  if (tile >= ntiles && which < 2) return;  // blocks past the last tile only pad V^T with zeros
-  if (threadIdx.x == 0 && tile < ntiles) {
-    float* sc = reinterpret_cast<float*>(ws + (which == 0 ? lay.off_sq : (which == 1 ? lay.off_sk : lay.off_sv)));
-    sc[static_cast<size_t>(bh) * ntiles + tile] = sigma;
   }
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int lrow = warp * kRowsPerWarp + r;
-    const int row = tile * kTileRows + lrow;
+#pragma unroll
+    for (int i = 0; i < E; ++i) x[r][i] *= sgn[i];
+    fwht_row<D>(x[r], lane);
+#pragma unroll
+    for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(x[r][i]));
+  }
+  amax = block_amax(amax, s_amax, warp, lane);
+  const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+  const float sigma = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  if (threadIdx.x == 0)
+    reinterpret_cast<float*>(ws + (which == 0 ? lay.off_sq : lay.off_sk))[static_cast<size_t>(bh) * ntiles + tile] =
+        sigma;
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int row = tile * kTileRows + warp * kRowsPerWarp + r;
+    if (row >= N) continue;
     uint8_t c[E];
 #pragma unroll
     for (int i = 0; i < E; i += 2) {
@@ -162,29 +213,11 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
       c[i] = static_cast<uint8_t>(two & 0xff);
       c[i + 1] = static_cast<uint8_t>(two >> 8);
     }
-    if (which < 2) {
-      if (row < N) {
-        uint8_t* dst = ws + (which == 0 ? lay.off_q8 : lay.off_k8) + (static_cast<size_t>(bh) * N + row) * D + E * lane;
-        if (E == 4)
-          *reinterpret_cast<uint32_t*>(dst) = c[0] | (c[1 % E] << 8) | (c[2 % E] << 16) | (c[3 % E] << 24);
-        else
-          *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(c[0] | (c[1 % E] << 8));
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < E; ++i) s_vt[(E * lane + i) * kTileRows + lrow] = c[i];
-    }
-  }
-  if (which == 2) {
-    __syncthreads();
-    // [d][64] tile -> V^T rows: 64 contiguous key bytes per d-row (16 bytes per thread).
-    uint8_t* vt = ws + lay.off_v8t + static_cast<size_t>(bh) * D * lay.npad + static_cast<size_t>(tile) * kTileRows;
-    for (int idx = threadIdx.x; idx < D * 4; idx += kPrepThreads) {
-      const int drow = idx >> 2;
-      const int part = idx & 3;
-      *reinterpret_cast<uint4*>(vt + static_cast<size_t>(drow) * lay.npad + part * 16) =
-          *reinterpret_cast<const uint4*>(s_vt + drow * kTileRows + part * 16);
-    }
+    uint8_t* dst = ws + (which == 0 ? lay.off_q8 : lay.off_k8) + (static_cast<size_t>(bh) * N + row) * D + E * lane;
+    if (E == 4)
+      *reinterpret_cast<uint32_t*>(dst) = c[0] | (c[1 % E] << 8) | (c[2 % E] << 16) | (c[3 % E] << 24);
+    else
+      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(c[0] | (c[1 % E] << 8));
   }
 }
 

@@ -51,7 +51,13 @@ constexpr uint32_t kRegsControl = 72;
 constexpr uint32_t kRegsNeeded = 2 * 128 * kRegsSoftmax + 128 * kRegsControl;
 static_assert(kRegsNeeded <= 65536, "register split exceeds the SM register file");
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: stale-max exponentials stay <= 256
+// A key block is exponentiated against the running maximum without computing
+// its own; the result is kept if the block's row sum is at most this bound
+// (then every P <= 2^16, far from fp32 overflow even after accumulation).
+constexpr float kSpeculationSumBound = 65536.0f;
+// FP8 keeps a per-block maximum and moves its reference only when a block's
+// maximum exceeds it by more than 2^8 (log2 units), so P <= 256 < 448 (e4m3).
+constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 // Sites recorded in the error word when a wait expires.
@@ -379,33 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(trow + col_s + c * 32, r[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait32(r[c]);
-
       const int kbase = j * kBlockK;
       const bool need_mask = (kbase + kBlockK > N) || (CAUSAL && j == diag);
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int key = kbase + c * 32 + i;
-            const bool masked = key >= N || (CAUSAL && key > qrow);
-            if (masked) r[c][i] = __float_as_uint(-INFINITY);
-          }
-      }
-      // Row maximum of the raw scores (scale > 0, so scaling commutes with max).
-      float mx[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float a = __uint_as_float(r[c][0]);
-#pragma unroll
-        for (int i = 1; i < 31; i += 2) a = max3(a, __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
-        mx[c] = fmaxf(a, __uint_as_float(r[c][31]));
-      }
       // Per 64-key half h: multiplier c[h] of the raw score (FP8: times that key
       // tile's K scale) and lg[h] = log2 of the V-scale fold of P (0 for bf16).
       float ch[2] = {crow, crow}, lg[2] = {0.f, 0.f}, fv[2] = {1.f, 1.f};
@@ -420,47 +401,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]) * ch[0], fmaxf(mx[2], mx[3]) * ch[1]);
-      const float m_new = fmaxf(m_used, m_tile);
-
-      if (j == 0) {
-        m_used = (m_new == -INFINITY) ? 0.f : m_new;
-      } else {
-        const bool need = m_new > m_used + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          // O_t already holds P V up to block j-1: Q K_j^T was issued after that P V.
-          float alpha = 1.f;
-          if (need) {
-            alpha = ex2_approx(m_used - m_new);
-            m_used = m_new;
-          }
-          l *= alpha;
-          const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(trow + col_o + c * 32, o);
-            tmem_ld_wait32(o);
+      uint32_t r[4][32];
+      auto load_and_mask = [&](int c) {
+        if (need_mask) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
-              o[i] = __float_as_uint(v.x);
-              o[i + 1] = __float_as_uint(v.y);
-            }
-            tmem_st32(trow + col_o + c * 32, o);
+          for (int i = 0; i < 32; ++i) {
+            const int key = kbase + c * 32 + i;
+            if (key >= N || (CAUSAL && key > qrow)) r[c][i] = __float_as_uint(-INFINITY);
           }
-          tmem_st_wait();
         }
-      }
-
-      // P = exp2(S * c - m) written back over the S buffer.  bf16: keys
-      // 32c..32c+31 become TMEM columns 16c..16c+15 (2 per column).  FP8: P * fv
-      // (the V-scale fold) as e4m3, 4 per column, keys 64h..64h+63 in columns
-      // 16h..16h+15.
-      float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      uint32_t pk8[16];
+      };
+      // Row maximum of the scaled scores (scale > 0: max commutes with it), as a
+      // shallow max3 tree per 32-key chunk.
+      auto tile_max = [&]() -> float {
+        float mc[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 4; ++c) {
+          float a[11];
+#pragma unroll
+          for (int i = 0; i < 10; ++i)
+            a[i] = max3(__uint_as_float(r[c][3 * i]), __uint_as_float(r[c][3 * i + 1]), __uint_as_float(r[c][3 * i + 2]));
+          a[10] = fmaxf(__uint_as_float(r[c][30]), __uint_as_float(r[c][31]));
+          const float b0 = max3(a[0], a[1], a[2]), b1 = max3(a[3], a[4], a[5]), b2 = max3(a[6], a[7], a[8]);
+          mc[c] = fmaxf(max3(b0, b1, b2), fmaxf(a[9], a[10]));
+        }
+        return fmaxf(fmaxf(mc[0], mc[1]) * ch[0], fmaxf(mc[2], mc[3]) * ch[1]);
+      };
+      // P = exp2(S * c - m) over chunk c, written back over the S buffer.  bf16:
+      // keys 32c..32c+31 become TMEM columns 16c..16c+15 (2 per column).  FP8:
+      // P * fv (the V-scale fold) as e4m3, 4 per column, keys 64h..64h+63 in
+      // columns 16h..16h+15.  Returns nothing; accumulates part[h].
+      float2 part[2];
+      uint32_t pk8[16];
+      auto exp_chunk = [&](int c) {
         const int h = c >> 1;
         const float2 c2 = make_float2(ch[h], ch[h]);
         const float2 b2 = make_float2(lg[h] - m_used, lg[h] - m_used);
@@ -483,9 +456,107 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           tmem_st16(trow + col_s + c * 16, pk);
         }
+      };
+      auto tile_sum = [&]() {
+        // l counts the unscaled P: undo the V-scale fold of each half.
+        return (part[0].x + part[0].y) / fv[0] + (part[1].x + part[1].y) / fv[1];
+      };
+
+      // O_t is rescaled (in TMEM) by alpha for rows whose reference maximum moves
+      // up; O_t already holds P V up to block j-1 because Q K_j^T was issued after it.
+      auto rescale_o = [&](float alpha, bool any) {
+        if (!any) return;
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(trow + col_o + c * 32, o);
+          tmem_ld_wait32(o);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+            o[i] = __float_as_uint(v.x);
+            o[i + 1] = __float_as_uint(v.y);
+          }
+          tmem_st32(trow + col_o + c * 32, o);
+        }
+      };
+
+      float l_tile;
+      if (j == 0 || FP8) {
+        // The block's own maximum first.  First block: it is the reference
+        // maximum.  FP8, later blocks: the reference moves up (and O is rescaled)
+        // only when the block's maximum exceeds it by more than 2^8, so every
+        // folded P stays <= 256, inside e4m3's range.  (Exponentiating before
+        // knowing the maximum, as bf16 does below, pays off only when blocks
+        // rarely overshoot; with outliers they often overshoot e4m3's 448.)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(trow + col_s + c * 32, r[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_wait32(r[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) load_and_mask(c);
+        const float mt = tile_max();
+        if (j == 0) {
+          m_used = (mt == -INFINITY) ? 0.f : mt;
+        } else {
+          const float m_new = fmaxf(m_used, mt);
+          const bool need = m_new > m_used + kRescaleThreshold;
+          float alpha = 1.f;
+          if (need) {
+            alpha = ex2_approx(m_used - m_new);
+            m_used = m_new;
+          }
+          l *= alpha;
+          rescale_o(alpha, __any_sync(0xffffffffu, need));
+        }
+        part[0] = part[1] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) exp_chunk(c);
+        l_tile = tile_sum();
+      } else {
+        // bf16, later blocks: exponentiate against the running maximum without
+        // looking for a new one.  This is exact as long as no P overflows, which
+        // the block's row sum proves (sum <= 2^16 => every P <= 2^16); otherwise
+        // the block is redone below with its own maximum.  The second half of S
+        // loads while the first half is exponentiated.
+        tmem_ld32(trow + col_s, r[0]);
+        tmem_ld32(trow + col_s + 32, r[1]);
+        tmem_ld_wait32(r[0]);
+        tmem_ld_wait32(r[1]);
+        tmem_ld32(trow + col_s + 64, r[2]);
+        tmem_ld32(trow + col_s + 96, r[3]);
+        part[0] = part[1] = make_float2(0.f, 0.f);
+        load_and_mask(0);
+        load_and_mask(1);
+        exp_chunk(0);
+        exp_chunk(1);
+        tmem_ld_wait32(r[2]);
+        tmem_ld_wait32(r[3]);
+        load_and_mask(2);
+        load_and_mask(3);
+        exp_chunk(2);
+        exp_chunk(3);
+        l_tile = tile_sum();
+        const bool bad = !(l_tile <= kSpeculationSumBound);  // also true for inf / NaN
+        if (__any_sync(0xffffffffu, bad)) {
+          tmem_st_wait();  // the speculative P has landed before it is overwritten
+          const float m_new = fmaxf(m_used, tile_max());
+          const bool need = m_new > m_used;
+          float alpha = 1.f;
+          if (need) {
+            alpha = ex2_approx(m_used - m_new);
+            m_used = m_new;
+          }
+          l *= alpha;
+          rescale_o(alpha, __any_sync(0xffffffffu, need));
+          part[0] = part[1] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) exp_chunk(c);
+          l_tile = tile_sum();
+        }
       }
-      // l counts the unscaled P: undo the V-scale fold of each half.
-      l += (part[0].x + part[0].y) / fv[0] + (part[1].x + part[1].y) / fv[1];
+      l += l_tile;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();

@@ -171,3 +171,23 @@ def test_runs_on_a_side_stream():
     fa.fa_sync_check(s)
     o_ref, _ = attention_forward(q, k, v, 128 ** -0.5, False)
     assert o_excess(o, o_ref) <= FWD_O_ATOL
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("growth", [4.0, 40.0])
+def test_row_max_jumps_between_key_blocks(growth, causal):
+    # Later key blocks carry much larger scores, so exponentials taken against the
+    # running maximum of earlier blocks grow beyond the kernel's bound (growth 4)
+    # or overflow to inf (growth 40): the kernel must redo those blocks with their
+    # own maximum and rescale O.
+    B, H, N, d = 1, 2, 640, 128
+    x = normal_qkv(B, H, N, d, 47)
+    for j in range(N // 128):
+        x["k"][:, :, j * 128:(j + 1) * 128] *= 1.0 + growth * j
+    q, k, v = to_dev_bf16(x)
+    o, lse = fa.fa_fwd(q, k, v, causal=causal)
+    fa.fa_sync_check()
+    o_ref, lse_ref = attention_forward(q, k, v, d ** -0.5, causal)
+    assert torch.isfinite(o).all()
+    assert o_excess(o, o_ref) <= FWD_O_ATOL
+    assert max_abs(lse, lse_ref) <= FWD_LSE_ATOL * max(1.0, float(np.abs(lse_ref).max()) / 100.0)
