@@ -36,9 +36,10 @@ namespace {
 constexpr int kD = 128;
 constexpr int kBkB = 128;       // keys per CTA
 constexpr int kBqB = 64;        // query rows per inner step
-constexpr int kThreads = 384;   // 0-3 compute, 4-7 dQ reduction, 8 TMA, 9 MMA, 10-11 spare
+constexpr int kThreads = 384;   // 0-3 compute, 4-7 dQ reduction, 8 TMA, 9-10 MMA issuers, 11 spare
 constexpr int kWarpLoad = 8;
-constexpr int kWarpMma = 9;
+constexpr int kWarpMma = 9;      // issues dV, dK, dQ^T (and owns the TMEM allocation)
+constexpr int kWarpMmaS = 10;    // issues S^T, dP^T
 constexpr int kStages = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_dkv, 1);
     mbar_init(bar_epi, 4);
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain, 2);  // one commit per MMA-issuing thread
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -219,8 +220,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------- MMA issuer
+  } else if (warp == kWarpMma || warp == kWarpMmaS) {
+    // ------------------------------------------------ MMA issuers (one thread each)
+    // Two threads issue MMAs so that S^T/dP^T of a later query block never waits
+    // behind dV/dK/dQ^T of an earlier one (or vice versa).  Each hazard between
+    // them is covered by a barrier: S^T(it) and dP^T(it) overwrite buffers whose
+    // previous contents (P^T, dS^T, dQ^T of it-2) were consumed by MMAs that
+    // completed before dQ^T(it-2) was read out (bar_dqe), and dV/dK/dQ^T(it)
+    // start only after the compute warps saw S^T, dP^T(it) (bar_comp).
     if (lane == 0) {
       constexpr uint32_t idesc_sdp = idesc_bf16_f32(kBkB, kBqB, 0, 0);   // keys x queries, K = d
       constexpr uint32_t idesc_dkv = idesc_bf16_f32(kBkB, kD, 0, 1);     // keys x d, K = queries
@@ -232,59 +239,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t ring_mn = sdesc_sw128(smem_u32(sRing), C::kQBox, 1024);
       const uint64_t ds_mn = sdesc_sw128(smem_u32(sDs), 16, 1024);
       bool ok = mbar_wait(bar_kv, 0, wc, kSiteBMmaKV);
-
-      // S^T = K Q_i^T and dP^T = V dO_i^T for local step `it` into buffer it & 1.
-      auto issue_sdp = [&](int it) -> bool {
-        const int slot = it % kStages;
-        const int b = it & 1;
-        if (!mbar_wait(&bar_full[slot], (it / kStages) & 1, wc, kSiteBMmaQ)) return false;
-        if (it >= 2 && !mbar_wait(&bar_dqe[b], ((it - 2) >> 1) & 1, wc, kSiteBMmaDq)) return false;
-        tc_fence_after();
-        const uint32_t st = slot * C::kStageBytes;
+      if (warp == kWarpMmaS) {
+        // S^T = K Q_i^T and dP^T = V dO_i^T for local step `it` into buffer it & 1.
+        for (int it = 0; ok && it < n; ++it) {
+          const int slot = it % kStages;
+          const int b = it & 1;
+          if (!(ok = mbar_wait(&bar_full[slot], (it / kStages) & 1, wc, kSiteBMmaQ))) break;
+          if (it >= 2 && !(ok = mbar_wait(&bar_dqe[b], ((it - 2) >> 1) & 1, wc, kSiteBMmaDq))) break;
+          tc_fence_after();
+          const uint32_t st = slot * C::kStageBytes;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
-          const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
-          mma_bf16_ss(tmem + C::col_s(b), sdesc_add(k_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageQ + offb),
-                      idesc_sdp, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
+            const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
+            mma_bf16_ss(tmem + C::col_s(b), sdesc_add(k_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageQ + offb),
+                        idesc_sdp, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
+            const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
+            mma_bf16_ss(tmem + C::col_dp(b), sdesc_add(v_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageDO + offb),
+                        idesc_sdp, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bar_sdp[b]);
         }
+      } else {
+        for (int it = 0; ok && it < n; ++it) {
+          const int b = it & 1;
+          const int slot = it % kStages;
+          if (!(ok = mbar_wait(&bar_comp[b], (it >> 1) & 1, wc, kSiteBMmaC))) break;
+          tc_fence_after();
+          const uint32_t st = slot * C::kStageBytes;
+          // dV += P^T dO_i ; dK += dS^T Q_i   (A from TMEM, B MN-major: 16 query rows per MMA)
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
-          const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
-          mma_bf16_ss(tmem + C::col_dp(b), sdesc_add(v_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageDO + offb),
-                      idesc_sdp, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kBqB / 16; ++kk)
+            mma_bf16_ts(tmem + C::kColDV, tmem + C::col_s(b) + kk * 8,
+                        sdesc_add(ring_mn, st + C::kStageDO + kk * 2048), idesc_dkv, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < kBqB / 16; ++kk)
+            mma_bf16_ts(tmem + C::kColDK, tmem + C::col_dp(b) + kk * 8,
+                        sdesc_add(ring_mn, st + C::kStageQ + kk * 2048), idesc_dkv, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bar_empty[slot]);
+          // dQ_i^T = K^T dS^T : A = K MN-major (d contiguous), B = dS^T rows of 64 queries; 16 keys per MMA.
+#pragma unroll
+          for (int kk = 0; kk < kBkB / 16; ++kk)
+            mma_bf16_ss(tmem + C::col_s(b), sdesc_add(k_mn, kk * 2048),
+                        sdesc_add(ds_mn, b * C::kDsBytes + kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
+          mma_commit(&bar_dqf[b]);
         }
-        mma_commit(&bar_sdp[b]);
-        return true;
-      };
-
-      if (ok) ok = issue_sdp(0);
-      for (int it = 0; ok && it < n; ++it) {
-        const int b = it & 1;
-        const int slot = it % kStages;
-        if (it + 1 < n && !(ok = issue_sdp(it + 1))) break;
-        if (!(ok = mbar_wait(&bar_comp[b], (it >> 1) & 1, wc, kSiteBMmaC))) break;
-        tc_fence_after();
-        const uint32_t st = slot * C::kStageBytes;
-        // dV += P^T dO_i ; dK += dS^T Q_i   (A from TMEM, B MN-major: 16 query rows per MMA)
-#pragma unroll
-        for (int kk = 0; kk < kBqB / 16; ++kk)
-          mma_bf16_ts(tmem + C::kColDV, tmem + C::col_s(b) + kk * 8,
-                      sdesc_add(ring_mn, st + C::kStageDO + kk * 2048), idesc_dkv, (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < kBqB / 16; ++kk)
-          mma_bf16_ts(tmem + C::kColDK, tmem + C::col_dp(b) + kk * 8,
-                      sdesc_add(ring_mn, st + C::kStageQ + kk * 2048), idesc_dkv, (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar_empty[slot]);
-        // dQ_i^T = K^T dS^T : A = K MN-major (d contiguous), B = dS^T rows of 64 queries; 16 keys per MMA.
-#pragma unroll
-        for (int kk = 0; kk < kBkB / 16; ++kk)
-          mma_bf16_ss(tmem + C::col_s(b), sdesc_add(k_mn, kk * 2048), sdesc_add(ds_mn, b * C::kDsBytes + kk * 2048),
-                      idesc_dq, kk > 0 ? 1u : 0u);
-        mma_commit(&bar_dqf[b]);
+        if (ok) mma_commit(bar_dkv);
       }
-      if (ok) mma_commit(bar_dkv);
+      // Every issued MMA of both threads must finish before TMEM is released.
       mma_commit(bar_drain);
       mbar_wait_drain(bar_drain, 0, wait_ns);
     }
