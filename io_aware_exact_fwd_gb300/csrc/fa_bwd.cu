@@ -17,13 +17,17 @@
 //  2. bwd_main: one CTA per (128-key block, head), the K/V-outer loop order.
 //     K_j, V_j stay in shared memory; Q_i, dO_i (64 query rows), LSE_i and D_i
 //     stream through a TMA ring.  Per query block, tcgen05 MMAs compute
-//     S^T = K Q_i^T and dP^T = V dO_i^T into TMEM (keys on TMEM lanes, so one
-//     thread owns one key row), four warps form P^T and dS^T in registers and
-//     write them back to TMEM as bf16 (A operands of dV += P^T dO_i and
-//     dK += dS^T Q_i) and to shared memory (B operand of dQ_i^T = K^T dS^T).
-//     dQ_i^T lands over the consumed S^T buffer; four more warps (one d-row
-//     per thread) add it into the fp32 accumulator with coalesced reductions.
-//     TMEM: dV, dK (128 columns each) + S^T, dP^T double-buffered (64 each).
+//     S^T = K Q_i^T and dP^T = V dO_i^T into TMEM (keys on TMEM lanes, so a
+//     thread owns one key row; two warpgroups split the 64 query columns),
+//     eight warps form P^T and dS^T in registers and write them back to TMEM
+//     as bf16 (A operands of dV += P^T dO_i and dK += dS^T Q_i) and to shared
+//     memory (B operand of dQ_i^T = K^T dS^T).  dQ_i^T lands over the consumed
+//     P^T, dS^T; four more warps (one d-row per thread) add it into the fp32
+//     accumulator with coalesced reductions.
+//     TMEM: dV, dK (128 columns each), one S^T, dP^T pair (64 each, free again
+//     as soon as the compute warps hold it in registers, so S^T, dP^T of the
+//     next block overlap this block's math), and two 64-column buffers for
+//     P^T, dS^T and then dQ^T.
 //  3. bwd_dq_convert: dQ = bf16(scale * dQacc).
 #include <math.h>
 
@@ -36,19 +40,23 @@ namespace {
 constexpr int kD = 128;
 constexpr int kBkB = 128;       // keys per CTA
 constexpr int kBqB = 64;        // query rows per inner step
-constexpr int kThreads = 384;   // 0-3 compute, 4-7 dQ reduction, 8 TMA, 9-10 MMA issuers, 11 spare
-constexpr int kWarpLoad = 8;
-constexpr int kWarpMma = 9;      // issues dV, dK, dQ^T (and owns the TMEM allocation)
-constexpr int kWarpMmaS = 10;    // issues S^T, dP^T
+constexpr int kThreads = 512;   // 0-7 compute, 8-11 dQ reduction, 12 TMA, 13-14 MMA issuers, 15 spare
+constexpr int kWarpDq = 8;
+constexpr int kWarpCtl = 12;
+constexpr int kWarpLoad = 12;
+constexpr int kWarpMma = 13;     // issues dV, dK, dQ^T (and owns the TMEM allocation)
+constexpr int kWarpMmaS = 14;    // issues S^T, dP^T
 constexpr int kStages = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
-// Launch budget 168 x 384 registers: compute warpgroup 224 (two 64-wide score
-// rows live), dQ warpgroup keeps 168, control warpgroup (TMA, MMA) gives back to 112.
-constexpr uint32_t kLaunchRegs = 168;
-constexpr uint32_t kRegsCompute = 224;
-constexpr uint32_t kRegsControl = 112;
-static_assert(128 * (kRegsCompute + kLaunchRegs + kRegsControl) <= kLaunchRegs * kThreads, "register split");
+// Launch budget 128 x 512 registers: the two compute warpgroups (one 32-query
+// half of a score row each) take 160, the dQ warpgroup 120, the control
+// warpgroup (TMA, MMA) gives back to 72.
+constexpr uint32_t kLaunchRegs = 128;
+constexpr uint32_t kRegsCompute = 160;
+constexpr uint32_t kRegsDq = 120;
+constexpr uint32_t kRegsControl = 72;
+static_assert(128 * (2 * kRegsCompute + kRegsDq + kRegsControl) <= kLaunchRegs * kThreads, "register split");
 
 enum : uint32_t {
   kSiteBLoad = 0x111,
@@ -56,6 +64,7 @@ enum : uint32_t {
   kSiteBMmaQ = 0x212,
   kSiteBMmaC = 0x213,
   kSiteBMmaDq = 0x214,
+  kSiteBMmaSd = 0x215,
   kSiteBComp = 0x311,
   kSiteBDq = 0x312,
   kSiteBEpi = 0x313,
@@ -78,14 +87,15 @@ struct BwdCfg {
   static constexpr int kRingOff = 2 * kKVTile;
   static constexpr int kDsOff = kRingOff + kStages * kStageBytes;
   static constexpr int kBarOff = kDsOff + 2 * kDsBytes;
-  // kv, full[S], empty[S], sdp[2], comp[2], dqf[2], dqe[2], dkv, epi, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2 + 1 + 1 + 1;
+  // kv, full[S], empty[S], sdp, sde, comp[2], dqf[2], dqe[2], dkv, epi, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 1 + 1 + 2 + 2 + 2 + 1 + 1 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
-  // TMEM columns
-  static constexpr uint32_t kColDV = 0, kColDK = 128;
-  static __device__ __forceinline__ uint32_t col_s(int b) { return 256u + 64u * b; }
-  static __device__ __forceinline__ uint32_t col_dp(int b) { return 384u + 64u * b; }
+  // TMEM columns: dV, dK accumulators; one S^T, dP^T pair (fp32, read once by
+  // the compute warps, then free for the next query block); two 64-column
+  // buffers that hold P^T | dS^T (bf16, 32 columns each) and then dQ^T (fp32).
+  static constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 320;
+  static __device__ __forceinline__ uint32_t col_pdq(int b) { return 384u + 64u * b; }
 };
 static_assert(BwdCfg::kStageTx <= BwdCfg::kStageBytes, "stage layout");
 static_assert(BwdCfg::kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -136,8 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_kv = bars;
   uint64_t* bar_full = bars + 1;
   uint64_t* bar_empty = bar_full + kStages;
-  uint64_t* bar_sdp = bar_empty + kStages;  // [2]
-  uint64_t* bar_comp = bar_sdp + 2;         // [2]
+  uint64_t* bar_sdp = bar_empty + kStages;  // S^T, dP^T ready in TMEM
+  uint64_t* bar_sde = bar_sdp + 1;          // S^T, dP^T read out of TMEM
+  uint64_t* bar_comp = bar_sde + 1;         // [2] P^T, dS^T written
   uint64_t* bar_dqf = bar_comp + 2;         // [2] dQ^T ready in TMEM
   uint64_t* bar_dqe = bar_dqf + 2;          // [2] dQ^T read out of TMEM
   uint64_t* bar_dkv = bar_dqe + 2;
@@ -167,14 +178,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
+    mbar_init(bar_sdp, 1);
+    mbar_init(bar_sde, 8);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar_sdp[b], 1);
-      mbar_init(&bar_comp[b], 4);
+      mbar_init(&bar_comp[b], 8);
       mbar_init(&bar_dqf[b], 1);
       mbar_init(&bar_dqe[b], 4);
     }
     mbar_init(bar_dkv, 1);
-    mbar_init(bar_epi, 4);
+    mbar_init(bar_epi, 8);
     mbar_init(bar_drain, 2);  // one commit per MMA-issuing thread
     *abort_flag = 0;
     fence_mbar_init();
@@ -188,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* lse2_h = lse2 + static_cast<size_t>(bh) * Npad;
   const float* dvec_h = dvec + static_cast<size_t>(bh) * Npad;
 
-  if (warp >= 8) {
+  if (warp >= kWarpCtl) {
    regs_decrease<kRegsControl>();
    if (warp == kWarpLoad) {
     // ------------------------------------------------------------ TMA producer
@@ -224,10 +236,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ MMA issuers (one thread each)
     // Two threads issue MMAs so that S^T/dP^T of a later query block never waits
     // behind dV/dK/dQ^T of an earlier one (or vice versa).  Each hazard between
-    // them is covered by a barrier: S^T(it) and dP^T(it) overwrite buffers whose
-    // previous contents (P^T, dS^T, dQ^T of it-2) were consumed by MMAs that
-    // completed before dQ^T(it-2) was read out (bar_dqe), and dV/dK/dQ^T(it)
-    // start only after the compute warps saw S^T, dP^T(it) (bar_comp).
+    // them is covered by a barrier: S^T(it), dP^T(it) overwrite the pair that the
+    // compute warps have already loaded into registers (bar_sde), dV/dK/dQ^T(it)
+    // start only after P^T, dS^T(it) are written (bar_comp), and the compute
+    // warps write P^T, dS^T(it) only after dQ^T(it-2), which they overwrite, was
+    // read out (bar_dqe).  MMAs of one thread run in issue order, so dQ^T(it)
+    // lands over P^T, dS^T(it) only after dV, dK(it) consumed them.
     if (lane == 0) {
       constexpr uint32_t idesc_sdp = idesc_bf16_f32(kBkB, kBqB, 0, 0);   // keys x queries, K = d
       constexpr uint32_t idesc_dkv = idesc_bf16_f32(kBkB, kD, 0, 1);     // keys x d, K = queries
@@ -240,29 +254,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t ds_mn = sdesc_sw128(smem_u32(sDs), 16, 1024);
       bool ok = mbar_wait(bar_kv, 0, wc, kSiteBMmaKV);
       if (warp == kWarpMmaS) {
-        // S^T = K Q_i^T and dP^T = V dO_i^T for local step `it` into buffer it & 1.
+        // S^T = K Q_i^T and dP^T = V dO_i^T for local step `it`, as soon as the
+        // compute warps have read the previous pair out of TMEM.
         for (int it = 0; ok && it < n; ++it) {
           const int slot = it % kStages;
-          const int b = it & 1;
           if (!(ok = mbar_wait(&bar_full[slot], (it / kStages) & 1, wc, kSiteBMmaQ))) break;
-          if (it >= 2 && !(ok = mbar_wait(&bar_dqe[b], ((it - 2) >> 1) & 1, wc, kSiteBMmaDq))) break;
+          if (it >= 1 && !(ok = mbar_wait(bar_sde, (it - 1) & 1, wc, kSiteBMmaSd))) break;
           tc_fence_after();
           const uint32_t st = slot * C::kStageBytes;
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
             const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
-            mma_bf16_ss(tmem + C::col_s(b), sdesc_add(k_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageQ + offb),
+            mma_bf16_ss(tmem + C::kColS, sdesc_add(k_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageQ + offb),
                         idesc_sdp, kk > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
             const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
-            mma_bf16_ss(tmem + C::col_dp(b), sdesc_add(v_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageDO + offb),
+            mma_bf16_ss(tmem + C::kColDP, sdesc_add(v_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageDO + offb),
                         idesc_sdp, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&bar_sdp[b]);
+          mma_commit(bar_sdp);
         }
       } else {
         for (int it = 0; ok && it < n; ++it) {
@@ -274,17 +288,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dV += P^T dO_i ; dK += dS^T Q_i   (A from TMEM, B MN-major: 16 query rows per MMA)
 #pragma unroll
           for (int kk = 0; kk < kBqB / 16; ++kk)
-            mma_bf16_ts(tmem + C::kColDV, tmem + C::col_s(b) + kk * 8,
+            mma_bf16_ts(tmem + C::kColDV, tmem + C::col_pdq(b) + kk * 8,
                         sdesc_add(ring_mn, st + C::kStageDO + kk * 2048), idesc_dkv, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < kBqB / 16; ++kk)
-            mma_bf16_ts(tmem + C::kColDK, tmem + C::col_dp(b) + kk * 8,
+            mma_bf16_ts(tmem + C::kColDK, tmem + C::col_pdq(b) + 32 + kk * 8,
                         sdesc_add(ring_mn, st + C::kStageQ + kk * 2048), idesc_dkv, (it > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bar_empty[slot]);
           // dQ_i^T = K^T dS^T : A = K MN-major (d contiguous), B = dS^T rows of 64 queries; 16 keys per MMA.
 #pragma unroll
           for (int kk = 0; kk < kBkB / 16; ++kk)
-            mma_bf16_ss(tmem + C::col_s(b), sdesc_add(k_mn, kk * 2048),
+            mma_bf16_ss(tmem + C::col_pdq(b), sdesc_add(k_mn, kk * 2048),
                         sdesc_add(ds_mn, b * C::kDsBytes + kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
           mma_commit(&bar_dqf[b]);
         }
@@ -296,69 +310,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
    }
-  } else if (warp < 4) {
+  } else if (warp < kWarpDq) {
     regs_increase<kRegsCompute>();
     // ------------------------------------- P and dS (one key row per thread)
-    const int row = threadIdx.x;
+    // Warpgroup g = warp / 4 takes query columns 32g .. 32g+31 of every 64-query
+    // block, so two warps share each SM sub-partition's TMEM lanes and the
+    // latency of one block's softmax-gradient math is split between them.
+    const int g = warp >> 2;
+    const int row = threadIdx.x & 127;
     const int key = kb * kBkB + row;
     const bool key_valid = key < N;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const float2 sl2 = make_float2(scale_log2, scale_log2);
     bool ok = true;
     for (int it = 0; it < n; ++it) {
       const int b = it & 1;
       const int slot = it % kStages;
       const int i = i0 + it;
-      if (!(ok = warp_wait_b(&bar_sdp[b], (it >> 1) & 1, wc, kSiteBComp))) break;
+      if (!(ok = warp_wait_b(bar_sdp, it & 1, wc, kSiteBComp))) break;
       if (!(ok = warp_wait_b(&bar_full[slot], (it / kStages) & 1, wc, kSiteBComp))) break;
       tc_fence_after();
-      uint32_t s[2][32], dp[2][32];
-      tmem_ld32(trow + C::col_s(b), s[0]);
-      tmem_ld32(trow + C::col_s(b) + 32, s[1]);
-      tmem_ld32(trow + C::col_dp(b), dp[0]);
-      tmem_ld32(trow + C::col_dp(b) + 32, dp[1]);
-      tmem_ld_wait32(s[0]);
-      tmem_ld_wait32(s[1]);
-      tmem_ld_wait32(dp[0]);
-      tmem_ld_wait32(dp[1]);
+      uint32_t s[32], dp[32];
+      tmem_ld32(trow + C::kColS + 32 * g, s);
+      tmem_ld32(trow + C::kColDP + 32 * g, dp);
+      tmem_ld_wait32(s);
+      tmem_ld_wait32(dp);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_sde);  // the MMA warp may now overwrite S^T, dP^T
       const uint8_t* st = sRing + slot * C::kStageBytes;
-      const float4* l4 = reinterpret_cast<const float4*>(st + C::kStageL);
-      const float4* d4 = reinterpret_cast<const float4*>(st + C::kStageD);
+      const float4* l4 = reinterpret_cast<const float4*>(st + C::kStageL) + 8 * g;
+      const float4* d4 = reinterpret_cast<const float4*>(st + C::kStageD) + 8 * g;
       const bool diag = CAUSAL && (i * kBqB < kb * kBkB + kBkB);  // some query in this block precedes a key
+      const int q0 = i * kBqB + 32 * g;
+      uint32_t ppk[16], dpk[16];
+#pragma unroll
+      for (int gg = 0; gg < 8; ++gg) {
+        const float4 lv = l4[gg];
+        const float4 dv = d4[gg];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = gg * 4 + 2 * e;
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2,
+                                      e == 0 ? make_float2(-lv.x, -lv.y) : make_float2(-lv.z, -lv.w));
+          float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          if (!key_valid || (diag && key > q0 + c)) p.x = 0.f;
+          if (!key_valid || (diag && key > q0 + c + 1)) p.y = 0.f;
+          const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
+                                       e == 0 ? make_float2(-dv.x, -dv.y) : make_float2(-dv.z, -dv.w));
+          const float2 ds = __fmul2_rn(p, dd);
+          ppk[2 * gg + e] = pack_bf16x2(p.x, p.y);
+          dpk[2 * gg + e] = pack_bf16x2(ds.x, ds.y);
+        }
+      }
+      // P^T, dS^T(it) overwrite dQ^T(it-2) (TMEM) and dS^T(it-2) (shared memory).
+      if (it >= 2 && !(ok = warp_wait_b(&bar_dqe[b], ((it - 2) >> 1) & 1, wc, kSiteBComp))) break;
+      tc_fence_after();
+      tmem_st16(trow + C::col_pdq(b) + 16 * g, ppk);
+      tmem_st16(trow + C::col_pdq(b) + 32 + 16 * g, dpk);
+      // dS row into shared memory, 128-byte swizzle: chunk ch holds queries 8ch..8ch+7.
       uint8_t* ds_row = sDs + b * C::kDsBytes + row * 128;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t ppk[16], dpk[16];
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float4 lv = l4[h * 8 + g];
-          const float4 dv = d4[h * 8 + g];
-          const float lz[4] = {lv.x, lv.y, lv.z, lv.w};
-          const float dz[4] = {dv.x, dv.y, dv.z, dv.w};
-          float p[4], ds[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = g * 4 + e;
-            const int q = i * kBqB + h * 32 + c;
-            float pe = ex2_approx(fmaf(__uint_as_float(s[h][c]), scale_log2, -lz[e]));
-            const bool masked = !key_valid || (diag && key > q);
-            pe = masked ? 0.f : pe;
-            p[e] = pe;
-            ds[e] = pe * (__uint_as_float(dp[h][c]) - dz[e]);
-          }
-          ppk[2 * g] = pack_bf16x2(p[0], p[1]);
-          ppk[2 * g + 1] = pack_bf16x2(p[2], p[3]);
-          dpk[2 * g] = pack_bf16x2(ds[0], ds[1]);
-          dpk[2 * g + 1] = pack_bf16x2(ds[2], ds[3]);
-        }
-        tmem_st16(trow + C::col_s(b) + h * 16, ppk);
-        tmem_st16(trow + C::col_dp(b) + h * 16, dpk);
-        // dS row into shared memory, 128-byte swizzle: chunk ch holds queries 8ch..8ch+7.
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int ch = h * 4 + c4;
-          *reinterpret_cast<uint4*>(ds_row + ((ch ^ (row & 7)) * 16)) =
-              make_uint4(dpk[4 * c4], dpk[4 * c4 + 1], dpk[4 * c4 + 2], dpk[4 * c4 + 3]);
-        }
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int ch = g * 4 + c4;
+        *reinterpret_cast<uint4*>(ds_row + ((ch ^ (row & 7)) * 16)) =
+            make_uint4(dpk[4 * c4], dpk[4 * c4 + 1], dpk[4 * c4 + 2], dpk[4 * c4 + 3]);
       }
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -366,35 +382,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_comp[b]);
     }
-    // ---------------------------------------------------------- dK, dV epilogue
+    // ------------------------------- dK, dV epilogue (warpgroup 0: dV, 1: dK)
     if (ok) ok = warp_wait_b(bar_dkv, 0, wc, kSiteBEpi);
     if (ok) {
       tc_fence_after();
-      stage_row_bf16(trow + C::kColDV, sV, row, 1.f);
-      stage_row_bf16(trow + C::kColDK, sK, row, scale);
+      if (g == 0) stage_row_bf16(trow + C::kColDV, sV, row, 1.f);
+      else stage_row_bf16(trow + C::kColDK, sK, row, scale);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_epi);
       if (threadIdx.x == 0 && mbar_wait(bar_epi, 0, wc, kSiteBEpi)) {
-        for (int b = 0; b < 2; ++b) {
-          tma_store_3d(&tm_dv, sV + b * C::kKVBox, b * 64, kb * kBkB, bh);
-          tma_store_3d(&tm_dk, sK + b * C::kKVBox, b * 64, kb * kBkB, bh);
+        for (int bb = 0; bb < 2; ++bb) {
+          tma_store_3d(&tm_dv, sV + bb * C::kKVBox, bb * 64, kb * kBkB, bh);
+          tma_store_3d(&tm_dk, sK + bb * C::kKVBox, bb * 64, kb * kBkB, bh);
         }
         tma_store_commit_and_wait_read();
       }
     }
     __syncwarp();
-  } else if (warp < 8) {
+  } else {
+    regs_decrease<kRegsDq>();
     // -------------------------------- dQ reduction (one d-row of dQ^T per thread)
-    const int dcol = threadIdx.x - 128;
+    const int dcol = threadIdx.x - kWarpDq * 32;
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     for (int it = 0; it < n; ++it) {
       const int b = it & 1;
       if (!warp_wait_b(&bar_dqf[b], (it >> 1) & 1, wc, kSiteBDq)) break;
       tc_fence_after();
       uint32_t v[2][32];
-      tmem_ld32(trow + C::col_s(b), v[0]);
-      tmem_ld32(trow + C::col_s(b) + 32, v[1]);
+      tmem_ld32(trow + C::col_pdq(b), v[0]);
+      tmem_ld32(trow + C::col_pdq(b) + 32, v[1]);
       tmem_ld_wait32(v[0]);
       tmem_ld_wait32(v[1]);
       tc_fence_before();
