@@ -10,13 +10,19 @@
 // softmax).  The single division by l happens once, after the inner loop.
 //
 // GB300 mapping of the pages' ideas:
-//  * TMA copies ("Asynchrone Datenübertragung (TMA)") move the Q tiles once and
-//    K_j, V_j through a ring of shared-memory slots guarded by full/empty
-//    mbarriers.
-//  * Warp specialisation ("Warp-Spezialisierung"): warp 8 issues TMA, one thread
-//    of warp 9 issues tcgen05 MMAs, and two softmax warpgroups (warps 0-3 and
-//    4-7, one thread per query row = one TMEM lane) each own one of the CTA's
-//    two 128-row query tiles.  While one warpgroup exponentiates its scores the
+//  * Persistent CTAs: one per SM, each walking a fixed list of work units
+//    (256 query rows of one head); causal units are ordered heaviest first and
+//    dealt out in zigzag passes so that every SM gets a similar total.  The K/V
+//    stream, the TMEM buffers and the barrier phases simply continue from one
+//    unit to the next, so a unit's Q load, first Q K^T and epilogue overlap the
+//    neighbouring unit's main loop instead of costing a CTA launch each.
+//  * TMA copies ("Asynchrone Datenübertragung (TMA)") move the Q tiles once per
+//    unit and K_j, V_j through a ring of shared-memory slots guarded by
+//    full/empty mbarriers.
+//  * Warp specialisation ("Warp-Spezialisierung"): warp 8 issues the K/V copies,
+//    warp 10 the Q copies, one thread of warp 9 issues tcgen05 MMAs, and two
+//    softmax warpgroups (warps 0-3 and 4-7, one thread per query row = one TMEM
+//    lane) each own one of the unit's two 128-row query tiles.  While one warpgroup exponentiates its scores the
 //    tensor core runs the other tile's P V and Q K^T ("Nahtloses Interleaving von
 //    Operationen" on the FlashAttention-3 page: matmul and softmax overlap).
 //  * Per tile, S = Q K_j^T accumulates in TMEM; P is written back over S as packed
@@ -40,9 +46,10 @@ namespace {
 
 constexpr int kTiles = 2;                       // query tiles per CTA
 constexpr int kRowsPerCta = kTiles * kBlockQ;   // 256 query rows
-constexpr int kThreads = 384;                   // warps 0-7 softmax (2 groups), 8 TMA, 9 MMA, 10-11 spare
+constexpr int kThreads = 384;                   // warps 0-7 softmax (2 groups), 8 K/V TMA, 9 MMA, 10 Q TMA, 11 spare
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpLoadQ = 10;
 // Launch budget: 168 registers x 384 threads.  Softmax warpgroups take 216 each
 // (128 live scores per thread), the TMA/MMA warpgroup gives back down to 72:
 // 2 x 128 x 216 + 128 x 72 = 168 x 384.
@@ -63,6 +70,7 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // Sites recorded in the error word when a wait expires.
 enum : uint32_t {
   kSiteLoadEmpty = 0x101,
+  kSiteLoadQ = 0x102,
   kSiteMmaQ = 0x201,
   kSiteMmaK = 0x202,
   kSiteMmaP = 0x203,
@@ -82,16 +90,18 @@ struct FwdCfg {
   static constexpr int kBoxBytes = kBlockK * 128;           // 16 KB: 128 rows x 128 bytes
   static constexpr int kTileBytes = kBlockK * kRowBytes;    // one Q, K or V tile
   static constexpr int kKSteps = kRowBytes / 32;            // MMA K-steps of 32 bytes over d
-  static constexpr int kQBytes = kBlockQ * D * 2;           // per query tile: Q, later the bf16 O staging
+  static constexpr int kOBytes = kBlockQ * D * 2;           // bf16 O staging of one query tile
   static constexpr int kOBoxes = D * 2 / 128;               // 128-byte boxes per bf16 O row
   static constexpr int kSlots = kTileBytes == 32768 ? 4 : 8;
-  static constexpr int kQOff = 0;                           // Q_a, Q_b
-  static constexpr int kRingOff = kTiles * kQBytes;
+  static constexpr int kQOff = 0;                           // Q_a, Q_b (one tile each)
+  static constexpr int kOOff = kTiles * kTileBytes;         // O staging, shared by both tiles in turn
+  static constexpr int kRingOff = kOOff + kOBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
-  // q_full[2], full[kSlots], empty[kSlots], s_full[2], p_full[2], o_done[2], epi[2], drain
-  static constexpr int kNumBars = 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1;
+  // q_full[2], q_empty[2], full[kSlots], empty[kSlots], s_full[2], p_full[2], o_done[2], epi[2], stg, drain
+  static constexpr int kNumBars = 2 + 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * static_cast<uint32_t>(t); }
   static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + D * static_cast<uint32_t>(t); }
 };
@@ -119,6 +129,24 @@ struct Fp8Scales {
   int ntiles;
 };
 
+// Work unit w -> (256-row query block u, head bh).  Causal units are numbered
+// heaviest first (largest u first), so the zigzag assignment below hands every
+// CTA a similar total.
+template <bool CAUSAL>
+__device__ __forceinline__ void decode_unit(int w, int nunits, int BH, int& u, int& bh) {
+  if (CAUSAL) {
+    u = nunits - 1 - w / BH;
+    bh = w % BH;
+  } else {
+    u = w % nunits;
+    bh = w / nunits;
+  }
+}
+
+// k-th unit of CTA c out of G persistent CTAs: pass k covers units kG .. kG+G-1,
+// in increasing CTA order on even passes and decreasing on odd ones.
+__device__ __forceinline__ int unit_of(int k, int c, int G) { return k * G + ((k & 1) ? (G - 1 - c) : c); }
+
 template <int D, bool CAUSAL, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -129,38 +157,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::kQOff;
+  uint8_t* sO = smem + C::kOOff;
   uint8_t* sRing = smem + C::kRingOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* bar_q = bars;                    // [2]
-  uint64_t* bar_full = bars + 2;             // [kSlots]
+  uint64_t* bar_q = bars;                    // [2] per tile: Q landed
+  uint64_t* bar_qe = bar_q + 2;              // [2] per tile: last Q K^T of a unit done (Q slot free)
+  uint64_t* bar_full = bar_qe + 2;           // [kSlots]
   uint64_t* bar_empty = bar_full + C::kSlots;
   uint64_t* bar_s = bar_empty + C::kSlots;   // [2] per tile: S ready
   uint64_t* bar_p = bar_s + 2;               // [2] per tile: P written
-  uint64_t* bar_o = bar_p + 2;               // [2] per tile: last P V done
+  uint64_t* bar_o = bar_p + 2;               // [2] per tile: last P V of a unit done
   uint64_t* bar_epi = bar_o + 2;             // [2] per tile: O staged in shared memory
-  uint64_t* bar_drain = bar_epi + 2;
+  uint64_t* bar_stg = bar_epi + 2;           // O staging buffer read out by the previous store
+  uint64_t* bar_drain = bar_stg + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // Work unit: (256-row query block, head).  Causal blocks are issued heaviest first.
-  int u, bh;
-  if (CAUSAL) {
-    u = nunits - 1 - static_cast<int>(blockIdx.x) / BH;
-    bh = static_cast<int>(blockIdx.x) % BH;
-  } else {
-    u = static_cast<int>(blockIdx.x) % nunits;
-    bh = static_cast<int>(blockIdx.x) / nunits;
-  }
-  const int n_a = kv_blocks<CAUSAL>(u, 0, N);
-  const int n_b = kv_blocks<CAUSAL>(u, 1, N);
-  const int n_max = max(n_a, n_b);
+  // Persistent CTAs: CTA c takes units unit_of(0, c, G), unit_of(1, c, G), ...
+  const int total = nunits * BH;
+  const int G = static_cast<int>(gridDim.x);
+  const int cta = static_cast<int>(blockIdx.x);
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&bar_q[t], 1);
+      mbar_init(&bar_qe[t], 1);
       mbar_init(&bar_s[t], 1);
       mbar_init(&bar_p[t], 4);
       mbar_init(&bar_o[t], 1);
@@ -170,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
+    mbar_init(bar_stg, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -191,21 +215,12 @@ __global__ void __launch_bounds__(kThreads, 1)
    // Control warpgroup: gives registers back to the softmax warpgroups.
    regs_decrease<kRegsControl>();
    if (warp == kWarpLoad) {
-    // ------------------------------------------------------------ TMA producer
+    // --------------------------------------------------------- K/V TMA producer
     if (lane == 0) {
-      const int nq[kTiles] = {n_a, n_b};
-      for (int t = 0; t < kTiles; ++t) {
-        if (nq[t] == 0) continue;
-        mbar_arrive_expect_tx(&bar_q[t], C::kTileBytes);
-#pragma unroll
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(sQ + t * C::kQBytes + b * C::kBoxBytes, &tm_q, &bar_q[t], b * kBoxCols,
-                      u * kRowsPerCta + t * kBlockQ, bh);
-      }
-      // Ring order = MMA first-use order: K0, V0, K1, V1, ...
+      // Ring order = MMA first-use order: K0, V0, K1, V1, ... of unit after unit.
       int issued = 0;
       bool ok = true;
-      auto push = [&](const CUtensorMap* tm, int j) -> bool {
+      auto push = [&](const CUtensorMap* tm, int j, int bh) -> bool {
         const int slot = issued % C::kSlots;
         const uint32_t ph = (issued / C::kSlots) & 1;
         if (!mbar_wait(&bar_empty[slot], ph ^ 1, wc, kSiteLoadEmpty)) return false;
@@ -223,16 +238,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++issued;
         return true;
       };
-      for (int j = 0; ok && j < n_max; ++j) {
-        ok = push(&tm_k, j);
-        if (ok) ok = push(&tm_v, j);
+      for (int k = 0; ok; ++k) {
+        const int w = unit_of(k, cta, G);
+        if (w >= total) break;
+        int u, bh;
+        decode_unit<CAUSAL>(w, nunits, BH, u, bh);
+        const int n_max = max(kv_blocks<CAUSAL>(u, 0, N), kv_blocks<CAUSAL>(u, 1, N));
+        for (int j = 0; ok && j < n_max; ++j) {
+          ok = push(&tm_k, j, bh);
+          if (ok) ok = push(&tm_v, j, bh);
+        }
       }
-      if (!ok) {
-        // Drain: the Q tiles and the last (up to kSlots) issued copies may still be landing.
-        for (int t = 0; t < kTiles; ++t)
-          if (nq[t] > 0) mbar_wait_drain(&bar_q[t], 0, wait_ns);
+      if (!ok) {  // drain: the last (up to kSlots) issued copies may still be landing
         for (int t = max(0, issued - C::kSlots); t < issued; ++t)
           mbar_wait_drain(&bar_full[t % C::kSlots], (t / C::kSlots) & 1, wait_ns);
+      }
+    }
+    __syncwarp();
+   } else if (warp == kWarpLoadQ) {
+    // ----------------------------------------------------------- Q TMA producer
+    // Q_t of the next unit loads as soon as the current unit's last Q_t K^T MMA
+    // has completed, so it overlaps that unit's last P V and epilogue.
+    if (lane == 0) {
+      int nload[kTiles] = {0, 0};
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int w = unit_of(k, cta, G);
+        if (w >= total) break;
+        int u, bh;
+        decode_unit<CAUSAL>(w, nunits, BH, u, bh);
+        for (int t = 0; ok && t < kTiles; ++t) {
+          if (kv_blocks<CAUSAL>(u, t, N) == 0) continue;
+          if (nload[t] > 0 && !(ok = mbar_wait(&bar_qe[t], (nload[t] - 1) & 1, wc, kSiteLoadQ))) break;
+          mbar_arrive_expect_tx(&bar_q[t], C::kTileBytes);
+#pragma unroll
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(sQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, &bar_q[t], b * kBoxCols,
+                        u * kRowsPerCta + t * kBlockQ, bh);
+          ++nload[t];
+        }
+      }
+      if (!ok) {  // drain the Q copies that may still be landing
+        for (int t = 0; t < kTiles; ++t)
+          if (nload[t] > 0) mbar_wait_drain(&bar_q[t], (nload[t] - 1) & 1, wait_ns);
       }
     }
     __syncwarp();
@@ -244,8 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = FP8 ? idesc_e4m3_f32(kBlockQ, D, 0, 0) : idesc_bf16_f32(kBlockQ, D, 0, 1);
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t ring_addr = smem_u32(sRing);
-      const int nq[kTiles] = {n_a, n_b};
-      int item = 0;  // ring index of the next K or V block to consume
+      int item = 0;               // ring index of the next K or V block to consume
+      int nq_seen[kTiles] = {0, 0};  // Q tiles consumed so far (bar_q phase)
+      int np[kTiles] = {0, 0};       // P blocks consumed so far (bar_p phase)
       bool ok = true;
 
       // Base descriptors; every MMA operand below is one of these advanced by a
@@ -257,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // S_t = Q_t K^T : both operands K-major (d contiguous), 16 d-columns per MMA.
       auto qk = [&](int t, int slot) {
-        const uint64_t qd = sdesc_add(qdesc, t * C::kQBytes);
+        const uint64_t qd = sdesc_add(qdesc, t * C::kTileBytes);
         const uint64_t kd = sdesc_add(kdesc, slot * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < C::kKSteps; ++kk) {
@@ -288,55 +337,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
 
-      // Prologue: S_a = Q_a K_0^T, S_b = Q_b K_0^T.
-      {
-        const int slot = item % C::kSlots;
-        ok = mbar_wait(&bar_full[slot], (item / C::kSlots) & 1, wc, kSiteMmaK);
-        for (int t = 0; ok && t < kTiles; ++t) {
-          if (nq[t] == 0) continue;
-          ok = mbar_wait(&bar_q[t], 0, wc, kSiteMmaQ);
+      for (int k = 0; ok; ++k) {
+        const int w = unit_of(k, cta, G);
+        if (w >= total) break;
+        int u, bh;
+        decode_unit<CAUSAL>(w, nunits, BH, u, bh);
+        const int nq[kTiles] = {kv_blocks<CAUSAL>(u, 0, N), kv_blocks<CAUSAL>(u, 1, N)};
+        const int n_max = max(nq[0], nq[1]);
+        // Prologue: S_a = Q_a K_0^T, S_b = Q_b K_0^T.  S_t is free: the previous
+        // unit's last P_t V MMA, which read P_t from it, was issued earlier.
+        {
+          const int slot = item % C::kSlots;
+          ok = mbar_wait(&bar_full[slot], (item / C::kSlots) & 1, wc, kSiteMmaK);
+          for (int t = 0; ok && t < kTiles; ++t) {
+            if (nq[t] == 0) continue;
+            ok = mbar_wait(&bar_q[t], nq_seen[t] & 1, wc, kSiteMmaQ);
+            if (!ok) break;
+            ++nq_seen[t];
+            tc_fence_after();
+            qk(t, slot);
+            if (nq[t] == 1) mma_commit(&bar_qe[t]);
+          }
           if (!ok) break;
-          tc_fence_after();
-          qk(t, slot);
+          mma_commit(&bar_empty[slot]);
+          ++item;
         }
-        if (ok) mma_commit(&bar_empty[slot]);
-        ++item;
-      }
-      for (int j = 0; ok && j < n_max; ++j) {
-        const int slot_v = item % C::kSlots;
-        ok = mbar_wait(&bar_full[slot_v], (item / C::kSlots) & 1, wc, kSiteMmaV);
-        ++item;
-        if (!ok) break;
-        const bool has_next = j + 1 < n_max;
-        const int slot_k = item % C::kSlots;
-        const uint32_t par_k = (item / C::kSlots) & 1;
-        if (has_next) ++item;
-        bool k_ready = false;
-        for (int t = 0; ok && t < kTiles; ++t) {
-          if (j >= nq[t]) continue;
-          ok = mbar_wait(&bar_p[t], j & 1, wc, kSiteMmaP);
+        for (int j = 0; ok && j < n_max; ++j) {
+          const int slot_v = item % C::kSlots;
+          ok = mbar_wait(&bar_full[slot_v], (item / C::kSlots) & 1, wc, kSiteMmaV);
+          ++item;
           if (!ok) break;
-          tc_fence_after();
-          pv(t, slot_v, j > 0);
-          if (j + 1 == nq[t]) mma_commit(&bar_o[t]);
-          if (j + 1 < nq[t]) {
-            if (!k_ready) {
+          const bool has_next = j + 1 < n_max;
+          const int slot_k = item % C::kSlots;
+          const uint32_t par_k = (item / C::kSlots) & 1;
+          if (has_next) ++item;
+          bool k_ready = false;
+          for (int t = 0; ok && t < kTiles; ++t) {
+            if (j >= nq[t]) continue;
+            ok = mbar_wait(&bar_p[t], np[t] & 1, wc, kSiteMmaP);
+            if (!ok) break;
+            ++np[t];
+            tc_fence_after();
+            // The first P V of a unit overwrites O_t: the softmax warpgroup read the
+            // previous unit's O_t out of TMEM before it wrote this P_t.
+            pv(t, slot_v, j > 0);
+            if (j + 1 == nq[t]) mma_commit(&bar_o[t]);
+            if (j + 1 < nq[t]) {
+              if (!k_ready) {
+                ok = mbar_wait(&bar_full[slot_k], par_k, wc, kSiteMmaK);
+                if (!ok) break;
+                tc_fence_after();
+                k_ready = true;
+              }
+              qk(t, slot_k);
+              if (j + 2 == nq[t]) mma_commit(&bar_qe[t]);
+            }
+          }
+          if (!ok) break;
+          mma_commit(&bar_empty[slot_v]);
+          if (has_next) {
+            if (!k_ready) {  // no tile needed K_{j+1} (cannot happen for n_max > j + 1, kept for safety)
               ok = mbar_wait(&bar_full[slot_k], par_k, wc, kSiteMmaK);
               if (!ok) break;
-              tc_fence_after();
-              k_ready = true;
             }
-            qk(t, slot_k);
+            mma_commit(&bar_empty[slot_k]);
           }
-        }
-        if (!ok) break;
-        mma_commit(&bar_empty[slot_v]);
-        if (has_next) {
-          if (!k_ready) {  // no tile needed K_{j+1} (cannot happen for n_max > j + 1, kept for safety)
-            ok = mbar_wait(&bar_full[slot_k], par_k, wc, kSiteMmaK);
-            if (!ok) break;
-          }
-          mma_commit(&bar_empty[slot_k]);
         }
       }
       // Every issued MMA must finish before TMEM is released.
@@ -350,228 +415,242 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------- softmax warpgroups (0-3, 4-7)
     const int t = warp >> 2;                 // query tile of this warpgroup
     const int row = threadIdx.x & 127;       // tile row == TMEM lane
-    const int qrow0 = u * kRowsPerCta + t * kBlockQ;
-    const int qrow = qrow0 + row;
-    const int nkt = t == 0 ? n_a : n_b;
-    const int diag = qrow0 / kBlockK;        // K/V block on this tile's diagonal
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t col_s = C::col_s(t);
     const uint32_t col_o = C::col_o(t);
-    float m_used = -INFINITY;  // running maximum in log2 units (possibly stale, see header)
-    float l = 0.f;
+    uint32_t scnt = 0;  // S blocks consumed so far (bar_s phase)
+    uint32_t ocnt = 0;  // units finished by this tile (bar_o, bar_epi phase)
+    uint32_t nepi = 0;  // epilogues of both tiles before this unit's (bar_stg phase)
     bool ok = true;
-    // FP8: the row's Q scale joins the score scale; V scales are folded into P
-    // relative to the head's largest V scale (so P stays <= 256 in e4m3) and
-    // undone in the epilogue.
-    float crow = scale_log2, inv_svmax = 1.f, svmax = 1.f;
-    const float* skh = nullptr;
-    const float* svh = nullptr;
-    if constexpr (FP8) {
-      const size_t hb = static_cast<size_t>(bh) * f8.ntiles;
-      skh = f8.sk + hb;
-      svh = f8.sv + hb;
-      float mxv = 0.f;
-      for (int i = lane; i < f8.ntiles; i += 32) mxv = fmaxf(mxv, svh[i]);
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) mxv = fmaxf(mxv, __shfl_xor_sync(0xffffffffu, mxv, m));
-      svmax = mxv;
-      inv_svmax = 1.f / mxv;
-      crow = scale_log2 * (qrow < N ? f8.sq[hb + qrow / 64] : 1.f);
-    }
-
-    for (int j = 0; j < nkt; ++j) {
-      if (!warp_wait(&bar_s[t], j & 1, wc, kSiteSoftS)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int kbase = j * kBlockK;
-      const bool need_mask = (kbase + kBlockK > N) || (CAUSAL && j == diag);
-      // Per 64-key half h: multiplier c[h] of the raw score (FP8: times that key
-      // tile's K scale) and lg[h] = log2 of the V-scale fold of P (0 for bf16).
-      float ch[2] = {crow, crow}, lg[2] = {0.f, 0.f}, fv[2] = {1.f, 1.f};
+    for (int k = 0; ok; ++k) {
+      const int w = unit_of(k, cta, G);
+      if (w >= total) break;
+      int u, bh;
+      decode_unit<CAUSAL>(w, nunits, BH, u, bh);
+      const int n_a = kv_blocks<CAUSAL>(u, 0, N);
+      const int n_b = kv_blocks<CAUSAL>(u, 1, N);
+      const int nkt = t == 0 ? n_a : n_b;
+      // Epilogues run in (unit, tile) order through one staging buffer.
+      const uint32_t epi_index = nepi + ((t == 1 && n_a > 0) ? 1u : 0u);
+      nepi += (n_a > 0 ? 1u : 0u) + (n_b > 0 ? 1u : 0u);
+      if (nkt == 0) continue;
+      const int qrow0 = u * kRowsPerCta + t * kBlockQ;
+      const int qrow = qrow0 + row;
+      const int diag = qrow0 / kBlockK;        // K/V block on this tile's diagonal
+      float m_used = -INFINITY;  // running maximum in log2 units (possibly stale, see header)
+      float l = 0.f;
+      // FP8: the row's Q scale joins the score scale; V scales are folded into P
+      // relative to the head's largest V scale (so P stays <= 256 in e4m3) and
+      // undone in the epilogue.
+      float crow = scale_log2, inv_svmax = 1.f, svmax = 1.f;
+      const float* skh = nullptr;
+      const float* svh = nullptr;
       if constexpr (FP8) {
+        const size_t hb = static_cast<size_t>(bh) * f8.ntiles;
+        skh = f8.sk + hb;
+        svh = f8.sv + hb;
+        float mxv = 0.f;
+        for (int i = lane; i < f8.ntiles; i += 32) mxv = fmaxf(mxv, svh[i]);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int kt = 2 * j + h;
-          if (kt < f8.ntiles) {
-            ch[h] = crow * skh[kt];
-            fv[h] = svh[kt] * inv_svmax;
-            lg[h] = __log2f(fv[h]);
-          }
-        }
+        for (int m = 16; m >= 1; m >>= 1) mxv = fmaxf(mxv, __shfl_xor_sync(0xffffffffu, mxv, m));
+        svmax = mxv;
+        inv_svmax = 1.f / mxv;
+        crow = scale_log2 * (qrow < N ? f8.sq[hb + qrow / 64] : 1.f);
       }
-      uint32_t r[4][32];
-      auto load_and_mask = [&](int c) {
-        if (need_mask) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int key = kbase + c * 32 + i;
-            if (key >= N || (CAUSAL && key > qrow)) r[c][i] = __float_as_uint(-INFINITY);
-          }
+
+      for (int j = 0; j < nkt; ++j, ++scnt) {
+        if (!warp_wait(&bar_s[t], scnt & 1, wc, kSiteSoftS)) {
+          ok = false;
+          break;
         }
-      };
-      // Row maximum of the scaled scores (scale > 0: max commutes with it), as a
-      // shallow max3 tree per 32-key chunk.
-      auto tile_max = [&]() -> float {
-        float mc[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float a[11];
-#pragma unroll
-          for (int i = 0; i < 10; ++i)
-            a[i] = max3(__uint_as_float(r[c][3 * i]), __uint_as_float(r[c][3 * i + 1]), __uint_as_float(r[c][3 * i + 2]));
-          a[10] = fmaxf(__uint_as_float(r[c][30]), __uint_as_float(r[c][31]));
-          const float b0 = max3(a[0], a[1], a[2]), b1 = max3(a[3], a[4], a[5]), b2 = max3(a[6], a[7], a[8]);
-          mc[c] = fmaxf(max3(b0, b1, b2), fmaxf(a[9], a[10]));
-        }
-        return fmaxf(fmaxf(mc[0], mc[1]) * ch[0], fmaxf(mc[2], mc[3]) * ch[1]);
-      };
-      // P = exp2(S * c - m) over chunk c, written back over the S buffer.  bf16:
-      // keys 32c..32c+31 become TMEM columns 16c..16c+15 (2 per column).  FP8:
-      // P * fv (the V-scale fold) as e4m3, 4 per column, keys 64h..64h+63 in
-      // columns 16h..16h+15.  Returns nothing; accumulates part[h].
-      float2 part[2];
-      uint32_t pk8[16];
-      auto exp_chunk = [&](int c) {
-        const int h = c >> 1;
-        const float2 c2 = make_float2(ch[h], ch[h]);
-        const float2 b2 = make_float2(lg[h] - m_used, lg[h] - m_used);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 x =
-              __ffma2_rn(make_float2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), c2, b2);
-          const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          part[h] = __fadd2_rn(part[h], p);
-          if constexpr (FP8)
-            pk[i] = e4m3x2_bits(p.x, p.y);
-          else
-            pk[i] = pack_bf16x2(p.x, p.y);
-        }
+        tc_fence_after();
+        const int kbase = j * kBlockK;
+        const bool need_mask = (kbase + kBlockK > N) || (CAUSAL && j == diag);
+        // Per 64-key half h: multiplier c[h] of the raw score (FP8: times that key
+        // tile's K scale) and lg[h] = log2 of the V-scale fold of P (0 for bf16).
+        float ch[2] = {crow, crow}, lg[2] = {0.f, 0.f}, fv[2] = {1.f, 1.f};
         if constexpr (FP8) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) pk8[(c & 1) * 8 + i] = pk[2 * i] | (pk[2 * i + 1] << 16);
-          if (c & 1) tmem_st16(trow + col_s + h * 16, pk8);
-        } else {
-          tmem_st16(trow + col_s + c * 16, pk);
+  #pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int kt = 2 * j + h;
+            if (kt < f8.ntiles) {
+              ch[h] = crow * skh[kt];
+              fv[h] = svh[kt] * inv_svmax;
+              lg[h] = __log2f(fv[h]);
+            }
+          }
         }
-      };
-      auto tile_sum = [&]() {
-        // l counts the unscaled P: undo the V-scale fold of each half.
-        return (part[0].x + part[0].y) / fv[0] + (part[1].x + part[1].y) / fv[1];
-      };
+        uint32_t r[4][32];
+        auto load_and_mask = [&](int c) {
+          if (need_mask) {
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int key = kbase + c * 32 + i;
+              if (key >= N || (CAUSAL && key > qrow)) r[c][i] = __float_as_uint(-INFINITY);
+            }
+          }
+        };
+        // Row maximum of the scaled scores (scale > 0: max commutes with it), as a
+        // shallow max3 tree per 32-key chunk.
+        auto tile_max = [&]() -> float {
+          float mc[4];
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float a[11];
+  #pragma unroll
+            for (int i = 0; i < 10; ++i)
+              a[i] = max3(__uint_as_float(r[c][3 * i]), __uint_as_float(r[c][3 * i + 1]), __uint_as_float(r[c][3 * i + 2]));
+            a[10] = fmaxf(__uint_as_float(r[c][30]), __uint_as_float(r[c][31]));
+            const float b0 = max3(a[0], a[1], a[2]), b1 = max3(a[3], a[4], a[5]), b2 = max3(a[6], a[7], a[8]);
+            mc[c] = fmaxf(max3(b0, b1, b2), fmaxf(a[9], a[10]));
+          }
+          return fmaxf(fmaxf(mc[0], mc[1]) * ch[0], fmaxf(mc[2], mc[3]) * ch[1]);
+        };
+        // P = exp2(S * c - m) over chunk c, written back over the S buffer.  bf16:
+        // keys 32c..32c+31 become TMEM columns 16c..16c+15 (2 per column).  FP8:
+        // P * fv (the V-scale fold) as e4m3, 4 per column, keys 64h..64h+63 in
+        // columns 16h..16h+15.  Returns nothing; accumulates part[h].
+        float2 part[2];
+        uint32_t pk8[16];
+        auto exp_chunk = [&](int c) {
+          const int h = c >> 1;
+          const float2 c2 = make_float2(ch[h], ch[h]);
+          const float2 b2 = make_float2(lg[h] - m_used, lg[h] - m_used);
+          uint32_t pk[16];
+  #pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 x =
+                __ffma2_rn(make_float2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), c2, b2);
+            const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            part[h] = __fadd2_rn(part[h], p);
+            if constexpr (FP8)
+              pk[i] = e4m3x2_bits(p.x, p.y);
+            else
+              pk[i] = pack_bf16x2(p.x, p.y);
+          }
+          if constexpr (FP8) {
+  #pragma unroll
+            for (int i = 0; i < 8; ++i) pk8[(c & 1) * 8 + i] = pk[2 * i] | (pk[2 * i + 1] << 16);
+            if (c & 1) tmem_st16(trow + col_s + h * 16, pk8);
+          } else {
+            tmem_st16(trow + col_s + c * 16, pk);
+          }
+        };
+        auto tile_sum = [&]() {
+          // l counts the unscaled P: undo the V-scale fold of each half.
+          return (part[0].x + part[0].y) / fv[0] + (part[1].x + part[1].y) / fv[1];
+        };
 
-      // O_t is rescaled (in TMEM) by alpha for rows whose reference maximum moves
-      // up; O_t already holds P V up to block j-1 because Q K_j^T was issued after it.
-      auto rescale_o = [&](float alpha, bool any) {
-        if (!any) return;
-        const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(trow + col_o + c * 32, o);
-          tmem_ld_wait32(o);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
-            o[i] = __float_as_uint(v.x);
-            o[i + 1] = __float_as_uint(v.y);
+        // O_t is rescaled (in TMEM) by alpha for rows whose reference maximum moves
+        // up; O_t already holds P V up to block j-1 because Q K_j^T was issued after it.
+        auto rescale_o = [&](float alpha, bool any) {
+          if (!any) return;
+          const float2 a2 = make_float2(alpha, alpha);
+  #pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(trow + col_o + c * 32, o);
+            tmem_ld_wait32(o);
+  #pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+              o[i] = __float_as_uint(v.x);
+              o[i + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(trow + col_o + c * 32, o);
           }
-          tmem_st32(trow + col_o + c * 32, o);
-        }
-      };
+        };
 
-      float l_tile;
-      if (j == 0 || FP8) {
-        // The block's own maximum first.  First block: it is the reference
-        // maximum.  FP8, later blocks: the reference moves up (and O is rescaled)
-        // only when the block's maximum exceeds it by more than 2^8, so every
-        // folded P stays <= 256, inside e4m3's range.  (Exponentiating before
-        // knowing the maximum, as bf16 does below, pays off only when blocks
-        // rarely overshoot; with outliers they often overshoot e4m3's 448.)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(trow + col_s + c * 32, r[c]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_wait32(r[c]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) load_and_mask(c);
-        const float mt = tile_max();
-        if (j == 0) {
-          m_used = (mt == -INFINITY) ? 0.f : mt;
-        } else {
-          const float m_new = fmaxf(m_used, mt);
-          const bool need = m_new > m_used + kRescaleThreshold;
-          float alpha = 1.f;
-          if (need) {
-            alpha = ex2_approx(m_used - m_new);
-            m_used = m_new;
+        float l_tile;
+        if (j == 0 || FP8) {
+          // The block's own maximum first.  First block: it is the reference
+          // maximum.  FP8, later blocks: the reference moves up (and O is rescaled)
+          // only when the block's maximum exceeds it by more than 2^8, so every
+          // folded P stays <= 256, inside e4m3's range.  (Exponentiating before
+          // knowing the maximum, as bf16 does below, pays off only when blocks
+          // rarely overshoot; with outliers they often overshoot e4m3's 448.)
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(trow + col_s + c * 32, r[c]);
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld_wait32(r[c]);
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) load_and_mask(c);
+          const float mt = tile_max();
+          if (j == 0) {
+            m_used = (mt == -INFINITY) ? 0.f : mt;
+          } else {
+            const float m_new = fmaxf(m_used, mt);
+            const bool need = m_new > m_used + kRescaleThreshold;
+            float alpha = 1.f;
+            if (need) {
+              alpha = ex2_approx(m_used - m_new);
+              m_used = m_new;
+            }
+            l *= alpha;
+            rescale_o(alpha, __any_sync(0xffffffffu, need));
           }
-          l *= alpha;
-          rescale_o(alpha, __any_sync(0xffffffffu, need));
-        }
-        part[0] = part[1] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) exp_chunk(c);
-        l_tile = tile_sum();
-      } else {
-        // bf16, later blocks: exponentiate against the running maximum without
-        // looking for a new one.  This is exact as long as no P overflows, which
-        // the block's row sum proves (sum <= 2^16 => every P <= 2^16); otherwise
-        // the block is redone below with its own maximum.  The second half of S
-        // loads while the first half is exponentiated.
-        tmem_ld32(trow + col_s, r[0]);
-        tmem_ld32(trow + col_s + 32, r[1]);
-        tmem_ld_wait32(r[0]);
-        tmem_ld_wait32(r[1]);
-        tmem_ld32(trow + col_s + 64, r[2]);
-        tmem_ld32(trow + col_s + 96, r[3]);
-        part[0] = part[1] = make_float2(0.f, 0.f);
-        load_and_mask(0);
-        load_and_mask(1);
-        exp_chunk(0);
-        exp_chunk(1);
-        tmem_ld_wait32(r[2]);
-        tmem_ld_wait32(r[3]);
-        load_and_mask(2);
-        load_and_mask(3);
-        exp_chunk(2);
-        exp_chunk(3);
-        l_tile = tile_sum();
-        const bool bad = !(l_tile <= kSpeculationSumBound);  // also true for inf / NaN
-        if (__any_sync(0xffffffffu, bad)) {
-          tmem_st_wait();  // the speculative P has landed before it is overwritten
-          const float m_new = fmaxf(m_used, tile_max());
-          const bool need = m_new > m_used;
-          float alpha = 1.f;
-          if (need) {
-            alpha = ex2_approx(m_used - m_new);
-            m_used = m_new;
-          }
-          l *= alpha;
-          rescale_o(alpha, __any_sync(0xffffffffu, need));
           part[0] = part[1] = make_float2(0.f, 0.f);
-#pragma unroll
+  #pragma unroll
           for (int c = 0; c < 4; ++c) exp_chunk(c);
           l_tile = tile_sum();
+        } else {
+          // bf16, later blocks: exponentiate against the running maximum without
+          // looking for a new one.  This is exact as long as no P overflows, which
+          // the block's row sum proves (sum <= 2^16 => every P <= 2^16); otherwise
+          // the block is redone below with its own maximum.  The second half of S
+          // loads while the first half is exponentiated.
+          tmem_ld32(trow + col_s, r[0]);
+          tmem_ld32(trow + col_s + 32, r[1]);
+          tmem_ld_wait32(r[0]);
+          tmem_ld_wait32(r[1]);
+          tmem_ld32(trow + col_s + 64, r[2]);
+          tmem_ld32(trow + col_s + 96, r[3]);
+          part[0] = part[1] = make_float2(0.f, 0.f);
+          load_and_mask(0);
+          load_and_mask(1);
+          exp_chunk(0);
+          exp_chunk(1);
+          tmem_ld_wait32(r[2]);
+          tmem_ld_wait32(r[3]);
+          load_and_mask(2);
+          load_and_mask(3);
+          exp_chunk(2);
+          exp_chunk(3);
+          l_tile = tile_sum();
+          const bool bad = !(l_tile <= kSpeculationSumBound);  // also true for inf / NaN
+          if (__any_sync(0xffffffffu, bad)) {
+            tmem_st_wait();  // the speculative P has landed before it is overwritten
+            const float m_new = fmaxf(m_used, tile_max());
+            const bool need = m_new > m_used;
+            float alpha = 1.f;
+            if (need) {
+              alpha = ex2_approx(m_used - m_new);
+              m_used = m_new;
+            }
+            l *= alpha;
+            rescale_o(alpha, __any_sync(0xffffffffu, need));
+            part[0] = part[1] = make_float2(0.f, 0.f);
+  #pragma unroll
+            for (int c = 0; c < 4; ++c) exp_chunk(c);
+            l_tile = tile_sum();
+          }
         }
+        l += l_tile;
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_p[t]);
       }
-      l += l_tile;
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_p[t]);
-    }
+      if (!ok) break;
 
-    // ------------------------------------------------------------ epilogue
-    if (ok && nkt > 0) ok = warp_wait(&bar_o[t], 0, wc, kSiteSoftO);
-    if (ok && nkt > 0) {
+      // ---------------------------------------------------------- epilogue
+      if (!(ok = warp_wait(&bar_o[t], ocnt & 1, wc, kSiteSoftO))) break;
       tc_fence_after();
+      // The staging buffer is free once the previous epilogue's store has read it.
+      if (epi_index > 0 && !(ok = warp_wait(bar_stg, (epi_index - 1) & 1, wc, kSiteEpi))) break;
       const float inv_l = svmax / l;  // svmax = 1 for bf16
       const float2 il2 = make_float2(inv_l, inv_l);
-      // O row -> bf16 -> this tile's Q staging area (free: its last Q K^T MMA has
-      // completed), laid out exactly as the 128-byte-swizzled TMA box expects.
-      uint8_t* sQt = sQ + t * C::kQBytes;
+      // O row -> bf16 -> the staging buffer, laid out as the 128-byte-swizzled TMA box expects.
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -583,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2);
           pk[i] = pack_bf16x2(v.x, v.y);
         }
-        uint8_t* box = sQt + (c / 2) * C::kBoxBytes + row * 128;
+        uint8_t* box = sO + (c / 2) * C::kBoxBytes + row * 128;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int chunk = (c % 2) * 4 + q4;
@@ -591,16 +670,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(box + ((chunk ^ (row & 7)) * 16)) = val;
         }
       }
+      // O_t has been read out of TMEM (tcgen05.wait::ld above); the next unit's
+      // first P V may overwrite it once this warpgroup signals its next P.
+      tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_epi[t]);
       if (qrow < N) lse[static_cast<size_t>(bh) * N + qrow] = (m_used + log2f(l)) * kLn2;
-      if (row == 0 && mbar_wait(&bar_epi[t], 0, wc, kSiteEpi)) {
+      if (row == 0) {
+        if ((ok = mbar_wait(&bar_epi[t], ocnt & 1, wc, kSiteEpi))) {
 #pragma unroll
-        for (int b = 0; b < C::kOBoxes; ++b)
-          tma_store_3d(&tm_o, sQt + b * C::kBoxBytes, b * kBoxCols, qrow0, bh);
-        tma_store_commit_and_wait_read();
+          for (int b = 0; b < C::kOBoxes; ++b)
+            tma_store_3d(&tm_o, sO + b * C::kBoxBytes, b * kBoxCols, qrow0, bh);
+          tma_store_commit_and_wait_read();
+          mbar_arrive(bar_stg);
+        }
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ++ocnt;
     }
     __syncwarp();
   }
@@ -628,7 +715,12 @@ cudaError_t launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   if ((e = cudaFuncGetAttributes(&fattr, kern))) return e;
   if (static_cast<uint32_t>(fattr.numRegs) * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
   const int nunits = (N + kRowsPerCta - 1) / kRowsPerCta;
-  dim3 grid(static_cast<unsigned>(nunits * BH));
+  // Persistent: one CTA per SM (shared memory and TMEM admit no second), each
+  // walking its share of the units.
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev))) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+  dim3 grid(static_cast<unsigned>(min(nunits * BH, sms)));
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, lse, N, BH, nunits, scale_log2, err_word,
                                                    dbg.wait_limit_ns, dbg.fault, f8);
   return cudaGetLastError();
