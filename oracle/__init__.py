@@ -13,6 +13,12 @@ check it against the pages by eye:
   deterministisch").  The tiled method reaches this same result, so the oracle is
   the definition itself, never an online or tiled softmax.
 * ``brute``      -- a scalar triple-loop twin of ``attention`` for tiny inputs.
+* ``splitkv``    -- attention partials over key ranges and their exact merge
+  (LSE = ln sum_s exp LSE_s, O = sum_s exp(LSE_s - LSE) O_s), with causal
+  queries aligned to the last keys when Nq < Nk.  Source of the setting:
+  "FlashAttention-Skalierung, Multi-GPU-Training und Gewichtsquantisierung",
+  section 3 (token-by-token inference is bandwidth-bound); the merge itself is
+  the softmax definition split over key ranges.
 * ``fp8``        -- the FP8 input preparation: random-sign Walsh-Hadamard rotation
   of Q and K (incoherent processing) and per-tile block quantisation to OCP e4m3.
   Source: "FlashAttention-Skalierung, Multi-GPU-Training und
@@ -35,6 +41,14 @@ from .attention import (
     attention_backward_rows,
 )
 from .brute import attention_forward_brute
+from .splitkv import (
+    split_key_ranges,
+    attention_partial,
+    attention_splitkv,
+    merge_partials,
+    attention_general,
+    splitkv_flops,
+)
 from .fp8 import (
     sylvester_hadamard,
     fwht_f32,
@@ -53,6 +67,12 @@ __all__ = [
     "attention_backward_sampled",
     "attention_backward_rows",
     "attention_forward_brute",
+    "split_key_ranges",
+    "attention_partial",
+    "attention_splitkv",
+    "merge_partials",
+    "attention_general",
+    "splitkv_flops",
     "sylvester_hadamard",
     "fwht_f32",
     "e4m3_encode",
