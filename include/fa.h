@@ -217,6 +217,72 @@ FA_API int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* ls
                       int causal, float scale, fa_stream_t stream);
 
 /*
+ * Split-KV forward ("decode"-shaped attention: few queries, many keys) and the
+ * exact merge of attention partials.  The setting is token-by-token inference,
+ * which the pages call bandwidth-bound rather than compute-bound
+ * ("FlashAttention-Skalierung, Multi-GPU-Training und Gewichtsquantisierung",
+ * section 3); one head's keys are then too few work units to fill the GPU, so
+ * the key range is cut into splits that run in parallel and are merged.
+ *
+ * Shapes: q [B, H, Nq, d]; k, v [B, H, Nk, d] (bf16, dense, d contiguous).
+ * Causal (Nq <= Nk required): the queries are the LAST Nq positions, so query i
+ * (0-based) sees key j iff j <= i + (Nk - Nq); with Nq == Nk this is fa_fwd's mask.
+ * Split rule: keys form nkb = ceil(Nk / 128) blocks of 128; with
+ * kbps = ceil(nkb / n_split), split s covers keys [128 s kbps, min(128 (s+1) kbps, Nk)).
+ * Trailing splits may be empty.  1 <= n_split <= 1024.
+ *
+ * Partial of split s, row i (natural log):
+ *   LSE_s[i] = ln sum_{j in s, visible} exp(scale q_i . k_j)   (-inf if no such j)
+ *   O_s[i]   = sum_{j in s, visible} exp(scale q_i . k_j - LSE_s[i]) v_j
+ * Merge: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s, which is the
+ * softmax over all keys (splits with LSE_s = -inf carry no weight and their O_s
+ * is not read; a row with every split empty gets O = 0, LSE = -inf).
+ */
+
+/* Bytes of workspace fa_fwd_splitkv needs (fp32 partials: n_split * B*H*Nq*(d + 1)
+ * floats, 256-byte aligned regions); 0 for invalid or unsupported sizes. */
+FA_API size_t fa_splitkv_workspace_size(int B, int H, int Nq, int d, int n_split);
+
+/* A split count for these sizes on the current device: the fewest splits (1..64,
+ * each of at least 4 key blocks) within 2 % of the best balance of work units over
+ * the SMs; 1 when Nq > 128 and the unsplit units already cover every SM.  Returns
+ * >= 1, or 0 for invalid sizes. */
+FA_API int fa_splitkv_default_splits(int B, int H, int Nq, int Nk, int d);
+
+/*
+ * fa_fwd_splitkv_partial -- the partials only (the building block of a merge
+ * done elsewhere, e.g. across devices holding different key ranges).
+ *   o_part   : float [n_split, B, H, Nq, d]  (output; rows of empty splits unwritten)
+ *   lse_part : float [n_split, B, H, Nq]     (output, every element written)
+ * Numerics: as fa_fwd (fp32 scores on the tensor cores, bf16 P for P V), but O_s
+ * stays fp32.  Errors: as fa_fwd; FA_ERR_INVALID_ARG also for n_split outside
+ * [1, 1024], Nk < 1, or causal with Nq > Nk.  B * H * Nq == 0 is a no-op.
+ */
+FA_API int fa_fwd_splitkv_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                                  int B, int H, int Nq, int Nk, int d, int n_split, int causal, float scale,
+                                  fa_stream_t stream);
+
+/*
+ * fa_merge_partials -- exact merge of n_split partials laid out as above.
+ *   o   : bf16 [B, H, Nq, d] (output)      lse : float [B, H, Nq] (output)
+ * Bandwidth-bound; fp32 arithmetic; O rounded to bf16 once.
+ */
+FA_API int fa_merge_partials(const float* o_part, const float* lse_part, void* o, float* lse, int n_split, int B,
+                             int H, int Nq, int d, fa_stream_t stream);
+
+/*
+ * fa_fwd_splitkv -- partials into `workspace`, then the merge: O and LSE of
+ * softmax(scale Q K^T [+mask]) V for Nq queries against Nk keys.
+ * n_split <= 0 selects fa_splitkv_default_splits(...).  The workspace (at least
+ * fa_splitkv_workspace_size(B, H, Nq, d, n_split) bytes for the split count used,
+ * 256-byte aligned, caller-owned) is scratch.  Errors: as the two calls above,
+ * plus FA_ERR_WORKSPACE for a missing or short workspace.
+ */
+FA_API int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                          size_t ws_bytes, int B, int H, int Nq, int Nk, int d, int n_split, int causal, float scale,
+                          fa_stream_t stream);
+
+/*
  * fa_sync_check -- synchronise `stream`, then report device-detected errors.
  * Returns FA_ERR_CUDA if the stream or a prior launch failed, FA_ERR_TIMEOUT
  * if any kernel of this library on the current device expired a bounded wait

@@ -85,6 +85,16 @@ def load_library():
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.fa_bwd_noalloc_max_workspace.restype = ctypes.c_size_t
     lib.fa_bwd_noalloc_max_workspace.argtypes = []
+    lib.fa_splitkv_workspace_size.restype = ctypes.c_size_t
+    lib.fa_splitkv_workspace_size.argtypes = [i, i, i, i, i]
+    lib.fa_splitkv_default_splits.restype = i
+    lib.fa_splitkv_default_splits.argtypes = [i, i, i, i, i]
+    lib.fa_fwd_splitkv_partial.restype = i
+    lib.fa_fwd_splitkv_partial.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.fa_merge_partials.restype = i
+    lib.fa_merge_partials.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.fa_fwd_splitkv.restype = i
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, i, i, f, vp]
     lib.fa_sync_check.restype = i
     lib.fa_sync_check.argtypes = [vp]
     lib.fa_last_error_site.restype = ctypes.c_uint
@@ -322,6 +332,99 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal: bool = False, scale:
 
 def fa_bwd_noalloc_max_workspace() -> int:
     return int(load_library().fa_bwd_noalloc_max_workspace())
+
+
+def fa_splitkv_workspace_size(B: int, H: int, Nq: int, d: int, n_split: int) -> int:
+    return int(load_library().fa_splitkv_workspace_size(B, H, Nq, d, n_split))
+
+
+def fa_splitkv_default_splits(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return int(load_library().fa_splitkv_default_splits(B, H, Nq, Nk, d))
+
+
+def _check_kv(q, k, v):
+    import torch
+
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    _check_bhnd("q", q, (B, H, Nq, d), torch.bfloat16)
+    _check_bhnd("k", k, (B, H, Nk, d), torch.bfloat16)
+    _check_bhnd("v", v, (B, H, Nk, d), torch.bfloat16)
+    return B, H, Nq, Nk, d
+
+
+def fa_fwd_splitkv_partial(q, k, v, n_split: int, o_part=None, lse_part=None, causal: bool = False,
+                           scale: float | None = None, stream=None):
+    """Split-KV partials: returns (o_part fp32 [n, B, H, Nq, d], lse_part fp32 [n, B, H, Nq]).
+
+    q: bf16 [B, H, Nq, d]; k, v: bf16 [B, H, Nk, d].  Causal queries are the last Nq
+    positions (query i sees key j iff j <= i + Nk - Nq).
+    """
+    import torch
+
+    lib = load_library()
+    B, H, Nq, Nk, d = _check_kv(q, k, v)
+    if o_part is None:
+        o_part = torch.empty((n_split, B, H, Nq, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((n_split, B, H, Nq), dtype=torch.float32, device=q.device)
+    _check_bhnd("o_part", o_part.view(n_split * B, H, Nq, d), (n_split * B, H, Nq, d), torch.float32)
+    _check_bhnd("lse_part", lse_part.view(n_split * B, H, Nq, 1), (n_split * B, H, Nq, 1), torch.float32)
+    sc = float(scale) if scale is not None else d ** -0.5
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_splitkv_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(o_part), _ptr(lse_part), B, H, Nq, Nk, d,
+                                        n_split, int(bool(causal)), sc, _stream_handle(stream))
+    _check(st, "fa_fwd_splitkv_partial")
+    return o_part, lse_part
+
+
+def fa_merge_partials(o_part, lse_part, o=None, lse=None, stream=None):
+    """Exact merge of split-KV partials: returns (o bf16 [B, H, Nq, d], lse fp32 [B, H, Nq])."""
+    import torch
+
+    lib = load_library()
+    n_split, B, H, Nq, d = o_part.shape
+    _check_bhnd("o_part", o_part.view(n_split * B, H, Nq, d), (n_split * B, H, Nq, d), torch.float32)
+    _check_bhnd("lse_part", lse_part.view(n_split * B, H, Nq, 1), (n_split * B, H, Nq, 1), torch.float32)
+    if o is None:
+        o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=o_part.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=o_part.device)
+    _check_bhnd("o", o, (B, H, Nq, d), torch.bfloat16)
+    _check_bhnd("lse", lse.view(B, H, Nq, 1), (B, H, Nq, 1), torch.float32)
+    with torch.cuda.device(o_part.device):
+        st = lib.fa_merge_partials(_ptr(o_part), _ptr(lse_part), _ptr(o), _ptr(lse), n_split, B, H, Nq, d,
+                                   _stream_handle(stream))
+    _check(st, "fa_merge_partials")
+    return o, lse
+
+
+def fa_fwd_splitkv(q, k, v, o=None, lse=None, workspace=None, n_split: int = 0, causal: bool = False,
+                   scale: float | None = None, stream=None):
+    """Split-KV attention (partials + merge): returns (o bf16 [B, H, Nq, d], lse fp32 [B, H, Nq]).
+
+    n_split <= 0 picks the library's default split count for the device.
+    """
+    import torch
+
+    lib = load_library()
+    B, H, Nq, Nk, d = _check_kv(q, k, v)
+    n = n_split if n_split > 0 else max(1, fa_splitkv_default_splits(B, H, Nq, Nk, d))
+    if o is None:
+        o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    _check_bhnd("o", o, (B, H, Nq, d), torch.bfloat16)
+    _check_bhnd("lse", lse.view(B, H, Nq, 1), (B, H, Nq, 1), torch.float32)
+    if workspace is None:
+        workspace = torch.empty(max(fa_splitkv_workspace_size(B, H, Nq, d, n), 1), dtype=torch.uint8,
+                                device=q.device)
+    sc = float(scale) if scale is not None else d ** -0.5
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace), _ws_bytes(workspace),
+                                B, H, Nq, Nk, d, n, int(bool(causal)), sc, _stream_handle(stream))
+    _check(st, "fa_fwd_splitkv")
+    return o, lse
 
 
 def fa_sync_check(stream=None):

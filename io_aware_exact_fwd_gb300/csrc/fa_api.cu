@@ -6,6 +6,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -161,6 +162,153 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   a.err_word = ds->err_word;
   a.dbg = knobs();
   return fa::launch_fwd_bf16(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+
+constexpr int kMaxSplits = 1024;
+
+struct SplitKvLayout {
+  size_t off_o, off_lse, total;
+};
+
+SplitKvLayout splitkv_layout(int B, int H, int Nq, int d, int n_split) {
+  const size_t rows = static_cast<size_t>(B) * H * Nq * n_split;
+  SplitKvLayout l;
+  l.off_o = 0;
+  l.off_lse = (rows * d * sizeof(float) + 255) & ~size_t(255);
+  l.total = l.off_lse + ((rows * sizeof(float) + 255) & ~size_t(255));
+  return l;
+}
+
+// Shape checks of the split-KV calls: FA_OK, a status, or -1 for "nothing to do".
+int validate_splitkv(int B, int H, int Nq, int Nk, int d, int n_split, int causal, float scale) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (n_split < 1 || n_split > kMaxSplits) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || Nq == 0) return -1;
+  if (Nk < 1) return FA_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long nunits = (static_cast<long long>(Nq) + 2 * fa::kBlockQ - 1) / (2 * fa::kBlockQ);
+  if (bh * nunits * n_split > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (bh * Nq > 0x7fffffffLL || bh * Nk > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+int default_splits(int B, int H, int Nq, int Nk) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess || sms < 1)
+    sms = 148;
+  const long long units = static_cast<long long>(B) * H * ((Nq + 2 * fa::kBlockQ - 1) / (2 * fa::kBlockQ));
+  const int nkb = (Nk + fa::kBlockK - 1) / fa::kBlockK;
+  // Many query rows and a full GPU: splitting would only add partials to merge.
+  if (Nq > fa::kBlockQ && units >= sms) return 1;
+  // Splits of at least 4 key blocks keep the per-unit Q load and epilogue small
+  // next to the key stream; at most 64 keep the merge's reads small.
+  const int n_max = static_cast<int>(std::min<long long>(std::max(1, nkb / 4), 64));
+  // Time of the busiest SM in units of one unsplit work unit: ceil(units n / sms) / n.
+  auto cost = [&](int n) { return static_cast<double>((units * n + sms - 1) / sms) / n; };
+  double best = cost(1);
+  for (int n = 2; n <= n_max; ++n) best = std::min(best, cost(n));
+  // The fewest splits within 2 % of the best balance.
+  for (int n = 1; n <= n_max; ++n)
+    if (cost(n) <= best * 1.02) return n;
+  return 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_splitkv_workspace_size(int B, int H, int Nq, int d, int n_split) {
+  if (validate_splitkv(B, H, Nq, 1, d, n_split, 0, 1.f) != FA_OK) return 0;
+  return splitkv_layout(B, H, Nq, d, n_split).total;
+}
+
+int fa_splitkv_default_splits(int B, int H, int Nq, int Nk, int d) {
+  if (validate_splitkv(B, H, Nq, Nk, d, 1, 0, 1.f) != FA_OK) return 0;
+  return default_splits(B, H, Nq, Nk);
+}
+
+int fa_fwd_splitkv_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int B, int H,
+                           int Nq, int Nk, int d, int n_split, int causal, float scale, fa_stream_t stream) {
+  const int vs = validate_splitkv(B, H, Nq, Nk, d, n_split, causal, scale);
+  if (vs < 0) return FA_OK;
+  if (vs != FA_OK) return vs;
+  if (!q || !k || !v || !o_part || !lse_part) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o_part, 16) || !aligned(lse_part, 4))
+    return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  const int st = device_state(&ds);
+  if (st != FA_OK) return st;
+  fa::SplitKvArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.n_split = n_split;
+  a.causal = causal;
+  a.scale = scale;
+  a.err_word = ds->err_word;
+  a.dbg = knobs();
+  return fa::launch_fwd_splitkv_partial(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                                   : FA_ERR_CUDA;
+}
+
+int fa_merge_partials(const float* o_part, const float* lse_part, void* o, float* lse, int n_split, int B, int H,
+                      int Nq, int d, fa_stream_t stream) {
+  const int vs = validate_splitkv(B, H, Nq, 1, d, n_split, 0, 1.f);
+  if (vs < 0) return FA_OK;
+  if (vs != FA_OK) return vs;
+  if (!o_part || !lse_part || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned(o_part, 16) || !aligned(lse_part, 4) || !aligned(o, 16) || !aligned(lse, 4)) return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  const int st = device_state(&ds);
+  if (st != FA_OK) return st;
+  fa::MergeArgs a;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.o = o;
+  a.lse = lse;
+  a.n_split = n_split;
+  a.BH = B * H;
+  a.Nq = Nq;
+  a.d = d;
+  return fa::launch_merge_partials(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace, size_t ws_bytes,
+                   int B, int H, int Nq, int Nk, int d, int n_split, int causal, float scale, fa_stream_t stream) {
+  if (n_split <= 0) {
+    const int pre = validate_splitkv(B, H, Nq, Nk, d, 1, causal, scale);
+    if (pre < 0) return FA_OK;
+    if (pre != FA_OK) return pre;
+    n_split = default_splits(B, H, Nq, Nk);
+  }
+  const int vs = validate_splitkv(B, H, Nq, Nk, d, n_split, causal, scale);
+  if (vs < 0) return FA_OK;
+  if (vs != FA_OK) return vs;
+  if (!o || !lse) return FA_ERR_INVALID_ARG;
+  const SplitKvLayout lay = splitkv_layout(B, H, Nq, d, n_split);
+  if (!workspace || ws_bytes < lay.total) return FA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  float* o_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lay.off_o);
+  float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lay.off_lse);
+  int st = fa_fwd_splitkv_partial(q, k, v, o_part, lse_part, B, H, Nq, Nk, d, n_split, causal, scale, stream);
+  if (st != FA_OK) return st;
+  return fa_merge_partials(o_part, lse_part, o, lse, n_split, B, H, Nq, d, stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {

@@ -111,13 +111,36 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-// Number of K/V blocks query tile t of work unit u attends to (0 if the tile is past N).
+// Key range of a launch and where its results go.  The plain forward has one
+// split covering all Nk = N keys.  The split-KV forward cuts the key blocks into
+// nsplit ranges of kbps blocks (split s: blocks [s kbps, (s+1) kbps)), aligns
+// causal queries with the last keys (query i sees key j iff j <= i + coff,
+// coff = Nk - Nq), and writes each split's normalised O (fp32) and LSE to
+// o_part [nsplit, BH, Nq, d] and lse_part [nsplit, BH, Nq].
+struct KeySplit {
+  int Nk;
+  int nsplit;
+  int kbps;
+  int coff;
+  float* o_part;
+  float* lse_part;
+};
+
+// K/V blocks [begin, begin + count) that query tile t of unit (u, split s) attends
+// to; count = 0 if the tile is past the last query row.
+struct KvSpan {
+  int begin, count;
+};
 template <bool CAUSAL>
-__device__ __forceinline__ int kv_blocks(int u, int t, int N) {
+__device__ __forceinline__ KvSpan kv_span(int u, int t, int s, int N, const KeySplit& ks) {
   const int row0 = u * kRowsPerCta + t * kBlockQ;
-  if (row0 >= N) return 0;
-  const int nkt_all = (N + kBlockK - 1) / kBlockK;
-  return CAUSAL ? min(row0 / kBlockK + 1, nkt_all) : nkt_all;
+  if (row0 >= N) return {0, 0};
+  const int nkb = (ks.Nk + kBlockK - 1) / kBlockK;
+  const int b = min(s * ks.kbps, nkb);
+  int e = min(b + ks.kbps, nkb);
+  // The tile's last row sees keys up to its index + coff.
+  if (CAUSAL) e = min(e, (min(row0 + kBlockQ - 1, N - 1) + ks.coff) / kBlockK + 1);
+  return {b, max(e - b, 0)};
 }
 
 // Dequantisation scales of the FP8 variant (unused by the bf16 one): per
@@ -129,17 +152,22 @@ struct Fp8Scales {
   int ntiles;
 };
 
-// Work unit w -> (256-row query block u, head bh).  Causal units are numbered
-// heaviest first (largest u first), so the zigzag assignment below hands every
-// CTA a similar total.
+// Work unit w -> (256-row query block u, head bh, key split s).  Causal units
+// are numbered heaviest first (largest u first), so the zigzag assignment below
+// hands every CTA a similar total.
 template <bool CAUSAL>
-__device__ __forceinline__ void decode_unit(int w, int nunits, int BH, int& u, int& bh) {
+__device__ __forceinline__ void decode_unit(int w, int nunits, int BH, int nsplit, int& u, int& bh, int& s) {
   if (CAUSAL) {
-    u = nunits - 1 - w / BH;
-    bh = w % BH;
+    const int per_u = BH * nsplit;
+    u = nunits - 1 - w / per_u;
+    const int r = w % per_u;
+    bh = r / nsplit;
+    s = r % nsplit;
   } else {
     u = w % nunits;
-    bh = w / nunits;
+    const int r = w / nunits;
+    s = r % nsplit;
+    bh = r / nsplit;
   }
 }
 
@@ -147,12 +175,13 @@ __device__ __forceinline__ void decode_unit(int w, int nunits, int BH, int& u, i
 // in increasing CTA order on even passes and decreasing on odd ones.
 __device__ __forceinline__ int unit_of(int k, int c, int G) { return k * G + ((k & 1) ? (G - 1 - c) : c); }
 
-template <int D, bool CAUSAL, bool FP8>
+template <int D, bool CAUSAL, bool FP8, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                float* __restrict__ lse, int N, int BH, int nunits, float scale_log2, unsigned int* err_word,
-               unsigned long long wait_ns, int fault, Fp8Scales f8) {
+               unsigned long long wait_ns, int fault, Fp8Scales f8, KeySplit ks) {
+  static_assert(!(SPLIT && FP8), "the split-KV variant is bf16 only");
   using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -176,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // Persistent CTAs: CTA c takes units unit_of(0, c, G), unit_of(1, c, G), ...
-  const int total = nunits * BH;
+  const int total = nunits * BH * ks.nsplit;
   const int G = static_cast<int>(gridDim.x);
   const int cta = static_cast<int>(blockIdx.x);
 
@@ -241,12 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; ok; ++k) {
         const int w = unit_of(k, cta, G);
         if (w >= total) break;
-        int u, bh;
-        decode_unit<CAUSAL>(w, nunits, BH, u, bh);
-        const int n_max = max(kv_blocks<CAUSAL>(u, 0, N), kv_blocks<CAUSAL>(u, 1, N));
+        int u, bh, sp;
+        decode_unit<CAUSAL>(w, nunits, BH, ks.nsplit, u, bh, sp);
+        const KvSpan a = kv_span<CAUSAL>(u, 0, sp, N, ks), b = kv_span<CAUSAL>(u, 1, sp, N, ks);
+        const int n_max = max(a.count, b.count);  // both tiles start at the split's first block
         for (int j = 0; ok && j < n_max; ++j) {
-          ok = push(&tm_k, j, bh);
-          if (ok) ok = push(&tm_v, j, bh);
+          ok = push(&tm_k, a.begin + j, bh);
+          if (ok) ok = push(&tm_v, a.begin + j, bh);
         }
       }
       if (!ok) {  // drain: the last (up to kSlots) issued copies may still be landing
@@ -265,10 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; ok; ++k) {
         const int w = unit_of(k, cta, G);
         if (w >= total) break;
-        int u, bh;
-        decode_unit<CAUSAL>(w, nunits, BH, u, bh);
+        int u, bh, sp;
+        decode_unit<CAUSAL>(w, nunits, BH, ks.nsplit, u, bh, sp);
         for (int t = 0; ok && t < kTiles; ++t) {
-          if (kv_blocks<CAUSAL>(u, t, N) == 0) continue;
+          if (kv_span<CAUSAL>(u, t, sp, N, ks).count == 0) continue;
           if (nload[t] > 0 && !(ok = mbar_wait(&bar_qe[t], (nload[t] - 1) & 1, wc, kSiteLoadQ))) break;
           mbar_arrive_expect_tx(&bar_q[t], C::kTileBytes);
 #pragma unroll
@@ -340,10 +370,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; ok; ++k) {
         const int w = unit_of(k, cta, G);
         if (w >= total) break;
-        int u, bh;
-        decode_unit<CAUSAL>(w, nunits, BH, u, bh);
-        const int nq[kTiles] = {kv_blocks<CAUSAL>(u, 0, N), kv_blocks<CAUSAL>(u, 1, N)};
+        int u, bh, sp;
+        decode_unit<CAUSAL>(w, nunits, BH, ks.nsplit, u, bh, sp);
+        const int nq[kTiles] = {kv_span<CAUSAL>(u, 0, sp, N, ks).count, kv_span<CAUSAL>(u, 1, sp, N, ks).count};
         const int n_max = max(nq[0], nq[1]);
+        if (n_max == 0) continue;  // an empty key split: nothing was loaded for it
         // Prologue: S_a = Q_a K_0^T, S_b = Q_b K_0^T.  S_t is free: the previous
         // unit's last P_t V MMA, which read P_t from it, was issued earlier.
         {
@@ -425,18 +456,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; ok; ++k) {
       const int w = unit_of(k, cta, G);
       if (w >= total) break;
-      int u, bh;
-      decode_unit<CAUSAL>(w, nunits, BH, u, bh);
-      const int n_a = kv_blocks<CAUSAL>(u, 0, N);
-      const int n_b = kv_blocks<CAUSAL>(u, 1, N);
-      const int nkt = t == 0 ? n_a : n_b;
+      int u, bh, sp;
+      decode_unit<CAUSAL>(w, nunits, BH, ks.nsplit, u, bh, sp);
+      const KvSpan span = kv_span<CAUSAL>(u, t, sp, N, ks);
+      const int n_a = kv_span<CAUSAL>(u, 0, sp, N, ks).count;
+      const int n_b = kv_span<CAUSAL>(u, 1, sp, N, ks).count;
+      const int nkt = span.count;
       // Epilogues run in (unit, tile) order through one staging buffer.
       const uint32_t epi_index = nepi + ((t == 1 && n_a > 0) ? 1u : 0u);
       nepi += (n_a > 0 ? 1u : 0u) + (n_b > 0 ? 1u : 0u);
-      if (nkt == 0) continue;
       const int qrow0 = u * kRowsPerCta + t * kBlockQ;
       const int qrow = qrow0 + row;
-      const int diag = qrow0 / kBlockK;        // K/V block on this tile's diagonal
+      if (nkt == 0) {
+        // No key of this split is visible to the tile: an empty partial.
+        if (SPLIT && qrow < N)
+          ks.lse_part[(static_cast<size_t>(sp) * BH + bh) * N + qrow] = -INFINITY;
+        continue;
+      }
       float m_used = -INFINITY;  // running maximum in log2 units (possibly stale, see header)
       float l = 0.f;
       // FP8: the row's Q scale joins the score scale; V scales are folded into P
@@ -464,15 +500,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const int kbase = j * kBlockK;
-        const bool need_mask = (kbase + kBlockK > N) || (CAUSAL && j == diag);
+        const int kbase = (span.begin + j) * kBlockK;
+        // Some key of the block is past Nk, or beyond what the tile's first row sees.
+        const bool need_mask = (kbase + kBlockK > ks.Nk) || (CAUSAL && kbase + kBlockK - 1 > qrow0 + ks.coff);
         // Per 64-key half h: multiplier c[h] of the raw score (FP8: times that key
         // tile's K scale) and lg[h] = log2 of the V-scale fold of P (0 for bf16).
         float ch[2] = {crow, crow}, lg[2] = {0.f, 0.f}, fv[2] = {1.f, 1.f};
         if constexpr (FP8) {
   #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int kt = 2 * j + h;
+            const int kt = 2 * (span.begin + j) + h;
             if (kt < f8.ntiles) {
               ch[h] = crow * skh[kt];
               fv[h] = svh[kt] * inv_svmax;
@@ -486,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int key = kbase + c * 32 + i;
-              if (key >= N || (CAUSAL && key > qrow)) r[c][i] = __float_as_uint(-INFINITY);
+              if (key >= ks.Nk || (CAUSAL && key > qrow + ks.coff)) r[c][i] = __float_as_uint(-INFINITY);
             }
           }
         };
@@ -646,6 +683,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- epilogue
       if (!(ok = warp_wait(&bar_o[t], ocnt & 1, wc, kSiteSoftO))) break;
       tc_fence_after();
+      if constexpr (SPLIT) {
+        // Partial of this split: O / l in fp32 straight from TMEM, LSE in natural
+        // log; a row that saw no key of the split gets LSE = -inf (O is not read).
+        const bool seen = l > 0.f;
+        const float inv_l = seen ? 1.f / l : 0.f;
+        float4* orow = reinterpret_cast<float4*>(ks.o_part + ((static_cast<size_t>(sp) * BH + bh) * N + qrow) * D);
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(trow + col_o + c * 32, o);
+          tmem_ld_wait32(o);
+          if (qrow < N) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              orow[c * 8 + i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                            __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+          }
+        }
+        tc_fence_before();
+        if (qrow < N)
+          ks.lse_part[(static_cast<size_t>(sp) * BH + bh) * N + qrow] = seen ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+        ++ocnt;
+        continue;
+      }
       // The staging buffer is free once the previous epilogue's store has read it.
       if (epi_index > 0 && !(ok = warp_wait(bar_stg, (epi_index - 1) & 1, wc, kSiteEpi))) break;
       const float inv_l = svmax / l;  // svmax = 1 for bf16
@@ -700,13 +761,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool FP8>
+template <int D, bool CAUSAL, bool FP8, bool SPLIT = false>
 cudaError_t launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                           float* lse, int N, int BH, float scale_log2, unsigned int* err_word, const DebugKnobs& dbg,
-                          const Fp8Scales& f8, cudaStream_t stream) {
+                          const Fp8Scales& f8, const KeySplit& ks, cudaStream_t stream) {
   using C = FwdCfg<D, FP8>;
   cudaError_t e;
-  auto kern = fwd_kernel<D, CAUSAL, FP8>;
+  auto kern = fwd_kernel<D, CAUSAL, FP8, SPLIT>;
   // Per device and idempotent; cheap enough to repeat on every launch.
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes))) return e;
   // setmaxnreg.inc can only draw on the registers the block was launched with; a
@@ -720,11 +781,15 @@ cudaError_t launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev))) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
-  dim3 grid(static_cast<unsigned>(min(nunits * BH, sms)));
+  const long long units = static_cast<long long>(nunits) * BH * ks.nsplit;
+  dim3 grid(static_cast<unsigned>(min(units, static_cast<long long>(sms))));
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, lse, N, BH, nunits, scale_log2, err_word,
-                                                   dbg.wait_limit_ns, dbg.fault, f8);
+                                                   dbg.wait_limit_ns, dbg.fault, f8, ks);
   return cudaGetLastError();
 }
+
+// The plain forward: one split over all N keys, queries aligned with keys.
+KeySplit whole_keys(int N) { return KeySplit{N, 1, (N + kBlockK - 1) / kBlockK, 0, nullptr, nullptr}; }
 
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
@@ -736,7 +801,21 @@ cudaError_t launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
   if ((e = make_tmap_3d(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockK))) return e;
   if ((e = make_tmap_3d(&to, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockQ))) return e;
   return launch_kernel<D, CAUSAL, false>(tq, tk, tv, to, a.lse, a.N, BH, a.scale * 1.4426950408889634f, a.err_word,
-                                         a.dbg, Fp8Scales{nullptr, nullptr, nullptr, 0}, stream);
+                                         a.dbg, Fp8Scales{nullptr, nullptr, nullptr, 0}, whole_keys(a.N), stream);
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_splitkv_impl(const SplitKvArgs& a, cudaStream_t stream) {
+  const int BH = a.B * a.H;
+  CUtensorMap tq, tk, tv;
+  cudaError_t e;
+  if ((e = make_tmap_3d(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.Nq, BH, kBoxCols, kBlockQ))) return e;
+  if ((e = make_tmap_3d(&tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.Nk, BH, kBoxCols, kBlockK))) return e;
+  if ((e = make_tmap_3d(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.Nk, BH, kBoxCols, kBlockK))) return e;
+  const KeySplit ks{a.Nk, a.n_split, splitkv_kbps(a.Nk, a.n_split), a.Nk - a.Nq, a.o_part, a.lse_part};
+  // The partial epilogue stores fp32 rows itself; the O tensor map is never used.
+  return launch_kernel<D, CAUSAL, false, true>(tq, tk, tv, tq, nullptr, a.Nq, BH, a.scale * 1.4426950408889634f,
+                                               a.err_word, a.dbg, Fp8Scales{nullptr, nullptr, nullptr, 0}, ks, stream);
 }
 
 template <bool CAUSAL>
@@ -756,7 +835,8 @@ cudaError_t launch_fwd_fp8_impl(const FwdArgs& a, const void* workspace, cudaStr
                      reinterpret_cast<const float*>(ws + lay.off_sv), lay.ntiles};
   // Scores of the rotated operands are d times the plain ones: fold 1/d into the scale.
   const float scale_log2 = a.scale * 1.4426950408889634f / static_cast<float>(D);
-  return launch_kernel<D, CAUSAL, true>(tq, tk, tv, to, a.lse, a.N, BH, scale_log2, a.err_word, a.dbg, f8, stream);
+  return launch_kernel<D, CAUSAL, true>(tq, tk, tv, to, a.lse, a.N, BH, scale_log2, a.err_word, a.dbg, f8,
+                                        whole_keys(a.N), stream);
 }
 
 }  // namespace
@@ -768,6 +848,16 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_fwd_fp8(const FwdArgs& a, const void* workspace, cudaStream_t stream) {
   return a.causal ? launch_fwd_fp8_impl<true>(a, workspace, stream) : launch_fwd_fp8_impl<false>(a, workspace, stream);
+}
+
+int splitkv_kbps(int Nk, int n_split) {
+  const int nkb = (Nk + kBlockK - 1) / kBlockK;
+  return (nkb + n_split - 1) / n_split;
+}
+
+cudaError_t launch_fwd_splitkv_partial(const SplitKvArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_splitkv_impl<64, true>(a, stream) : launch_splitkv_impl<64, false>(a, stream);
+  return a.causal ? launch_splitkv_impl<128, true>(a, stream) : launch_splitkv_impl<128, false>(a, stream);
 }
 
 }  // namespace fa

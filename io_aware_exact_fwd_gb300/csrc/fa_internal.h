@@ -38,6 +38,37 @@ struct FwdArgs {
 // Forward launcher (fa_fwd.cu).  Returns a cudaError_t.
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream);
 
+// Split-KV forward (fa_fwd.cu): the keys are cut into n_split ranges of
+// splitkv_kbps(Nk, n_split) 128-key blocks; for each range the normalised
+// partial O (fp32 [n_split, B*H, Nq, d]) and its LSE (fp32 [n_split, B*H, Nq],
+// -inf where a row sees no key of the range).  Causal queries are aligned with
+// the last keys (query i sees key j iff j <= i + Nk - Nq).
+struct SplitKvArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  float* o_part;
+  float* lse_part;
+  int B, H, Nq, Nk, d, n_split;
+  int causal;
+  float scale;
+  unsigned int* err_word;
+  DebugKnobs dbg;
+};
+int splitkv_kbps(int Nk, int n_split);
+cudaError_t launch_fwd_splitkv_partial(const SplitKvArgs& a, cudaStream_t stream);
+
+// Exact merge of split-KV partials into bf16 O [B*H, Nq, d] and fp32 LSE
+// [B*H, Nq] (fa_splitkv.cu).
+struct MergeArgs {
+  const float* o_part;
+  const float* lse_part;
+  void* o;
+  float* lse;
+  int n_split, BH, Nq, d;
+};
+cudaError_t launch_merge_partials(const MergeArgs& a, cudaStream_t stream);
+
 struct BwdArgs {
   const void* q;
   const void* k;

@@ -90,3 +90,31 @@ def test_product_path_does_not_import_the_oracle():
                 src = open(os.path.join(dirpath, fn), encoding="utf-8").read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", src, re.M), fn
                 assert "oracle/" not in src, fn
+
+
+def _part(lib, B=1, H=1, Nq=1, Nk=1000, d=128, n=4, causal=0, scale=0.125, q=FAKE, k=FAKE, v=FAKE, o=FAKE,
+          lse=FAKE):
+    vp = ctypes.c_void_p
+    return lib.fa_fwd_splitkv_partial(vp(q), vp(k), vp(v), vp(o), vp(lse), B, H, Nq, Nk, d, n, causal, scale,
+                                      vp(0))
+
+
+def test_splitkv_validation_statuses(lib):
+    assert _part(lib, n=0) == 1
+    assert _part(lib, n=1025) == 1
+    assert _part(lib, Nk=0) == 1
+    assert _part(lib, Nq=-1) == 1
+    assert _part(lib, causal=1, Nq=2000, Nk=1000) == 1   # causal needs Nq <= Nk
+    assert _part(lib, d=96) == 2
+    assert _part(lib, q=0) == 1
+    assert _part(lib, o=FAKE + 4) == 3
+    assert _part(lib, Nq=0, q=0, k=0, v=0, o=0, lse=0) == 0  # empty: no-op
+    vp = ctypes.c_void_p
+    assert lib.fa_merge_partials(vp(FAKE), vp(FAKE), vp(FAKE + 8), vp(FAKE), 2, 1, 1, 4, 64, vp(0)) == 3
+    assert lib.fa_merge_partials(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 0, 1, 1, 4, 64, vp(0)) == 1
+    # The combined call refuses a short workspace before any device work.
+    need = lib.fa_splitkv_workspace_size(2, 3, 5, 64, 7)
+    assert need >= 7 * 2 * 3 * 5 * (64 + 1) * 4
+    assert lib.fa_fwd_splitkv(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), need - 1, 2, 3, 5, 900, 64,
+                              7, 0, 0.125, vp(0)) == 6
+    assert lib.fa_splitkv_workspace_size(1, 1, 1, 96, 1) == 0
