@@ -85,9 +85,11 @@ FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* l
            int causal, float scale, fa_stream_t stream);
 
 /*
- * fa_bwd_workspace_size -- bytes of device workspace fa_bwd needs for these
- * sizes (0 if the sizes are invalid or unsupported).  The workspace holds an
- * fp32 dQ accumulator [B, H, N, d] and two fp32 vectors of B*H*roundup(N, 64).
+ * fa_bwd_workspace_size -- bytes of device workspace fa_bwd (and
+ * fa_bwd_deterministic) needs for these sizes (0 if the sizes are invalid or
+ * unsupported).  The workspace holds an fp32 dQ accumulator [B, H, N, d], two
+ * fp32 vectors of B*H*roundup(N, 64), and B*H*(roundup(N, 64)/64 + 2) floats of
+ * bounds used by the deterministic variant.
  */
 FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -115,6 +117,24 @@ FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                   void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
                   int causal, float scale, fa_stream_t stream);
+
+/*
+ * fa_bwd_deterministic -- fa_bwd whose dQ is the same bits on every run.
+ * The pages call the method exact and deterministic ("FlashAttention-2 (DE)",
+ * section "Leistung und Effizienz").  fa_bwd's dQ sums the contributions of the
+ * key blocks with fp32 atomic adds, whose order varies run to run; here each
+ * contribution is rounded once to an integer multiple of 2^-S and added as int32,
+ * and integer addition does not depend on order.  S is a power of two chosen per
+ * 64-row query block from a bound on |dQ| that holds for any inputs:
+ *     |dQacc_ic| <= 2 |dO_i| max_j |v_j| max_jc |k_jc|   (x 1.125 margin)
+ * so that every partial sum stays below 2^22 in magnitude; the rounding of each
+ * contribution is at most 2^-S / 2, far below the bf16 output's rounding.  dK and
+ * dV are those of fa_bwd (already reproducible).  Costs one extra pass over K and
+ * V for the bound.  Arguments, workspace and errors: exactly as fa_bwd.
+ */
+FA_API int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                                int B, int H, int N, int d, int causal, float scale, fa_stream_t stream);
 
 /*
  * The three stages of fa_bwd, for callers that schedule or time them one by one.

@@ -67,6 +67,8 @@ def load_library():
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, f, vp]
+    lib.fa_bwd_deterministic.restype = i
+    lib.fa_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, f, vp]
     lib.fa_bwd_prep.restype = i
     lib.fa_bwd_prep.argtypes = [vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, vp]
     lib.fa_bwd_main.restype = i
@@ -173,12 +175,13 @@ def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
 
 
 def fa_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, workspace=None, causal: bool = False,
-           scale: float | None = None, stream=None):
+           scale: float | None = None, stream=None, deterministic: bool = False):
     """bf16 attention backward (d = 128): returns (dq, dk, dv).
 
     q, k, v, o, do: bf16 CUDA tensors [B, H, N, d]; lse: fp32 [B, H, N] from fa_fwd
     with the same causal/scale.  Outputs are allocated if not given; the
     workspace (uint8 CUDA tensor of fa_bwd_workspace_size bytes) too.
+    ``deterministic=True`` calls fa_bwd_deterministic (dQ identical bits on every run).
     """
     import torch
 
@@ -199,10 +202,11 @@ def fa_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, workspace=None, causa
     if scale is None:
         scale = d ** -0.5
     with torch.cuda.device(q.device):
-        st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-                        _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, N, d,
-                        int(bool(causal)), float(scale), _stream_handle(stream))
-    _check(st, "fa_bwd")
+        fn = lib.fa_bwd_deterministic if deterministic else lib.fa_bwd
+        st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, N, d,
+                int(bool(causal)), float(scale), _stream_handle(stream))
+    _check(st, "fa_bwd_deterministic" if deterministic else "fa_bwd")
     return dq, dk, dv
 
 

@@ -361,6 +361,7 @@ int bwd_setup(fa::BwdArgs& a, unsigned use, const void* q, const void* k, const 
   a.N = N;
   a.d = d;
   a.causal = causal;
+  a.deterministic = 0;
   a.scale = scale;
   a.err_word = ds->err_word;
   a.dbg = knobs();
@@ -381,6 +382,18 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
                            dk, dv, workspace, ws_bytes, B, H, N, d, causal, scale);
   if (st < 0) return FA_OK;
   if (st != FA_OK) return st;
+  return status_of(fa::launch_bwd_bf16(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B,
+                         int H, int N, int d, int causal, float scale, fa_stream_t stream) {
+  fa::BwdArgs a;
+  const int st = bwd_setup(a, kUseQKV | kUseO | kUseDout | kUseLse | kUseDq | kUseDkDv, q, k, v, o, dout, lse, dq,
+                           dk, dv, workspace, ws_bytes, B, H, N, d, causal, scale);
+  if (st < 0) return FA_OK;
+  if (st != FA_OK) return st;
+  a.deterministic = 1;
   return status_of(fa::launch_bwd_bf16(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

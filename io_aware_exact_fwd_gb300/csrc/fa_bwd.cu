@@ -105,6 +105,28 @@ __device__ __forceinline__ bool warp_wait_b(uint64_t* bar, uint32_t parity, cons
   return __all_sync(0xffffffffu, ok);
 }
 
+// Deterministic dQ: fixed-point accumulation.  Every contribution of a key block
+// to dQacc[i, c] is sum_j dS_ij k_jc, and the whole sum over all key blocks obeys
+//   |sum_j dS_ij k_jc| <= sum_j |dS_ij| max|k| <= 2 max_j |dP_ij| max|k|
+//                      <= 2 |dO_i| max_j |v_j| max|k|
+// (|dS_ij| = P_ij |dP_ij - D_i| with D_i a P-weighted mean of dP_i., and
+// |dP_ij| = |dO_i . v_j| <= |dO_i| |v_j|).  With a 64-row block's largest |dO_i|,
+// the head's largest |v_j| and largest |k_jc|, and a 12.5 % margin for the bf16
+// rounding of P and dS, the power of two 2^S below puts every partial sum of the
+// block's rows under 2^22 in magnitude.  Contributions are rounded to integers
+// once (x 2^S, nearest) and added as int32: integer addition does not depend on
+// order, so dQ is the same bits on every run.  2^22 keeps the float-to-int step
+// a single add of 1.5 * 2^23 (the rounding is the fp32 add's).
+__device__ __forceinline__ int det_shift(float dq_block_max, float vmax, float kmax) {
+  const float bound = 2.25f * dq_block_max * vmax * kmax;
+  if (!(bound > 0.f)) return 100;           // all-zero block (or no data): nothing to scale
+  if (!(bound < 3.0e38f)) return -100;      // non-finite inputs: the result is undefined anyway
+  int e;
+  frexpf(bound, &e);                        // bound < 2^e
+  return max(-100, min(100, 22 - e));
+}
+__device__ __forceinline__ float pow2f(int s) { return __int_as_float((s + 127) << 23); }  // -126 <= s <= 127
+
 // Stage the 128 x 128 fp32 accumulator row of this thread as bf16 into a
 // 128-byte-swizzled [128 rows][64 cols] x 2 TMA box pair.
 __device__ __forceinline__ void stage_row_bf16(uint32_t taddr_row, uint8_t* boxes, int row, float mul) {
@@ -127,14 +149,14 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t taddr_row, uint8_t* boxe
   }
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool DET>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                     const float* __restrict__ lse2, const float* __restrict__ dvec, float* __restrict__ dq_acc,
-                    int N, int Npad, int BH, int nkb, float scale, float scale_log2, unsigned int* err_word,
-                    unsigned long long wait_ns) {
+                    const float* __restrict__ dq_bmax, const float* __restrict__ kv_max, int N, int Npad, int BH,
+                    int nkb, float scale, float scale_log2, unsigned int* err_word, unsigned long long wait_ns) {
   using C = BwdCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -420,11 +442,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = (i0 + it) * kBqB;
       float* dst = dq_acc + (static_cast<size_t>(bh) * N + q0) * kD + dcol;
       const int lim = min(kBqB, N - q0);
+      if constexpr (DET) {
+        const float mul = pow2f(det_shift(dq_bmax[static_cast<size_t>(bh) * (Npad / kBqB) + i0 + it],
+                                          kv_max[2 * bh], kv_max[2 * bh + 1]));
+        constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: x + kMagic rounds x to an integer in the low bits
+        int* dsti = reinterpret_cast<int*>(dst);
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (h * 32 + c < lim) atomicAdd(dst + static_cast<size_t>(h * 32 + c) * kD, __uint_as_float(v[h][c]));
+          for (int c = 0; c < 32; ++c)
+            if (h * 32 + c < lim)
+              atomicAdd(dsti + static_cast<size_t>(h * 32 + c) * kD,
+                        __float_as_int(fmaf(__uint_as_float(v[h][c]), mul, kMagic)) - 0x4B400000);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (h * 32 + c < lim) atomicAdd(dst + static_cast<size_t>(h * 32 + c) * kD, __uint_as_float(v[h][c]));
+      }
     }
     __syncwarp();
   }
@@ -439,17 +475,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // D_i = sum_c dO_ic O_ic ; LSE2_i = LSE_i * log2(e) (rows >= N: D = 0, LSE2 = +inf);
 // dQacc rows < N are zeroed.  16 threads per row, 8 elements each.
+template <bool DET>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              const float* __restrict__ lse, float* __restrict__ dvec,
                                                              float* __restrict__ lse2, float* __restrict__ dq_acc,
-                                                             int N, int Npad, long long rows_pad) {
+                                                             unsigned int* __restrict__ dq_bmax, int N, int Npad,
+                                                             long long rows_pad) {
   const long long r = static_cast<long long>(blockIdx.x) * 16 + (threadIdx.x >> 4);
   const int t = threadIdx.x & 15;
-  if (r >= rows_pad) return;
+  // The grid is exactly rows_pad / 16 blocks (Npad is a multiple of 64), so every
+  // thread has a row and all of them reach the shuffles and the barrier below.
   const long long bh = r / Npad;
   const int nrow = static_cast<int>(r - bh * Npad);
-  float acc = 0.f;
+  float acc = 0.f, nrm = 0.f;
   if (nrow < N) {
     const size_t base = (static_cast<size_t>(bh) * N + nrow) * kD + t * 8;
     const uint4 ov = *reinterpret_cast<const uint4*>(o + base);
@@ -462,6 +501,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
       const float2 g = __bfloat1622float2(gp[e]);
       acc = fmaf(a.x, g.x, acc);
       acc = fmaf(a.y, g.y, acc);
+      if (DET) {
+        nrm = fmaf(g.x, g.x, nrm);
+        nrm = fmaf(g.y, g.y, nrm);
+      }
     }
     float4* z = reinterpret_cast<float4*>(dq_acc + base);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -473,16 +516,103 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     dvec[r] = nrow < N ? acc : 0.f;
     lse2[r] = nrow < N ? lse[static_cast<size_t>(bh) * N + nrow] * kLog2e : INFINITY;
   }
+  if (DET) {
+    // The block's 16 rows lie in one 64-row query block (Npad and the block
+    // start are multiples of 16): reduce to one atomic per block.
+#pragma unroll
+    for (int m = 8; m >= 1; m >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, m, 16);
+    float mx = sqrtf(nrm);  // 0 for padded rows
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    __shared__ float red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red[w]);
+      const long long r_first = static_cast<long long>(blockIdx.x) * 16;
+      const long long bh0 = r_first / Npad;
+      atomicMax(dq_bmax + bh0 * (Npad / kBqB) + (r_first - bh0 * Npad) / kBqB, __float_as_uint(mx));
+    }
+  }
 }
 
-// dQ = bf16(scale * dQacc), 8 elements per thread.
+// Deterministic mode: per head, the largest |v_j| and the largest |k_jc| (atomicMax
+// on float bits, both >= 0).  A block of 256 threads covers 256 rows of one head
+// (16 threads per row, 8 elements each, 16 rows per pass) and issues one atomic
+// per value.
+constexpr int kBoundRows = 256;
+__global__ void __launch_bounds__(256) bwd_kv_bound_kernel(const __nv_bfloat16* __restrict__ k,
+                                                           const __nv_bfloat16* __restrict__ v,
+                                                           unsigned int* __restrict__ kv_max, int N) {
+  const int bh = blockIdx.y;
+  const int t = threadIdx.x & 15;
+  const int r0 = blockIdx.x * kBoundRows + (threadIdx.x >> 4);
+  float km = 0.f, vm = 0.f;
+  // Every thread runs all passes (the shuffles below need the whole warp); rows
+  // past N contribute zeros.
+#pragma unroll 1
+  for (int pass = 0; pass < kBoundRows / 16; ++pass) {
+    const int r = r0 + pass * 16;
+    uint4 kv4 = make_uint4(0, 0, 0, 0), vv4 = make_uint4(0, 0, 0, 0);
+    if (r < N) {
+      const size_t base = (static_cast<size_t>(bh) * N + r) * kD + t * 8;
+      kv4 = *reinterpret_cast<const uint4*>(k + base);
+      vv4 = *reinterpret_cast<const uint4*>(v + base);
+    }
+    const __nv_bfloat162* kp = reinterpret_cast<const __nv_bfloat162*>(&kv4);
+    const __nv_bfloat162* vp = reinterpret_cast<const __nv_bfloat162*>(&vv4);
+    float vn = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 a = __bfloat1622float2(kp[e]);
+      const float2 b = __bfloat1622float2(vp[e]);
+      km = fmaxf(km, fmaxf(fabsf(a.x), fabsf(a.y)));
+      vn = fmaf(b.x, b.x, fmaf(b.y, b.y, vn));
+    }
+#pragma unroll
+    for (int m = 8; m >= 1; m >>= 1) vn += __shfl_xor_sync(0xffffffffu, vn, m, 16);
+    vm = fmaxf(vm, sqrtf(vn));
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, m));
+    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, m));
+  }
+  __shared__ float red[2][8];
+  if ((threadIdx.x & 31) == 0) {
+    red[0][threadIdx.x >> 5] = vm;
+    red[1][threadIdx.x >> 5] = km;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < 8; ++w) {
+      vm = fmaxf(vm, red[0][w]);
+      km = fmaxf(km, red[1][w]);
+    }
+    atomicMax(kv_max + 2 * bh, __float_as_uint(vm));
+    atomicMax(kv_max + 2 * bh + 1, __float_as_uint(km));
+  }
+}
+
+// dQ = bf16(scale * dQacc), 8 elements per thread.  Deterministic mode: the
+// accumulator holds integers in units of 2^-S of the row block's shift S.
+template <bool DET>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ dq_acc,
                                                              __nv_bfloat16* __restrict__ dq, float scale,
-                                                             long long n8) {
+                                                             long long n8, const float* __restrict__ dq_bmax,
+                                                             const float* __restrict__ kv_max, int N, int Npad) {
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= n8) return;
-  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * idx];
-  const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * idx + 1];
+  float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * idx];
+  float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * idx + 1];
+  if (DET) {
+    const long long row = idx * 8 / kD;  // (bh, query row) flattened
+    const long long bh = row / N;
+    const int qrow = static_cast<int>(row - bh * N);
+    const float inv = pow2f(-det_shift(dq_bmax[bh * (Npad / kBqB) + qrow / kBqB], kv_max[2 * bh], kv_max[2 * bh + 1]));
+    auto cv = [&](float x) { return static_cast<float>(__float_as_int(x)) * inv; };
+    a = make_float4(cv(a.x), cv(a.y), cv(a.z), cv(a.w));
+    b = make_float4(cv(b.x), cv(b.y), cv(b.z), cv(b.w));
+  }
   uint4 out;
   out.x = pack_bf16x2(a.x * scale, a.y * scale);
   out.y = pack_bf16x2(a.z * scale, a.w * scale);
@@ -503,7 +633,9 @@ BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
   w.off_dq = 0;
   w.off_d = align256(bh * N * d * sizeof(float));
   w.off_lse2 = w.off_d + align256(bh * npad * sizeof(float));
-  w.total = w.off_lse2 + align256(bh * npad * sizeof(float));
+  w.off_dqmax = w.off_lse2 + align256(bh * npad * sizeof(float));
+  w.off_kvmax = w.off_dqmax + align256(bh * (npad / kBqB) * sizeof(float));
+  w.total = w.off_kvmax + align256(bh * 2 * sizeof(float));
   return w;
 }
 
@@ -512,10 +644,21 @@ cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream) {
   const BwdWorkspace w = bwd_workspace_layout(a.B, a.H, a.N, a.d);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   const long long rows_pad = static_cast<long long>(BH) * w.npad;
-  bwd_preprocess_kernel<<<static_cast<unsigned>((rows_pad + 15) / 16), 256, 0, stream>>>(
+  unsigned int* dq_bmax = reinterpret_cast<unsigned int*>(ws + w.off_dqmax);
+  if (a.deterministic) {
+    // The block and head maxima are built with atomicMax from zero.
+    cudaError_t e = cudaMemsetAsync(ws + w.off_dqmax, 0, w.total - w.off_dqmax, stream);
+    if (e) return e;
+    bwd_kv_bound_kernel<<<dim3(static_cast<unsigned>((a.N + kBoundRows - 1) / kBoundRows), BH), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.v),
+        reinterpret_cast<unsigned int*>(ws + w.off_kvmax), a.N);
+    if ((e = cudaGetLastError())) return e;
+  }
+  auto kern = a.deterministic ? bwd_preprocess_kernel<true> : bwd_preprocess_kernel<false>;
+  kern<<<static_cast<unsigned>((rows_pad + 15) / 16), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
       reinterpret_cast<float*>(ws + w.off_d), reinterpret_cast<float*>(ws + w.off_lse2),
-      reinterpret_cast<float*>(ws + w.off_dq), a.N, w.npad, rows_pad);
+      reinterpret_cast<float*>(ws + w.off_dq), dq_bmax, a.N, w.npad, rows_pad);
   return cudaGetLastError();
 }
 
@@ -532,7 +675,8 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
   if ((e = make_tmap_3d(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBkB))) return e;
   if ((e = make_tmap_3d(&tdk, a.dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBkB))) return e;
   if ((e = make_tmap_3d(&tdv, a.dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBkB))) return e;
-  auto kern = a.causal ? bwd_main_kernel<true> : bwd_main_kernel<false>;
+  auto kern = a.deterministic ? (a.causal ? bwd_main_kernel<true, true> : bwd_main_kernel<false, true>)
+                              : (a.causal ? bwd_main_kernel<true, false> : bwd_main_kernel<false, false>);
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes))) return e;
   // The register split assumes the block launches with kLaunchRegs per thread.
   cudaFuncAttributes fattr;
@@ -541,17 +685,21 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
   const int nkb = (a.N + kBkB - 1) / kBkB;
   kern<<<static_cast<unsigned>(nkb * BH), kThreads, C::kSmemBytes, stream>>>(
       tq, tk, tv, tdo, tdk, tdv, reinterpret_cast<const float*>(ws + w.off_lse2),
-      reinterpret_cast<const float*>(ws + w.off_d), reinterpret_cast<float*>(ws + w.off_dq), a.N, w.npad, BH, nkb,
-      a.scale, a.scale * kLog2e, a.err_word, a.dbg.wait_limit_ns);
+      reinterpret_cast<const float*>(ws + w.off_d), reinterpret_cast<float*>(ws + w.off_dq),
+      reinterpret_cast<const float*>(ws + w.off_dqmax), reinterpret_cast<const float*>(ws + w.off_kvmax), a.N, w.npad,
+      BH, nkb, a.scale, a.scale * kLog2e, a.err_word, a.dbg.wait_limit_ns);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream) {
   const BwdWorkspace w = bwd_workspace_layout(a.B, a.H, a.N, a.d);
-  const float* dq_acc = reinterpret_cast<const float*>(static_cast<uint8_t*>(a.workspace) + w.off_dq);
+  const uint8_t* ws = static_cast<const uint8_t*>(a.workspace);
+  const float* dq_acc = reinterpret_cast<const float*>(ws + w.off_dq);
   const long long n8 = static_cast<long long>(a.B) * a.H * a.N * kD / 8;
-  bwd_dq_convert_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
-      dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.scale, n8);
+  auto kern = a.deterministic ? bwd_dq_convert_kernel<true> : bwd_dq_convert_kernel<false>;
+  kern<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
+      dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.scale, n8, reinterpret_cast<const float*>(ws + w.off_dqmax),
+      reinterpret_cast<const float*>(ws + w.off_kvmax), a.N, w.npad);
   return cudaGetLastError();
 }
 

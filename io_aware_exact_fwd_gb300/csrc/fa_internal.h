@@ -82,16 +82,19 @@ struct BwdArgs {
   void* workspace;
   int B, H, N, d;
   int causal;
+  int deterministic;  // 1: dQ accumulates as fixed-point integers (bitwise reproducible)
   float scale;
   unsigned int* err_word;
   DebugKnobs dbg;
 };
 
-// Workspace of the backward: fp32 dQ accumulator [BH, N, d], then D and
-// LSE * log2(e), each [BH, npad] with npad = N rounded up to 64.  Every region
-// starts on a 256-byte boundary.
+// Workspace of the backward: fp32 dQ accumulator [BH, N, d] (int32 in the
+// deterministic mode), then D and LSE * log2(e), each [BH, npad] with npad = N
+// rounded up to 64, then (deterministic mode) the largest |dO_i| per 64-row
+// block [BH, npad / 64] and the head's largest |v_j| and |k_jc| [BH, 2].  Every
+// region starts on a 256-byte boundary.
 struct BwdWorkspace {
-  size_t off_dq, off_d, off_lse2, total;
+  size_t off_dq, off_d, off_lse2, off_dqmax, off_kvmax, total;
   int npad;
 };
 BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d);
