@@ -270,6 +270,8 @@ def run_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
     d2h = sum(t.numel() * t.element_size() for t in houts)
 
+    nxt = next_rows(fa, q, k, v, g, o, lse, dq, dk, dv, ws, causal, scale, stage_ms) if rank == 0 else None
+
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -345,11 +347,87 @@ def run_ours(args):
         "wall_s_timed_region": round(t_wall, 3),
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "next": finish_next_rows(nxt, peaks),
     }
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return line
+
+
+# Rows past the hot path, timed after the step (not part of `value`): the split-KV
+# decode forward on its own workload, and the deterministic backward on the step's.
+DECODE = {"B": 8, "H": 16, "Nq": 1, "Nk": 32768, "d": 128, "causal": False, "seed": 5}
+
+
+def _median_ms(fn, reps, flush=None):
+    import torch
+
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return sorted(x.elapsed_time(y) for x, y in ts)[reps // 2]
+
+
+def next_rows(fa, q, k, v, g, o, lse, dq, dk, dv, ws, causal, scale, stage_ms):
+    import torch
+
+    from synth import normal_qkv
+
+    out = {}
+    w = DECODE
+    B, H, Nq, Nk, d = w["B"], w["H"], w["Nq"], w["Nk"], w["d"]
+    kv = normal_qkv(B, H, Nk, d, w["seed"])
+    qd = normal_qkv(B, H, Nq, d, w["seed"] + 1)["q"].to(torch.bfloat16).cuda()
+    kd, vd = kv["k"].to(torch.bfloat16).cuda(), kv["v"].to(torch.bfloat16).cuda()
+    del kv
+    n = fa.fa_splitkv_default_splits(B, H, Nq, Nk, d)
+    wsd = torch.empty(fa.fa_splitkv_workspace_size(B, H, Nq, d, n), dtype=torch.uint8, device="cuda")
+    od = torch.empty_like(qd)
+    lsed = torch.empty(B, H, Nq, dtype=torch.float32, device="cuda")
+    call = lambda: fa.fa_fwd_splitkv(qd, kd, vd, od, lsed, wsd, n_split=n, causal=w["causal"])
+    for _ in range(3):
+        call()
+    ms = _median_ms(call, 20)  # K and V (2.1 GB) are far larger than L2
+    byts = 4 * B * H * Nk * d + 4 * B * H * Nq * d + 8 * n * B * H * Nq * (d + 1)
+    out["splitkv_decode"] = {"config": dict(w, n_split=n), "ms": round(ms, 5), "bytes": byts, "gbs": byts / ms / 1e6,
+                             "launches": 2}
+    del kd, vd
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    det = lambda: fa.fa_bwd(q, k, v, o, g, lse, dq, dk, dv, ws, causal=causal, scale=scale, deterministic=True)
+    for _ in range(3):
+        det()
+    ms_det = _median_ms(det, 20, flush)
+    fa.fa_sync_check()
+    out["bwd_deterministic"] = {"ms": round(ms_det, 5),
+                                "ms_atomic": round(stage_ms["bwd_prep"] + stage_ms["bwd_main"] + stage_ms["bwd_dq"], 5),
+                                "launches": 4}
+    return out
+
+
+def finish_next_rows(nxt, peaks):
+    if nxt is None:
+        return None
+    w = WORKLOAD
+    sk = nxt["splitkv_decode"]
+    f_bwd = 2.5 * fwd_flops(w["B"], w["H"], w["N"], w["d"], w["causal"])
+    bd = nxt["bwd_deterministic"]
+    return {
+        "splitkv_decode": {"workload": "split-KV decode forward + merge", "config": sk["config"], "ms": sk["ms"],
+                           "bound": "hbm", "achieved": round(sk["gbs"], 1), "unit": "GB/s",
+                           "peak": peaks["hbm_gbs"], "frac": round(sk["gbs"] / peaks["hbm_gbs"], 4),
+                           "algorithmic_bytes": sk["bytes"], "gpu_launches": sk["launches"]},
+        "bwd_deterministic": {"workload": "bf16 backward with order-free dQ, the step's configuration",
+                              "ms": bd["ms"], "tflops": round(f_bwd / (bd["ms"] * 1e-3) / 1e12, 1),
+                              "ms_atomic_dq": bd["ms_atomic"], "gpu_launches": bd["launches"]},
+    }
 
 
 def _oracle_step_sample(q, k, v, g, scale, causal, head, r0, rows_per_step):
