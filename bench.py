@@ -92,6 +92,24 @@ def profile_traffic(profile: str, source: str):
         return None
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time: every rank gets the maximum (a no-op for one process)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: the work of every rank over the slowest rank's time."""
+    return flops_per_rank_step * steps * world / (max_ms * 1e-3) / 1e12
+
+
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
         os.environ.get("LOCAL_RANK", "0"))
@@ -228,15 +246,11 @@ def run_ours(args):
     stage_ms = {st: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
                 for j, st in enumerate(stages)}
     dev_ms = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps))
-    if world > 1:
-        t = torch.tensor([dev_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.barrier()
-        dev_ms = float(t.item())
+    dev_ms = max_over_ranks(dev_ms, "cuda")
     f_fwd = fwd_flops(B, H, N, d, causal)
     flops_step = 4.5 * f_fwd  # bf16 forward + backward (2.5x) + FP8 forward
     ms_per_step = dev_ms / args.steps
-    value = flops_step * args.steps * world / (dev_ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops_step, args.steps, world, dev_ms)
 
     # End to end through the public calls: pinned host inputs in, every output back out.
     hq, hk, hv, hg = (t.cpu().pin_memory() for t in (q, k, v, g))
