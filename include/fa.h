@@ -85,6 +85,20 @@ FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* l
            int causal, float scale, fa_stream_t stream);
 
 /*
+ * fa_fwd_strided -- fa_fwd for tensors in other layouts, e.g. [B, N, H, d] as a
+ * projection produces it before any transpose.  Element (b, h, n, c) of a tensor
+ * lives at ptr + b*strides[2] + h*strides[1] + n*strides[0] + c (in elements; d is
+ * contiguous).  A NULL strides pointer means the dense [B, H, N, d] layout
+ * {d, N*d, H*N*d}.  Every stride must be positive and a multiple of 8 elements
+ * (16 bytes; FA_ERR_MISALIGNED otherwise), and strides[0] >= d.  Output rows must
+ * not overlap one another or any input.  LSE stays dense [B, H, N].  Results are
+ * bitwise those of fa_fwd on the same values laid out densely.
+ */
+FA_API int fa_fwd_strided(const void* q, const int64_t* q_strides, const void* k, const int64_t* k_strides,
+                          const void* v, const int64_t* v_strides, void* o, const int64_t* o_strides, float* lse,
+                          int B, int H, int N, int d, int causal, float scale, fa_stream_t stream);
+
+/*
  * fa_bwd_workspace_size -- bytes of device workspace fa_bwd (and
  * fa_bwd_deterministic) needs for these sizes (0 if the sizes are invalid or
  * unsupported).  The workspace holds an fp32 dQ accumulator [B, H, N, d], two
@@ -117,6 +131,20 @@ FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                   void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
                   int causal, float scale, fa_stream_t stream);
+
+/*
+ * fa_bwd_strided -- fa_bwd (deterministic = 0) or fa_bwd_deterministic
+ * (deterministic = 1) for strided tensors, with the stride rules of
+ * fa_fwd_strided for each of q, k, v, o, dout, dq, dk, dv (NULL = dense).  The
+ * workspace and LSE stay dense.  Results are bitwise those of the dense call on
+ * the same values (dQ of the non-deterministic mode up to its summation order).
+ */
+FA_API int fa_bwd_strided(const void* q, const int64_t* q_strides, const void* k, const int64_t* k_strides,
+                          const void* v, const int64_t* v_strides, const void* o, const int64_t* o_strides,
+                          const void* dout, const int64_t* dout_strides, const float* lse, void* dq,
+                          const int64_t* dq_strides, void* dk, const int64_t* dk_strides, void* dv,
+                          const int64_t* dv_strides, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
+                          int causal, float scale, int deterministic, fa_stream_t stream);
 
 /*
  * fa_bwd_deterministic -- fa_bwd whose dQ is the same bits on every run.

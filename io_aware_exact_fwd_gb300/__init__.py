@@ -67,6 +67,10 @@ def load_library():
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.fa_bwd.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, f, vp]
+    lib.fa_fwd_strided.restype = i
+    lib.fa_fwd_strided.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.fa_bwd_strided.restype = i
+    lib.fa_bwd_strided.argtypes = [vp] * 17 + [vp, ctypes.c_size_t, i, i, i, i, i, f, i, vp]
     lib.fa_bwd_deterministic.restype = i
     lib.fa_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, f, vp]
     lib.fa_bwd_prep.restype = i
@@ -141,30 +145,59 @@ def _check_bhnd(name, t, shape, dtype):
         raise ValueError(f"{name} must be contiguous ([B, H, N, d] row-major)")
 
 
+def _strides(t):
+    """(row, head, batch) element strides of a [B, H, N, d] tensor with contiguous d, as int64[3]."""
+    arr = (ctypes.c_int64 * 3)(t.stride(2), t.stride(1), t.stride(0))
+    return ctypes.cast(arr, ctypes.c_void_p)  # the cast keeps the array alive
+
+
+def _check_strided(name, t, shape, dtype):
+    """Like _check_bhnd, but any layout whose last dimension is contiguous is accepted."""
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.stride(3) != 1:
+        raise ValueError(f"{name} must have a contiguous last dimension")
+
+
 def fa_fwd(q, k, v, o=None, lse=None, causal: bool = False, scale: float | None = None, stream=None):
     """bf16 attention forward: returns (o, lse).
 
-    q, k, v: bf16 CUDA tensors [B, H, N, d], contiguous.  ``o`` (bf16 [B,H,N,d]) and
-    ``lse`` (fp32 [B,H,N]) are allocated if not given.  ``scale`` defaults to 1/sqrt(d).
+    q, k, v: bf16 CUDA tensors indexed [B, H, N, d] with contiguous d: dense, or any
+    strided view such as x.view(B, N, H, d).transpose(1, 2) (fa_fwd_strided).  ``o``
+    (bf16 [B,H,N,d], allocated dense if not given, any such layout if given) and
+    ``lse`` (fp32 [B,H,N], dense).  ``scale`` defaults to 1/sqrt(d).
     """
     import torch
 
     lib = load_library()
     B, H, N, d = q.shape
     for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_bhnd(name, t, (B, H, N, d), torch.bfloat16)
+        _check_strided(name, t, (B, H, N, d), torch.bfloat16)
     if o is None:
-        o = torch.empty_like(q)
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    _check_bhnd("o", o, (B, H, N, d), torch.bfloat16)
+    _check_strided("o", o, (B, H, N, d), torch.bfloat16)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 tensor [B, H, N]")
     if scale is None:
         scale = d ** -0.5
     with torch.cuda.device(q.device):
-        st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
-                        float(scale), _stream_handle(stream))
+        if all(t.is_contiguous() for t in (q, k, v, o)):
+            st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
+                            float(scale), _stream_handle(stream))
+        else:
+            st = lib.fa_fwd_strided(_ptr(q), _strides(q), _ptr(k), _strides(k), _ptr(v), _strides(v), _ptr(o),
+                                    _strides(o), _ptr(lse), B, H, N, d, int(bool(causal)), float(scale),
+                                    _stream_handle(stream))
     _check(st, "fa_fwd")
     return o, lse
 
@@ -188,24 +221,32 @@ def fa_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, workspace=None, causa
     lib = load_library()
     B, H, N, d = q.shape
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
-        _check_bhnd(name, t, (B, H, N, d), torch.bfloat16)
+        _check_strided(name, t, (B, H, N, d), torch.bfloat16)
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 tensor [B, H, N]")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dense = lambda: torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device)
+    dq = dense() if dq is None else dq
+    dk = dense() if dk is None else dk
+    dv = dense() if dv is None else dv
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        _check_bhnd(name, t, (B, H, N, d), torch.bfloat16)
+        _check_strided(name, t, (B, H, N, d), torch.bfloat16)
     need = int(lib.fa_bwd_workspace_size(B, H, N, d))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     if scale is None:
         scale = d ** -0.5
     with torch.cuda.device(q.device):
-        fn = lib.fa_bwd_deterministic if deterministic else lib.fa_bwd
-        st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-                _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, N, d,
-                int(bool(causal)), float(scale), _stream_handle(stream))
+        if all(t.is_contiguous() for t in (q, k, v, o, do, dq, dk, dv)):
+            fn = lib.fa_bwd_deterministic if deterministic else lib.fa_bwd
+            st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                    _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, N, d,
+                    int(bool(causal)), float(scale), _stream_handle(stream))
+        else:
+            st = lib.fa_bwd_strided(_ptr(q), _strides(q), _ptr(k), _strides(k), _ptr(v), _strides(v), _ptr(o),
+                                    _strides(o), _ptr(do), _strides(do), _ptr(lse), _ptr(dq), _strides(dq), _ptr(dk),
+                                    _strides(dk), _ptr(dv), _strides(dv), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), B, H, N, d, int(bool(causal)),
+                                    float(scale), int(bool(deterministic)), _stream_handle(stream))
     _check(st, "fa_bwd_deterministic" if deterministic else "fa_bwd")
     return dq, dk, dv
 

@@ -98,6 +98,22 @@ int validate_shape(int B, int H, int N, int d, int causal, float scale) {
   return FA_OK;
 }
 
+// Row, head and batch strides of a strided tensor (NULL: dense [B, H, N, d]).  Each
+// must be positive and a multiple of 8 elements (16 bytes), as the tensor maps need.
+int strides_or_dense(fa::Strides* out, const int64_t* s, int H, int N, int d) {
+  if (!s) {
+    *out = fa::dense_strides(H, N, d);
+    return FA_OK;
+  }
+  for (int i = 0; i < 3; ++i) {
+    if (s[i] <= 0 || s[i] > (int64_t(1) << 38)) return FA_ERR_INVALID_ARG;
+    if (s[i] % 8 != 0) return FA_ERR_MISALIGNED;
+    out->s[i] = s[i];
+  }
+  if (s[0] < d) return FA_ERR_INVALID_ARG;  // rows of one head may not overlap
+  return FA_OK;
+}
+
 }  // namespace
 
 namespace fa {
@@ -112,6 +128,23 @@ cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int cols,
+                         int rows, int heads, int batch, const int64_t strides[3], int box_cols, int box_rows) {
+  if (!g_encode) return cudaErrorInitializationError;
+  // strides: {row, head, batch} in elements; the column stride is 1.
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch)};
+  const cuuint64_t gstr[3] = {static_cast<cuuint64_t>(strides[0]) * elem_bytes,
+                              static_cast<cuuint64_t>(strides[1]) * elem_bytes,
+                              static_cast<cuuint64_t>(strides[2]) * elem_bytes};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(map, dtype, 4, const_cast<void*>(base), dims, gstr, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -136,18 +169,24 @@ const char* fa_strerror(int status) {
 
 int fa_version(void) { return (0 << 16) | 1; }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int causal,
-           float scale, fa_stream_t stream) {
+int fa_fwd_strided(const void* q, const int64_t* q_strides, const void* k, const int64_t* k_strides, const void* v,
+                   const int64_t* v_strides, void* o, const int64_t* o_strides, float* lse, int B, int H, int N, int d,
+                   int causal, float scale, fa_stream_t stream) {
   const int vs = validate_shape(B, H, N, d, causal, scale);
   if (vs < 0) return FA_OK;
   if (vs != FA_OK) return vs;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa::FwdArgs a;
+  int st = strides_or_dense(&a.sq, q_strides, H, N, d);
+  if (st == FA_OK) st = strides_or_dense(&a.sk, k_strides, H, N, d);
+  if (st == FA_OK) st = strides_or_dense(&a.sv, v_strides, H, N, d);
+  if (st == FA_OK) st = strides_or_dense(&a.so, o_strides, H, N, d);
+  if (st != FA_OK) return st;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return FA_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
-  const int st = device_state(&ds);
+  st = device_state(&ds);
   if (st != FA_OK) return st;
-  fa::FwdArgs a;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -162,6 +201,11 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   a.err_word = ds->err_word;
   a.dbg = knobs();
   return fa::launch_fwd_bf16(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d, int causal,
+           float scale, fa_stream_t stream) {
+  return fa_fwd_strided(q, nullptr, k, nullptr, v, nullptr, o, nullptr, lse, B, H, N, d, causal, scale, stream);
 }
 
 }  // extern "C"
@@ -328,7 +372,7 @@ enum BwdUse : unsigned {
 // Validation shared by fa_bwd and its three stages; fills `a` on success.
 int bwd_setup(fa::BwdArgs& a, unsigned use, const void* q, const void* k, const void* v, const void* o,
               const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
-              int B, int H, int N, int d, int causal, float scale) {
+              int B, int H, int N, int d, int causal, float scale, const int64_t* const* strides = nullptr) {
   const int vs = validate_shape(B, H, N, d, causal, scale);
   if (vs < 0) return -1;
   if (vs != FA_OK) return vs;
@@ -338,6 +382,12 @@ int bwd_setup(fa::BwdArgs& a, unsigned use, const void* q, const void* k, const 
     return FA_ERR_INVALID_ARG;
   if (!workspace) return FA_ERR_WORKSPACE;
   if (ws_bytes < fa::bwd_workspace_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
+  // strides (optional): q, k, v, o, dout, dq, dk, dv; NULL entries are dense.
+  fa::Strides* dst[8] = {&a.sq, &a.sk, &a.sv, &a.so, &a.sdo, &a.sdq, &a.sdk, &a.sdv};
+  for (int t = 0; t < 8; ++t) {
+    const int st = strides_or_dense(dst[t], strides ? strides[t] : nullptr, H, N, d);
+    if (st != FA_OK) return st;
+  }
   const bool al = (!(use & kUseQKV) || (aligned(q, 16) && aligned(k, 16) && aligned(v, 16))) &&
                   (!(use & kUseO) || aligned(o, 16)) && (!(use & kUseDout) || aligned(dout, 16)) &&
                   (!(use & kUseLse) || aligned(lse, 4)) && (!(use & kUseDq) || aligned(dq, 16)) &&
@@ -382,6 +432,22 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
                            dk, dv, workspace, ws_bytes, B, H, N, d, causal, scale);
   if (st < 0) return FA_OK;
   if (st != FA_OK) return st;
+  return status_of(fa::launch_bwd_bf16(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd_strided(const void* q, const int64_t* q_strides, const void* k, const int64_t* k_strides, const void* v,
+                   const int64_t* v_strides, const void* o, const int64_t* o_strides, const void* dout,
+                   const int64_t* dout_strides, const float* lse, void* dq, const int64_t* dq_strides, void* dk,
+                   const int64_t* dk_strides, void* dv, const int64_t* dv_strides, void* workspace, size_t ws_bytes,
+                   int B, int H, int N, int d, int causal, float scale, int deterministic, fa_stream_t stream) {
+  if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
+  const int64_t* st8[8] = {q_strides, k_strides, v_strides, o_strides, dout_strides, dq_strides, dk_strides, dv_strides};
+  fa::BwdArgs a;
+  const int st = bwd_setup(a, kUseQKV | kUseO | kUseDout | kUseLse | kUseDq | kUseDkDv, q, k, v, o, dout, lse, dq,
+                           dk, dv, workspace, ws_bytes, B, H, N, d, causal, scale, st8);
+  if (st < 0) return FA_OK;
+  if (st != FA_OK) return st;
+  a.deterministic = deterministic;
   return status_of(fa::launch_bwd_bf16(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -491,6 +557,7 @@ int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* lse, int 
   if (st != FA_OK) return st;
   fa::FwdArgs a{};
   a.o = o;
+  a.so = fa::dense_strides(H, N, d);
   a.lse = lse;
   a.B = B;
   a.H = H;

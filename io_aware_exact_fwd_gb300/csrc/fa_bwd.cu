@@ -127,6 +127,11 @@ __device__ __forceinline__ int det_shift(float dq_block_max, float vmax, float k
 }
 __device__ __forceinline__ float pow2f(int s) { return __int_as_float((s + 127) << 23); }  // -126 <= s <= 127
 
+// Element offset of row n of head (b, h) in a strided [B, H, N, d] tensor.
+__device__ __forceinline__ size_t row_offset(const Strides& st, long long bh, int H, int n) {
+  return static_cast<size_t>((bh / H) * st.s[2] + (bh % H) * st.s[1] + static_cast<long long>(n) * st.s[0]);
+}
+
 // Stage the 128 x 128 fp32 accumulator row of this thread as bf16 into a
 // 128-byte-swizzled [128 rows][64 cols] x 2 TMA box pair.
 __device__ __forceinline__ void stage_row_bf16(uint32_t taddr_row, uint8_t* boxes, int row, float mul) {
@@ -155,8 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                     const float* __restrict__ lse2, const float* __restrict__ dvec, float* __restrict__ dq_acc,
-                    const float* __restrict__ dq_bmax, const float* __restrict__ kv_max, int N, int Npad, int BH,
-                    int nkb, float scale, float scale_log2, unsigned int* err_word, unsigned long long wait_ns) {
+                    const float* __restrict__ dq_bmax, const float* __restrict__ kv_max, int N, int Npad, int H,
+                    int BH, int nkb, float scale, float scale_log2, unsigned int* err_word, unsigned long long wait_ns) {
   using C = BwdCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -190,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     kb = static_cast<int>(blockIdx.x) % nkb;
     bh = static_cast<int>(blockIdx.x) / nkb;
   }
+  const int h_idx = bh % H, b_idx = bh / H;  // head and batch of the TMA coordinates
   const int nqb = (N + kBqB - 1) / kBqB;
   const int i0 = CAUSAL ? (kb * kBkB) / kBqB : 0;
   const int n = nqb - i0;  // >= 1: query row kb*128 < N exists
@@ -229,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(bar_kv, 2 * C::kKVTile);
       for (int b = 0; b < 2; ++b) {
-        tma_load_3d(sK + b * C::kKVBox, &tm_k, bar_kv, b * 64, kb * kBkB, bh);
-        tma_load_3d(sV + b * C::kKVBox, &tm_v, bar_kv, b * 64, kb * kBkB, bh);
+        tma_load_4d(sK + b * C::kKVBox, &tm_k, bar_kv, b * 64, kb * kBkB, h_idx, b_idx);
+        tma_load_4d(sV + b * C::kKVBox, &tm_v, bar_kv, b * 64, kb * kBkB, h_idx, b_idx);
       }
       int issued = 0;
       for (int it = 0; it < n; ++it) {
@@ -240,8 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = sRing + slot * C::kStageBytes;
         mbar_arrive_expect_tx(&bar_full[slot], C::kStageTx);
         for (int b = 0; b < 2; ++b) {
-          tma_load_3d(st + C::kStageQ + b * C::kQBox, &tm_q, &bar_full[slot], b * 64, i * kBqB, bh);
-          tma_load_3d(st + C::kStageDO + b * C::kQBox, &tm_do, &bar_full[slot], b * 64, i * kBqB, bh);
+          tma_load_4d(st + C::kStageQ + b * C::kQBox, &tm_q, &bar_full[slot], b * 64, i * kBqB, h_idx, b_idx);
+          tma_load_4d(st + C::kStageDO + b * C::kQBox, &tm_do, &bar_full[slot], b * 64, i * kBqB, h_idx, b_idx);
         }
         bulk_load(st + C::kStageL, lse2_h + i * kBqB, kBqB * 4, &bar_full[slot]);
         bulk_load(st + C::kStageD, dvec_h + i * kBqB, kBqB * 4, &bar_full[slot]);
@@ -415,8 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar_epi);
       if (threadIdx.x == 0 && mbar_wait(bar_epi, 0, wc, kSiteBEpi)) {
         for (int bb = 0; bb < 2; ++bb) {
-          tma_store_3d(&tm_dv, sV + bb * C::kKVBox, bb * 64, kb * kBkB, bh);
-          tma_store_3d(&tm_dk, sK + bb * C::kKVBox, bb * 64, kb * kBkB, bh);
+          tma_store_4d(&tm_dv, sV + bb * C::kKVBox, bb * 64, kb * kBkB, h_idx, b_idx);
+          tma_store_4d(&tm_dk, sK + bb * C::kKVBox, bb * 64, kb * kBkB, h_idx, b_idx);
         }
         tma_store_commit_and_wait_read();
       }
@@ -481,7 +487,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
                                                              const float* __restrict__ lse, float* __restrict__ dvec,
                                                              float* __restrict__ lse2, float* __restrict__ dq_acc,
                                                              unsigned int* __restrict__ dq_bmax, int N, int Npad,
-                                                             long long rows_pad) {
+                                                             long long rows_pad, int H, Strides so, Strides sdo) {
   const long long r = static_cast<long long>(blockIdx.x) * 16 + (threadIdx.x >> 4);
   const int t = threadIdx.x & 15;
   // The grid is exactly rows_pad / 16 blocks (Npad is a multiple of 64), so every
@@ -490,9 +496,9 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
   const int nrow = static_cast<int>(r - bh * Npad);
   float acc = 0.f, nrm = 0.f;
   if (nrow < N) {
-    const size_t base = (static_cast<size_t>(bh) * N + nrow) * kD + t * 8;
-    const uint4 ov = *reinterpret_cast<const uint4*>(o + base);
-    const uint4 gv = *reinterpret_cast<const uint4*>(dout + base);
+    const size_t base = (static_cast<size_t>(bh) * N + nrow) * kD + t * 8;  // dense: the dQ accumulator
+    const uint4 ov = *reinterpret_cast<const uint4*>(o + row_offset(so, bh, H, nrow) + t * 8);
+    const uint4 gv = *reinterpret_cast<const uint4*>(dout + row_offset(sdo, bh, H, nrow) + t * 8);
     const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
     const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(&gv);
 #pragma unroll
@@ -542,7 +548,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
 constexpr int kBoundRows = 256;
 __global__ void __launch_bounds__(256) bwd_kv_bound_kernel(const __nv_bfloat16* __restrict__ k,
                                                            const __nv_bfloat16* __restrict__ v,
-                                                           unsigned int* __restrict__ kv_max, int N) {
+                                                           unsigned int* __restrict__ kv_max, int N, int H,
+                                                           Strides sk, Strides sv) {
   const int bh = blockIdx.y;
   const int t = threadIdx.x & 15;
   const int r0 = blockIdx.x * kBoundRows + (threadIdx.x >> 4);
@@ -554,9 +561,8 @@ __global__ void __launch_bounds__(256) bwd_kv_bound_kernel(const __nv_bfloat16* 
     const int r = r0 + pass * 16;
     uint4 kv4 = make_uint4(0, 0, 0, 0), vv4 = make_uint4(0, 0, 0, 0);
     if (r < N) {
-      const size_t base = (static_cast<size_t>(bh) * N + r) * kD + t * 8;
-      kv4 = *reinterpret_cast<const uint4*>(k + base);
-      vv4 = *reinterpret_cast<const uint4*>(v + base);
+      kv4 = *reinterpret_cast<const uint4*>(k + row_offset(sk, bh, H, r) + t * 8);
+      vv4 = *reinterpret_cast<const uint4*>(v + row_offset(sv, bh, H, r) + t * 8);
     }
     const __nv_bfloat162* kp = reinterpret_cast<const __nv_bfloat162*>(&kv4);
     const __nv_bfloat162* vp = reinterpret_cast<const __nv_bfloat162*>(&vv4);
@@ -599,15 +605,16 @@ template <bool DET>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ dq_acc,
                                                              __nv_bfloat16* __restrict__ dq, float scale,
                                                              long long n8, const float* __restrict__ dq_bmax,
-                                                             const float* __restrict__ kv_max, int N, int Npad) {
+                                                             const float* __restrict__ kv_max, int N, int Npad, int H,
+                                                             Strides sdq) {
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= n8) return;
   float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * idx];
   float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * idx + 1];
+  const long long row = idx * 8 / kD;  // (bh, query row) flattened
+  const long long bh = row / N;
+  const int qrow = static_cast<int>(row - bh * N);
   if (DET) {
-    const long long row = idx * 8 / kD;  // (bh, query row) flattened
-    const long long bh = row / N;
-    const int qrow = static_cast<int>(row - bh * N);
     const float inv = pow2f(-det_shift(dq_bmax[bh * (Npad / kBqB) + qrow / kBqB], kv_max[2 * bh], kv_max[2 * bh + 1]));
     auto cv = [&](float x) { return static_cast<float>(__float_as_int(x)) * inv; };
     a = make_float4(cv(a.x), cv(a.y), cv(a.z), cv(a.w));
@@ -618,7 +625,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
   out.y = pack_bf16x2(a.z * scale, a.w * scale);
   out.z = pack_bf16x2(b.x * scale, b.y * scale);
   out.w = pack_bf16x2(b.z * scale, b.w * scale);
-  reinterpret_cast<uint4*>(dq)[idx] = out;
+  *reinterpret_cast<uint4*>(dq + row_offset(sdq, bh, H, qrow) + (idx * 8) % kD) = out;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -651,14 +658,14 @@ cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream) {
     if (e) return e;
     bwd_kv_bound_kernel<<<dim3(static_cast<unsigned>((a.N + kBoundRows - 1) / kBoundRows), BH), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.v),
-        reinterpret_cast<unsigned int*>(ws + w.off_kvmax), a.N);
+        reinterpret_cast<unsigned int*>(ws + w.off_kvmax), a.N, a.H, a.sk, a.sv);
     if ((e = cudaGetLastError())) return e;
   }
   auto kern = a.deterministic ? bwd_preprocess_kernel<true> : bwd_preprocess_kernel<false>;
   kern<<<static_cast<unsigned>((rows_pad + 15) / 16), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
       reinterpret_cast<float*>(ws + w.off_d), reinterpret_cast<float*>(ws + w.off_lse2),
-      reinterpret_cast<float*>(ws + w.off_dq), dq_bmax, a.N, w.npad, rows_pad);
+      reinterpret_cast<float*>(ws + w.off_dq), dq_bmax, a.N, w.npad, rows_pad, a.H, a.so, a.sdo);
   return cudaGetLastError();
 }
 
@@ -669,12 +676,13 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   cudaError_t e;
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if ((e = make_tmap_3d(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBqB))) return e;
-  if ((e = make_tmap_3d(&tdo, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBqB))) return e;
-  if ((e = make_tmap_3d(&tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBkB))) return e;
-  if ((e = make_tmap_3d(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBkB))) return e;
-  if ((e = make_tmap_3d(&tdk, a.dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBkB))) return e;
-  if ((e = make_tmap_3d(&tdv, a.dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, BH, 64, kBkB))) return e;
+  constexpr auto kBf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if ((e = make_tmap_4d(&tq, a.q, kBf16, 2, kD, a.N, a.H, a.B, a.sq.s, 64, kBqB))) return e;
+  if ((e = make_tmap_4d(&tdo, a.dout, kBf16, 2, kD, a.N, a.H, a.B, a.sdo.s, 64, kBqB))) return e;
+  if ((e = make_tmap_4d(&tk, a.k, kBf16, 2, kD, a.N, a.H, a.B, a.sk.s, 64, kBkB))) return e;
+  if ((e = make_tmap_4d(&tv, a.v, kBf16, 2, kD, a.N, a.H, a.B, a.sv.s, 64, kBkB))) return e;
+  if ((e = make_tmap_4d(&tdk, a.dk, kBf16, 2, kD, a.N, a.H, a.B, a.sdk.s, 64, kBkB))) return e;
+  if ((e = make_tmap_4d(&tdv, a.dv, kBf16, 2, kD, a.N, a.H, a.B, a.sdv.s, 64, kBkB))) return e;
   auto kern = a.deterministic ? (a.causal ? bwd_main_kernel<true, true> : bwd_main_kernel<false, true>)
                               : (a.causal ? bwd_main_kernel<true, false> : bwd_main_kernel<false, false>);
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes))) return e;
@@ -687,7 +695,7 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
       tq, tk, tv, tdo, tdk, tdv, reinterpret_cast<const float*>(ws + w.off_lse2),
       reinterpret_cast<const float*>(ws + w.off_d), reinterpret_cast<float*>(ws + w.off_dq),
       reinterpret_cast<const float*>(ws + w.off_dqmax), reinterpret_cast<const float*>(ws + w.off_kvmax), a.N, w.npad,
-      BH, nkb, a.scale, a.scale * kLog2e, a.err_word, a.dbg.wait_limit_ns);
+      a.H, BH, nkb, a.scale, a.scale * kLog2e, a.err_word, a.dbg.wait_limit_ns);
   return cudaGetLastError();
 }
 
@@ -699,7 +707,7 @@ cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream) {
   auto kern = a.deterministic ? bwd_dq_convert_kernel<true> : bwd_dq_convert_kernel<false>;
   kern<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
       dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.scale, n8, reinterpret_cast<const float*>(ws + w.off_dqmax),
-      reinterpret_cast<const float*>(ws + w.off_kvmax), a.N, w.npad);
+      reinterpret_cast<const float*>(ws + w.off_kvmax), a.N, w.npad, a.H, a.sdq);
   return cudaGetLastError();
 }
 

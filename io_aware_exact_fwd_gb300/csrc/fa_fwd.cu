@@ -179,8 +179,8 @@ template <int D, bool CAUSAL, bool FP8, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-               float* __restrict__ lse, int N, int BH, int nunits, float scale_log2, unsigned int* err_word,
-               unsigned long long wait_ns, int fault, Fp8Scales f8, KeySplit ks) {
+               float* __restrict__ lse, int N, int H, int BH, int nunits, float scale_log2,
+               unsigned int* err_word, unsigned long long wait_ns, int fault, Fp8Scales f8, KeySplit ks) {
   static_assert(!(SPLIT && FP8), "the split-KV variant is bf16 only");
   using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
@@ -258,11 +258,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* dst = sRing + slot * C::kTileBytes;
         if (FP8 && tm == &tm_v) {
           // V^T codes [d rows][keys]: one 128-key x d-row box at key offset j * 128.
-          tma_load_3d(dst, tm, &bar_full[slot], j * kBlockK, 0, bh);
+          tma_load_4d(dst, tm, &bar_full[slot], j * kBlockK, 0, bh % H, bh / H);
         } else {
 #pragma unroll
           for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(dst + b * C::kBoxBytes, tm, &bar_full[slot], b * kBoxCols, j * kBlockK, bh);
+            tma_load_4d(dst + b * C::kBoxBytes, tm, &bar_full[slot], b * kBoxCols, j * kBlockK, bh % H, bh / H);
         }
         ++issued;
         return true;
@@ -303,8 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&bar_q[t], C::kTileBytes);
 #pragma unroll
           for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(sQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, &bar_q[t], b * kBoxCols,
-                        u * kRowsPerCta + t * kBlockQ, bh);
+            tma_load_4d(sQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, &bar_q[t], b * kBoxCols,
+                        u * kRowsPerCta + t * kBlockQ, bh % H, bh / H);
           ++nload[t];
         }
       }
@@ -742,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((ok = mbar_wait(&bar_epi[t], ocnt & 1, wc, kSiteEpi))) {
 #pragma unroll
           for (int b = 0; b < C::kOBoxes; ++b)
-            tma_store_3d(&tm_o, sO + b * C::kBoxBytes, b * kBoxCols, qrow0, bh);
+            tma_store_4d(&tm_o, sO + b * C::kBoxBytes, b * kBoxCols, qrow0, bh % H, bh / H);
           tma_store_commit_and_wait_read();
           mbar_arrive(bar_stg);
         }
@@ -763,8 +763,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool CAUSAL, bool FP8, bool SPLIT = false>
 cudaError_t launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-                          float* lse, int N, int BH, float scale_log2, unsigned int* err_word, const DebugKnobs& dbg,
-                          const Fp8Scales& f8, const KeySplit& ks, cudaStream_t stream) {
+                          float* lse, int N, int H, int BH, float scale_log2, unsigned int* err_word,
+                          const DebugKnobs& dbg, const Fp8Scales& f8, const KeySplit& ks, cudaStream_t stream) {
   using C = FwdCfg<D, FP8>;
   cudaError_t e;
   auto kern = fwd_kernel<D, CAUSAL, FP8, SPLIT>;
@@ -783,7 +783,7 @@ cudaError_t launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
   const long long units = static_cast<long long>(nunits) * BH * ks.nsplit;
   dim3 grid(static_cast<unsigned>(min(units, static_cast<long long>(sms))));
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, lse, N, BH, nunits, scale_log2, err_word,
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, lse, N, H, BH, nunits, scale_log2, err_word,
                                                    dbg.wait_limit_ns, dbg.fault, f8, ks);
   return cudaGetLastError();
 }
@@ -796,12 +796,14 @@ cudaError_t launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
   const int BH = a.B * a.H;
   CUtensorMap tq, tk, tv, to;
   cudaError_t e;
-  if ((e = make_tmap_3d(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockQ))) return e;
-  if ((e = make_tmap_3d(&tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockK))) return e;
-  if ((e = make_tmap_3d(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockK))) return e;
-  if ((e = make_tmap_3d(&to, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockQ))) return e;
-  return launch_kernel<D, CAUSAL, false>(tq, tk, tv, to, a.lse, a.N, BH, a.scale * 1.4426950408889634f, a.err_word,
-                                         a.dbg, Fp8Scales{nullptr, nullptr, nullptr, 0}, whole_keys(a.N), stream);
+  constexpr auto kBf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if ((e = make_tmap_4d(&tq, a.q, kBf16, 2, D, a.N, a.H, a.B, a.sq.s, kBoxCols, kBlockQ))) return e;
+  if ((e = make_tmap_4d(&tk, a.k, kBf16, 2, D, a.N, a.H, a.B, a.sk.s, kBoxCols, kBlockK))) return e;
+  if ((e = make_tmap_4d(&tv, a.v, kBf16, 2, D, a.N, a.H, a.B, a.sv.s, kBoxCols, kBlockK))) return e;
+  if ((e = make_tmap_4d(&to, a.o, kBf16, 2, D, a.N, a.H, a.B, a.so.s, kBoxCols, kBlockQ))) return e;
+  return launch_kernel<D, CAUSAL, false>(tq, tk, tv, to, a.lse, a.N, a.H, BH, a.scale * 1.4426950408889634f,
+                                         a.err_word, a.dbg, Fp8Scales{nullptr, nullptr, nullptr, 0}, whole_keys(a.N),
+                                         stream);
 }
 
 template <int D, bool CAUSAL>
@@ -809,12 +811,14 @@ cudaError_t launch_splitkv_impl(const SplitKvArgs& a, cudaStream_t stream) {
   const int BH = a.B * a.H;
   CUtensorMap tq, tk, tv;
   cudaError_t e;
-  if ((e = make_tmap_3d(&tq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.Nq, BH, kBoxCols, kBlockQ))) return e;
-  if ((e = make_tmap_3d(&tk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.Nk, BH, kBoxCols, kBlockK))) return e;
-  if ((e = make_tmap_3d(&tv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.Nk, BH, kBoxCols, kBlockK))) return e;
+  constexpr auto kBf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const Strides sq = dense_strides(a.H, a.Nq, D), skv = dense_strides(a.H, a.Nk, D);
+  if ((e = make_tmap_4d(&tq, a.q, kBf16, 2, D, a.Nq, a.H, a.B, sq.s, kBoxCols, kBlockQ))) return e;
+  if ((e = make_tmap_4d(&tk, a.k, kBf16, 2, D, a.Nk, a.H, a.B, skv.s, kBoxCols, kBlockK))) return e;
+  if ((e = make_tmap_4d(&tv, a.v, kBf16, 2, D, a.Nk, a.H, a.B, skv.s, kBoxCols, kBlockK))) return e;
   const KeySplit ks{a.Nk, a.n_split, splitkv_kbps(a.Nk, a.n_split), a.Nk - a.Nq, a.o_part, a.lse_part};
   // The partial epilogue stores fp32 rows itself; the O tensor map is never used.
-  return launch_kernel<D, CAUSAL, false, true>(tq, tk, tv, tq, nullptr, a.Nq, BH, a.scale * 1.4426950408889634f,
+  return launch_kernel<D, CAUSAL, false, true>(tq, tk, tv, tq, nullptr, a.Nq, a.H, BH, a.scale * 1.4426950408889634f,
                                                a.err_word, a.dbg, Fp8Scales{nullptr, nullptr, nullptr, 0}, ks, stream);
 }
 
@@ -826,16 +830,18 @@ cudaError_t launch_fwd_fp8_impl(const FwdArgs& a, const void* workspace, cudaStr
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   CUtensorMap tq, tk, tv, to;
   cudaError_t e;
-  if ((e = make_tmap_3d(&tq, ws + lay.off_q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D, a.N, BH, 128, kBlockQ))) return e;
-  if ((e = make_tmap_3d(&tk, ws + lay.off_k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D, a.N, BH, 128, kBlockK))) return e;
-  if ((e = make_tmap_3d(&tv, ws + lay.off_v8t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, lay.npad, D, BH, kBlockK, D)))
+  constexpr auto kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const Strides s8 = dense_strides(a.H, a.N, D), svt = dense_strides(a.H, D, lay.npad);
+  if ((e = make_tmap_4d(&tq, ws + lay.off_q8, kU8, 1, D, a.N, a.H, a.B, s8.s, 128, kBlockQ))) return e;
+  if ((e = make_tmap_4d(&tk, ws + lay.off_k8, kU8, 1, D, a.N, a.H, a.B, s8.s, 128, kBlockK))) return e;
+  if ((e = make_tmap_4d(&tv, ws + lay.off_v8t, kU8, 1, lay.npad, D, a.H, a.B, svt.s, kBlockK, D))) return e;
+  if ((e = make_tmap_4d(&to, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.H, a.B, a.so.s, kBoxCols, kBlockQ)))
     return e;
-  if ((e = make_tmap_3d(&to, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, BH, kBoxCols, kBlockQ))) return e;
   const Fp8Scales f8{reinterpret_cast<const float*>(ws + lay.off_sq), reinterpret_cast<const float*>(ws + lay.off_sk),
                      reinterpret_cast<const float*>(ws + lay.off_sv), lay.ntiles};
   // Scores of the rotated operands are d times the plain ones: fold 1/d into the scale.
   const float scale_log2 = a.scale * 1.4426950408889634f / static_cast<float>(D);
-  return launch_kernel<D, CAUSAL, true>(tq, tk, tv, to, a.lse, a.N, BH, scale_log2, a.err_word, a.dbg, f8,
+  return launch_kernel<D, CAUSAL, true>(tq, tk, tv, to, a.lse, a.N, a.H, BH, scale_log2, a.err_word, a.dbg, f8,
                                         whole_keys(a.N), stream);
 }
 

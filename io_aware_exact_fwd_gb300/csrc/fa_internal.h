@@ -22,12 +22,22 @@ struct DebugKnobs {
   int fault;                // test-only fault injection (0 = none)
 };
 
+// Element strides {row, head, batch} of a [B, H, N, d]-indexed tensor whose d is
+// contiguous.  The dense [B, H, N, d] layout is {d, N d, H N d}.
+struct Strides {
+  int64_t s[3];
+};
+inline Strides dense_strides(int H, int N, int d) {
+  return Strides{{static_cast<int64_t>(d), static_cast<int64_t>(N) * d, static_cast<int64_t>(H) * N * d}};
+}
+
 struct FwdArgs {
   const void* q;
   const void* k;
   const void* v;
   void* o;
   float* lse;
+  Strides sq, sk, sv, so;
   int B, H, N, d;
   int causal;
   float scale;
@@ -79,6 +89,7 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
+  Strides sq, sk, sv, so, sdo, sdq, sdk, sdv;
   void* workspace;
   int B, H, N, d;
   int causal;
@@ -135,6 +146,8 @@ cudaError_t launch_fp8_prepare(const Fp8PrepArgs& a, cudaStream_t stream);
 // Encodes a 3-D tiled tensor map over a [BH, N, cols] row-major tensor with
 // `elem_bytes`-byte elements, box {box_cols, box_rows, 1}, 128-byte swizzle.
 // Implemented in fa_api.cu (driver entry point resolved once).
+cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int cols,
+                         int rows, int heads, int batch, const int64_t strides[3], int box_cols, int box_rows);
 cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
                          int cols, int rows, int depth, int box_cols, int box_rows);
 

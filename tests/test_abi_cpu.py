@@ -118,3 +118,17 @@ def test_splitkv_validation_statuses(lib):
     assert lib.fa_fwd_splitkv(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), need - 1, 2, 3, 5, 900, 64,
                               7, 0, 0.125, vp(0)) == 6
     assert lib.fa_splitkv_workspace_size(1, 1, 1, 96, 1) == 0
+
+
+def test_strided_validation_statuses(lib):
+    vp = ctypes.c_void_p
+    good = (ctypes.c_int64 * 3)(128, 128 * 64, 128 * 64 * 2)
+    odd = (ctypes.c_int64 * 3)(132, 132 * 64, 132 * 64 * 2)
+    short = (ctypes.c_int64 * 3)(64, 128 * 64, 128 * 64 * 2)
+    def fwd(qs):
+        return lib.fa_fwd_strided(vp(FAKE), ctypes.cast(qs, vp) if qs is not None else None, vp(FAKE), None,
+                                  vp(FAKE), None, vp(FAKE), None, vp(FAKE), 2, 2, 64, 128, 0, 0.1, vp(0))
+    assert fwd(odd) == 3      # row stride of 132 elements is not 16-byte aligned
+    assert fwd(short) == 1    # rows of one head would overlap
+    neg = (ctypes.c_int64 * 3)(128, -1, 1)
+    assert fwd(neg) == 1
