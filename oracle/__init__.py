@@ -19,6 +19,10 @@ check it against the pages by eye:
   "FlashAttention-Skalierung, Multi-GPU-Training und Gewichtsquantisierung",
   section 3 (token-by-token inference is bandwidth-bound); the merge itself is
   the softmax definition split over key ranges.
+* ``w4a16``      -- the 4-bit-weight GEMM of "FlashAttention-Skalierung, Multi-GPU-Training
+  und Gewichtsquantisierung", section 3 (W4A16): unpack eight 4-bit codes per
+  32-bit word, dequantise with per-group scale and zero point to fp16, multiply
+  with fp16 activations.
 * ``fp8``        -- the FP8 input preparation: random-sign Walsh-Hadamard rotation
   of Q and K (incoherent processing) and per-tile block quantisation to OCP e4m3.
   Source: "FlashAttention-Skalierung, Multi-GPU-Training und
@@ -49,6 +53,7 @@ from .splitkv import (
     attention_general,
     splitkv_flops,
 )
+from .w4a16 import w4a16_unpack, w4a16_dequant, w4a16_gemm, w4a16_abs_sum
 from .fp8 import (
     sylvester_hadamard,
     fwht_f32,
@@ -73,6 +78,10 @@ __all__ = [
     "merge_partials",
     "attention_general",
     "splitkv_flops",
+    "w4a16_unpack",
+    "w4a16_dequant",
+    "w4a16_gemm",
+    "w4a16_abs_sum",
     "sylvester_hadamard",
     "fwht_f32",
     "e4m3_encode",

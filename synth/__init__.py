@@ -52,3 +52,20 @@ def rotation_signs(d: int, seed: int) -> torch.Tensor:
     g = torch.Generator().manual_seed(seed * 7919 + 17)
     bits = torch.randint(0, 2, (d,), generator=g)
     return (bits * 2 - 1).to(torch.int8)
+
+
+def w4a16_inputs(M: int, N: int, K: int, seed: int, group: int = 128):
+    """Seeded inputs of the 4-bit-weight GEMM: activations and random packed weights.
+
+    x: fp16 [M, K] ~ N(0, 1).  wq: int32 [N, K / 8] of uniformly random bits (so
+    every 4-bit code is uniform on 0..15; how the bits map to codes is the
+    kernel's interface, not this module's).  scales: fp16 [K / group, N], uniform
+    on [0.005, 0.02].  zeros: uint8 [K / group, N], uniform integers 0..15.
+    CPU tensors.
+    """
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((M, K), generator=g, dtype=torch.float32).to(torch.float16)
+    wq = torch.randint(-(2 ** 31), 2 ** 31, (N, K // 8), generator=g, dtype=torch.int64).to(torch.int32)
+    scales = (0.005 + 0.015 * torch.rand((K // group, N), generator=g)).to(torch.float16)
+    zeros = torch.randint(0, 16, (K // group, N), generator=g, dtype=torch.int64).to(torch.uint8)
+    return {"x": x, "wq": wq, "scales": scales, "zeros": zeros}
