@@ -331,6 +331,36 @@ FA_API int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, 
                           fa_stream_t stream);
 
 /*
+ * W4A16: 4-bit weights times 16-bit activations, dequantised on the fly
+ * ("FlashAttention-Skalierung, Multi-GPU-Training und Gewichtsquantisierung",
+ * section 3, "Wie spezielle CUDA-Kernels während der Ausführung dequantisieren
+ * (W4A16)": packed 4-bit weights are read from memory, unpacked in registers with
+ * shifts and masks, given their scale and zero point, and fed as fp16 with the
+ * fp16 activations to the tensor cores, never written back unpacked).
+ *
+ *   Y[m, n] = sum_k X[m, k] * W[n, k],   W[n, k] = fp16((q[n, k] - z[g, n]) * s[g, n]),  g = k / 128
+ *
+ *   x      : const fp16 [M, K] (row-major)          y : fp16 [M, N] (output)
+ *   wq     : const uint32 [N, K / 8]: word w of row n holds k = 8w .. 8w+7; the code
+ *            of k = 8w + 2i is bits 4i..4i+3, that of k = 8w + 2i + 1 bits
+ *            4i+16..4i+19 (i = 0..3), so one shift and one mask give a pair
+ *   scales : const fp16 [K / 128, N]     zeros : const uint8 [K / 128, N] (0..15)
+ * Limits: 1 <= M <= 128 (decode-sized batches; the product is then bound by
+ * reading the weights), N a multiple of 16, K a multiple of 256.  n_split cuts K
+ * into ranges computed in parallel whose fp32 partials are summed in a fixed order
+ * (the same bits on every run); n_split <= 0 selects fa_w4a16_default_splits.
+ * Numerics: each weight is the fp16 rounding of (q - z) s; products accumulate in
+ * fp32 on the tensor cores; Y is rounded to fp16 once.
+ * Errors: FA_ERR_UNSUPPORTED for sizes outside the limits, FA_ERR_WORKSPACE when
+ * a split needs fa_w4a16_workspace_size(...) bytes of workspace (256-byte
+ * aligned) that were not given, FA_ERR_MISALIGNED for a tensor not 16-byte aligned.
+ */
+FA_API size_t fa_w4a16_workspace_size(int M, int N, int K, int n_split);
+FA_API int fa_w4a16_default_splits(int M, int N, int K);
+FA_API int fa_w4a16_gemm(const void* x, const void* wq, const void* scales, const void* zeros, void* y,
+                         void* workspace, size_t ws_bytes, int M, int N, int K, int n_split, fa_stream_t stream);
+
+/*
  * fa_sync_check -- synchronise `stream`, then report device-detected errors.
  * Returns FA_ERR_CUDA if the stream or a prior launch failed, FA_ERR_TIMEOUT
  * if any kernel of this library on the current device expired a bounded wait

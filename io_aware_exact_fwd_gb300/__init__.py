@@ -101,6 +101,12 @@ def load_library():
     lib.fa_merge_partials.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
     lib.fa_fwd_splitkv.restype = i
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, i, i, f, vp]
+    lib.fa_w4a16_workspace_size.restype = ctypes.c_size_t
+    lib.fa_w4a16_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_w4a16_default_splits.restype = i
+    lib.fa_w4a16_default_splits.argtypes = [i, i, i]
+    lib.fa_w4a16_gemm.restype = i
+    lib.fa_w4a16_gemm.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, vp]
     lib.fa_sync_check.restype = i
     lib.fa_sync_check.argtypes = [vp]
     lib.fa_last_error_site.restype = ctypes.c_uint
@@ -470,6 +476,43 @@ def fa_fwd_splitkv(q, k, v, o=None, lse=None, workspace=None, n_split: int = 0, 
                                 B, H, Nq, Nk, d, n, int(bool(causal)), sc, _stream_handle(stream))
     _check(st, "fa_fwd_splitkv")
     return o, lse
+
+
+def fa_w4a16_workspace_size(M: int, N: int, K: int, n_split: int) -> int:
+    return int(load_library().fa_w4a16_workspace_size(M, N, K, n_split))
+
+
+def fa_w4a16_default_splits(M: int, N: int, K: int) -> int:
+    return int(load_library().fa_w4a16_default_splits(M, N, K))
+
+
+def fa_w4a16_gemm(x, wq, scales, zeros, y=None, workspace=None, n_split: int = 0, stream=None):
+    """Y = X W^T with W given as packed 4-bit codes (see fa_w4a16_gemm in include/fa.h).
+
+    x: fp16 [M, K]; wq: int32 [N, K/8]; scales: fp16 [K/128, N]; zeros: uint8 [K/128, N];
+    all CUDA, contiguous.  Returns y (fp16 [M, N]).
+    """
+    import torch
+
+    lib = load_library()
+    M, K = x.shape
+    N = wq.shape[0]
+    for name, t, shape, dt in (("x", x, (M, K), torch.float16), ("wq", wq, (N, K // 8), torch.int32),
+                               ("scales", scales, (K // 128, N), torch.float16),
+                               ("zeros", zeros, (K // 128, N), torch.uint8)):
+        if t.dtype != dt or tuple(t.shape) != shape or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor of shape {shape}")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    n = n_split if n_split > 0 else max(1, int(lib.fa_w4a16_default_splits(M, N, K)))
+    need = int(lib.fa_w4a16_workspace_size(M, N, K, n))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        st = lib.fa_w4a16_gemm(_ptr(x), _ptr(wq), _ptr(scales), _ptr(zeros), _ptr(y), _ptr(workspace),
+                               0 if workspace is None else _ws_bytes(workspace), M, N, K, n, _stream_handle(stream))
+    _check(st, "fa_w4a16_gemm")
+    return y
 
 
 def fa_sync_check(stream=None):

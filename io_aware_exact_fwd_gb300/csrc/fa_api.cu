@@ -133,6 +133,20 @@ cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int cols,
+                         int rows, int64_t row_stride_elems, int box_cols, int box_rows, bool swizzle128) {
+  if (!g_encode) return cudaErrorInitializationError;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t gstr[1] = {static_cast<cuuint64_t>(row_stride_elems) * elem_bytes};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, gstr, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int cols,
                          int rows, int heads, int batch, const int64_t strides[3], int box_cols, int box_rows) {
   if (!g_encode) return cudaErrorInitializationError;
@@ -353,6 +367,69 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   int st = fa_fwd_splitkv_partial(q, k, v, o_part, lse_part, B, H, Nq, Nk, d, n_split, causal, scale, stream);
   if (st != FA_OK) return st;
   return fa_merge_partials(o_part, lse_part, o, lse, n_split, B, H, Nq, d, stream);
+}
+
+size_t fa_w4a16_workspace_size(int M, int N, int K, int n_split) {
+  if (M < 1 || M > 128 || N < 16 || N % 16 != 0 || K < 256 || K % 256 != 0 || n_split < 1 || n_split > 1024) return 0;
+  const int cps = fa::w4a16_chunks_per_split(K, n_split);
+  const int nsplit = (K / 256 + cps - 1) / cps;
+  return nsplit > 1 ? static_cast<size_t>(nsplit) * M * N * sizeof(float) : 0;
+}
+
+int fa_w4a16_default_splits(int M, int N, int K) {
+  if (M < 1 || M > 128 || N < 16 || N % 16 != 0 || K < 256 || K % 256 != 0) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess || sms < 1)
+    sms = 148;
+  const long long strips = (N + 127) / 128;
+  const int kchunks = K / 256;
+  // Splits of at least 4 chunks (1024 of K); the fewest within 2 % of the best
+  // balance of units over the SMs (the same rule as the split-KV attention).
+  const int n_max = std::max(1, std::min(kchunks / 4, 64));
+  auto cost = [&](int n) {
+    const int cps = (kchunks + n - 1) / n;
+    const int eff = (kchunks + cps - 1) / cps;
+    return static_cast<double>((strips * eff + sms - 1) / sms) * cps;
+  };
+  double best = cost(1);
+  for (int n = 2; n <= n_max; ++n) best = std::min(best, cost(n));
+  for (int n = 1; n <= n_max; ++n)
+    if (cost(n) <= best * 1.02) return n;
+  return 1;
+}
+
+int fa_w4a16_gemm(const void* x, const void* wq, const void* scales, const void* zeros, void* y, void* workspace,
+                  size_t ws_bytes, int M, int N, int K, int n_split, fa_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return FA_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return FA_OK;
+  if (M > 128 || N % 16 != 0 || K < 256 || K % 256 != 0) return FA_ERR_UNSUPPORTED;
+  if (n_split <= 0) n_split = fa_w4a16_default_splits(M, N, K);
+  if (n_split < 1 || n_split > 1024) return FA_ERR_INVALID_ARG;
+  if (!x || !wq || !scales || !zeros || !y) return FA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(scales, 16) || !aligned(zeros, 16) || !aligned(y, 16))
+    return FA_ERR_MISALIGNED;
+  const size_t need = fa_w4a16_workspace_size(M, N, K, n_split);
+  if (need > 0 && (!workspace || ws_bytes < need)) return FA_ERR_WORKSPACE;
+  if (need > 0 && !aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  if (static_cast<long long>(N) * (K / 8) > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  DeviceState* ds = nullptr;
+  const int st = device_state(&ds);
+  if (st != FA_OK) return st;
+  fa::W4a16Args a;
+  a.x = x;
+  a.wq = wq;
+  a.scales = scales;
+  a.zeros = zeros;
+  a.y = y;
+  a.partials = static_cast<float*>(workspace);
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.n_split = n_split;
+  a.err_word = ds->err_word;
+  a.dbg = knobs();
+  return fa::launch_w4a16(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {

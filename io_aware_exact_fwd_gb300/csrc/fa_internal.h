@@ -146,6 +146,28 @@ cudaError_t launch_fp8_prepare(const Fp8PrepArgs& a, cudaStream_t stream);
 // Encodes a 3-D tiled tensor map over a [BH, N, cols] row-major tensor with
 // `elem_bytes`-byte elements, box {box_cols, box_rows, 1}, 128-byte swizzle.
 // Implemented in fa_api.cu (driver entry point resolved once).
+// 2-D map over a row-major matrix (row stride in elements); optional 128-byte swizzle.
+cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int cols,
+                         int rows, int64_t row_stride_elems, int box_cols, int box_rows, bool swizzle128);
+
+// 4-bit-weight GEMM (fa_w4a16.cu): Y [M, N] = X [M, K] (fp16) times the transpose
+// of W [N, K], W given as packed 4-bit codes wq [N, K/8] with fp16 scales and
+// uint8 zero points [K/128, N].  n_split > 1 cuts K into that many ranges whose
+// fp32 partials [n_split, M, N] land in `partials` and are summed in order.
+struct W4a16Args {
+  const void* x;
+  const void* wq;
+  const void* scales;
+  const void* zeros;
+  void* y;
+  float* partials;
+  int M, N, K, n_split;
+  unsigned int* err_word;
+  DebugKnobs dbg;
+};
+int w4a16_chunks_per_split(int K, int n_split);
+cudaError_t launch_w4a16(const W4a16Args& a, cudaStream_t stream);
+
 cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int cols,
                          int rows, int heads, int batch, const int64_t strides[3], int box_cols, int box_rows);
 cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,

@@ -1,0 +1,358 @@
+// 4-bit-weight, 16-bit-activation matrix product (W4A16) for sm_103a.
+//
+// "FlashAttention-Skalierung, Multi-GPU-Training und Gewichtsquantisierung",
+// section 3 ("Wie spezielle CUDA-Kernels während der Ausführung dequantisieren
+// (W4A16)"): the weights stay packed in memory (eight 4-bit codes per 32-bit
+// word), are taken apart in registers with shifts and masks, turned back into
+// fp16 with stored scale and zero-point factors, and fed with the fp16
+// activations to the tensor cores; the unpacked weights never return to memory.
+//
+//   Y[m, n] = sum_k X[m, k] * fp16((q[n, k] - z[k/128, n]) * s[k/128, n])
+//
+// Decode-sized M (<= 128 tokens) makes this a stream over the weights, so the
+// bound is HBM: 0.5 byte per weight plus 3 bytes of scale and zero per 128.
+//
+// GB300 mapping.  A persistent CTA per SM takes work units = (128 output rows,
+// K range).  Per 256-wide K chunk:
+//  * warp 0 loads, by TMA, the packed 128 x 256 weight tile (16 KB), the chunk's
+//    activations X[:, k0:k0+256] (four 64-column boxes, rows past M zero-filled)
+//    and the two groups' scales and zero points into a ring of stages;
+//  * eight dequantising warps (thread = weight row = TMEM lane; warpgroup g takes
+//    group g of the chunk) turn each word into four fp16 pairs -- one shift, one
+//    mask-and-or with 0x6400 (1024 + code as fp16), one subtraction of 1024 + z
+//    (exact), one multiplication by s (the only rounding) -- and store them to
+//    TMEM, two fp16 per column, as the A operand of the MMA;
+//  * one thread issues tcgen05.mma kind::f16 with A from TMEM (128 rows x 16 k)
+//    and B = X from shared memory (K-major, 128-byte swizzle), accumulating
+//    Y^T[128 rows x M] in TMEM; three A buffers let the dequantisation of the
+//    next chunks overlap the MMAs of this one;
+//  * after the unit's last chunk, warpgroup 0 reads Y^T out of TMEM and writes
+//    fp16 Y (one split) or fp32 partials (several), coalesced along n.
+// Every wait is bounded, as in the attention kernels.
+#include <cuda_fp16.h>
+
+#include "fa_device.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kW4Threads = 384;  // 0 TMA, 1 MMA (+TMEM), 2-3 idle, 4-11 dequantisation
+constexpr int kW4Rows = 128;     // output rows per unit (MMA M, TMEM lanes)
+constexpr int kW4Kc = 256;       // K per chunk: two groups of 128
+constexpr uint32_t kW4TmemCols = 512;
+
+enum : uint32_t {
+  kSiteW4Load = 0x401,
+  kSiteW4Mma = 0x402,
+  kSiteW4Deq = 0x403,
+  kSiteW4Epi = 0x404,
+};
+
+template <int MP>  // tokens padded to 16 or a multiple of 32 (the MMA's N)
+struct W4Cfg {
+  static constexpr int kWBytes = kW4Rows * 128;              // 128 rows x 32 words
+  static constexpr int kXBox = MP * 128;                      // MP rows x 64 fp16
+  static constexpr int kXBytes = 4 * kXBox;
+  static constexpr int kSBytes = 2 * kW4Rows * 2;             // two groups x 128 fp16
+  static constexpr int kZBytes = 2 * kW4Rows;                 // two groups x 128 uint8
+  static constexpr int kOffX = kWBytes;
+  static constexpr int kOffS = kOffX + kXBytes;
+  static constexpr int kOffZ = kOffS + kSBytes;
+  static constexpr int kStageTx = kOffZ + kZBytes;
+  static constexpr int kStageBytes = (kStageTx + 1023) / 1024 * 1024;
+  // As many stages as fit next to the barriers (more bytes in flight per SM).
+  static constexpr int kStages = (220 * 1024 / kStageBytes) < 8 ? (220 * 1024 / kStageBytes) : 8;
+  static constexpr int kBarOff = kStages * kStageBytes;
+  // full[S], empty[S], afull[kA], aempty[kA], dfull, dempty, drain
+  static constexpr int kA = 3;  // A buffers in TMEM (128 columns each)
+  static constexpr int kNumBars = 2 * kStages + 2 * kA + 1 + 1 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  static constexpr uint32_t kColA = 0, kColD = 384;  // A buffers at 0, 128, 256; D (MP <= 128 columns) at 384
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ bool w4_warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc, uint32_t site) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc, site));
+}
+
+template <int MP>
+__global__ void __launch_bounds__(kW4Threads, 1)
+    w4a16_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                 const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_z,
+                 __half* __restrict__ y, float* __restrict__ partials, int M, int N, int nstrips, int nsplit,
+                 int kchunks, int cps, unsigned int* err_word, unsigned long long wait_ns) {
+  using C = W4Cfg<MP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* bar_full = bars;
+  uint64_t* bar_empty = bar_full + C::kStages;
+  uint64_t* bar_afull = bar_empty + C::kStages;  // [kA] A buffer written
+  uint64_t* bar_aempty = bar_afull + C::kA;      // [kA] A buffer consumed by the MMAs
+  uint64_t* bar_dfull = bar_aempty + C::kA;      // unit's Y^T complete in TMEM
+  uint64_t* bar_dempty = bar_dfull + 1;          // Y^T read out
+  uint64_t* bar_drain = bar_dempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int total = nstrips * nsplit;
+  const int G = static_cast<int>(gridDim.x);
+  // Unit w = strip + nstrips * split; CTA c takes w = c, c + G, ...
+  auto unit_range = [&](int w, int& strip, int& c0, int& c1) {
+    strip = w % nstrips;
+    const int sp = w / nstrips;
+    c0 = min(sp * cps, kchunks);
+    c1 = min(c0 + cps, kchunks);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 8 + 1);  // eight dequantising warps + the MMA commit
+    }
+    for (int b = 0; b < C::kA; ++b) {
+      mbar_init(&bar_afull[b], 8);
+      mbar_init(&bar_aempty[b], 1);
+    }
+    mbar_init(bar_dfull, 1);
+    mbar_init(bar_dempty, 4);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kW4TmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, err_word, wait_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int item = 0;
+      bool ok = true;
+      for (int w = static_cast<int>(blockIdx.x); ok && w < total; w += G) {
+        int strip, c0, c1;
+        unit_range(w, strip, c0, c1);
+        for (int c = c0; ok && c < c1; ++c, ++item) {
+          const int slot = item % C::kStages;
+          if (!(ok = mbar_wait(&bar_empty[slot], ((item / C::kStages) & 1) ^ 1, wc, kSiteW4Load))) break;
+          uint8_t* st = smem + slot * C::kStageBytes;
+          mbar_arrive_expect_tx(&bar_full[slot], C::kStageTx);
+          tma_load_2d(st, &tm_w, &bar_full[slot], c * (kW4Kc / 8), strip * kW4Rows);
+#pragma unroll
+          for (int bx = 0; bx < 4; ++bx)
+            tma_load_2d(st + C::kOffX + bx * C::kXBox, &tm_x, &bar_full[slot], c * kW4Kc + bx * 64, 0);
+          tma_load_2d(st + C::kOffS, &tm_s, &bar_full[slot], strip * kW4Rows, 2 * c);
+          tma_load_2d(st + C::kOffZ, &tm_z, &bar_full[slot], strip * kW4Rows, 2 * c);
+        }
+      }
+      if (!ok) {  // let the copies already issued land before the CTA exits
+        for (int t = max(0, item - C::kStages); t < item; ++t)
+          mbar_wait_drain(&bar_full[t % C::kStages], (t / C::kStages) & 1, wait_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(kW4Rows, MP, 0, 0);  // rows x tokens, K-major B
+      const uint64_t xdesc = sdesc_sw128(smem_u32(smem + C::kOffX), 16, 1024);
+      int item = 0, units = 0;
+      bool ok = true;
+      for (int w = static_cast<int>(blockIdx.x); ok && w < total; w += G) {
+        int strip, c0, c1;
+        unit_range(w, strip, c0, c1);
+        if (c1 <= c0) continue;
+        for (int c = c0; ok && c < c1; ++c, ++item) {
+          const int slot = item % C::kStages;
+          const int b = item % C::kA;
+          if (!(ok = mbar_wait(&bar_full[slot], (item / C::kStages) & 1, wc, kSiteW4Mma))) break;
+          if (!(ok = mbar_wait(&bar_afull[b], (item / C::kA) & 1, wc, kSiteW4Mma))) break;
+          // The unit's first MMA overwrites Y^T: the previous unit's must be read out.
+          if (c == c0 && units > 0 && !(ok = mbar_wait(bar_dempty, (units - 1) & 1, wc, kSiteW4Mma))) break;
+          tc_fence_after();
+          const uint32_t st = slot * C::kStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < kW4Kc / 16; ++kk)  // kind::f16; the descriptor selects fp16 operands
+            mma_bf16_ts(tmem + C::kColD, tmem + C::kColA + 128u * b + 8u * kk,
+                        sdesc_add(xdesc, st + (kk / 4) * C::kXBox + (kk % 4) * 32), idesc,
+                        (c > c0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bar_aempty[b]);
+          mma_commit(&bar_empty[slot]);
+        }
+        if (!ok) break;
+        mma_commit(bar_dfull);
+        ++units;
+      }
+      mma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0, wait_ns);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------ dequantisation (thread = weight row)
+    const int g = (warp - 4) >> 2;           // group of the chunk this warpgroup unpacks
+    const int r = ((warp & 3) << 5) + lane;  // row within the 128-row tile
+    const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    int item = 0, units = 0;
+    bool ok = true;
+    for (int w = static_cast<int>(blockIdx.x); ok && w < total; w += G) {
+      int strip, c0, c1;
+      unit_range(w, strip, c0, c1);
+      if (c1 <= c0) continue;
+      for (int c = c0; ok && c < c1; ++c, ++item) {
+        const int slot = item % C::kStages;
+        const int b = item % C::kA;
+        if (!(ok = w4_warp_wait(&bar_full[slot], (item / C::kStages) & 1, wc, kSiteW4Deq))) break;
+        if (item >= C::kA && !(ok = w4_warp_wait(&bar_aempty[b], ((item - C::kA) / C::kA) & 1, wc, kSiteW4Deq)))
+          break;
+        tc_fence_after();
+        const uint8_t* st = smem + slot * C::kStageBytes;
+        const __half s = reinterpret_cast<const __half*>(st + C::kOffS)[g * kW4Rows + r];
+        const int z = st[C::kOffZ + g * kW4Rows + r];
+        const __half2 s2 = __halves2half2(s, s);
+        const __half zb = __int2half_rn(1024 + z);  // exact: an integer below 2048
+        const __half2 zb2 = __halves2half2(zb, zb);
+        // This warpgroup's 16 words of the row: 16-byte chunks 4g .. 4g+3 of the
+        // 128-byte swizzled row.
+        const uint8_t* wrow = st + r * 128;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t out[32];
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            const int chunk = 4 * g + 2 * half + ch;
+            const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((chunk ^ (r & 7)) * 16));
+            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                // Codes of k = 8w + 2i (bits 4i..) and 8w + 2i + 1 (bits 4i + 16..) as
+                // fp16 1024 + code, then (code - z) exactly, then times s.
+                const uint32_t t = ((wd[e] >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+                const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&t), zb2);
+                const __half2 wv = __hmul2(d, s2);
+                out[(ch * 4 + e) * 4 + i] = *reinterpret_cast<const uint32_t*>(&wv);
+              }
+            }
+          }
+          tmem_st32(trow + C::kColA + 128u * b + 64u * g + 32u * half, out);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bar_afull[b]);
+          mbar_arrive(&bar_empty[slot]);
+        }
+      }
+      if (!ok) break;
+      if (g == 0) {
+        // ------------------------------------------------- epilogue (warpgroup 0)
+        if (!(ok = w4_warp_wait(bar_dfull, units & 1, wc, kSiteW4Epi))) break;
+        tc_fence_after();
+        const int n = strip * kW4Rows + r;
+        const int sp = w / nstrips;
+#pragma unroll 1
+        for (int mc = 0; mc < (MP + 31) / 32; ++mc) {  // MP = 16 reads 16 unused columns too
+          uint32_t v[32];
+          tmem_ld32(trow + C::kColD + 32u * mc, v);
+          tmem_ld_wait32(v);
+          if (n < N) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int m = mc * 32 + j;
+              if (m < M) {
+                if (nsplit == 1)
+                  y[static_cast<size_t>(m) * N + n] = __float2half_rn(__uint_as_float(v[j]));
+                else
+                  partials[(static_cast<size_t>(sp) * M + m) * N + n] = __uint_as_float(v[j]);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_dempty);
+      }
+      ++units;
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kW4TmemCols);
+  }
+}
+
+// Y = fp16(sum_s partials[s]), in split order (the same bits on every run).
+__global__ void __launch_bounds__(256) w4a16_reduce_kernel(const float* __restrict__ partials,
+                                                           __half* __restrict__ y, int nsplit, long long mn) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= mn) return;
+  float acc = 0.f;
+  for (int s = 0; s < nsplit; ++s) acc += partials[static_cast<size_t>(s) * mn + i];
+  y[i] = __float2half_rn(acc);
+}
+
+template <int MP>
+cudaError_t launch_mp(const W4a16Args& a, cudaStream_t stream) {
+  using C = W4Cfg<MP>;
+  cudaError_t e;
+  CUtensorMap tw, tx, ts, tz;
+  if ((e = make_tmap_2d(&tw, a.wq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, a.K / 8, a.N, a.K / 8, kW4Kc / 8, kW4Rows,
+                        true)))
+    return e;
+  if ((e = make_tmap_2d(&tx, a.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.K, a.M, a.K, 64, MP, true))) return e;
+  if ((e = make_tmap_2d(&ts, a.scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.N, a.K / 128, a.N, kW4Rows, 2, false)))
+    return e;
+  if ((e = make_tmap_2d(&tz, a.zeros, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.N, a.K / 128, a.N, kW4Rows, 2, false)))
+    return e;
+  auto kern = w4a16_kernel<MP>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes))) return e;
+  const int kchunks = a.K / kW4Kc;
+  const int cps = w4a16_chunks_per_split(a.K, a.n_split);
+  const int nsplit = (kchunks + cps - 1) / cps;  // no empty split
+  const int nstrips = (a.N + kW4Rows - 1) / kW4Rows;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev))) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+  const int units = nstrips * nsplit;
+  kern<<<static_cast<unsigned>(units < sms ? units : sms), kW4Threads, C::kSmemBytes, stream>>>(
+      tw, tx, ts, tz, static_cast<__half*>(a.y), a.partials, a.M, a.N, nstrips, nsplit, kchunks, cps, a.err_word,
+      a.dbg.wait_limit_ns);
+  if ((e = cudaGetLastError())) return e;
+  if (nsplit > 1) {
+    const long long mn = static_cast<long long>(a.M) * a.N;
+    w4a16_reduce_kernel<<<static_cast<unsigned>((mn + 255) / 256), 256, 0, stream>>>(
+        a.partials, static_cast<__half*>(a.y), nsplit, mn);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace
+
+int w4a16_chunks_per_split(int K, int n_split) {
+  const int kchunks = K / kW4Kc;
+  return (kchunks + n_split - 1) / n_split;
+}
+
+cudaError_t launch_w4a16(const W4a16Args& a, cudaStream_t stream) {
+  if (a.M <= 16) return launch_mp<16>(a, stream);
+  if (a.M <= 32) return launch_mp<32>(a, stream);
+  if (a.M <= 64) return launch_mp<64>(a, stream);
+  if (a.M <= 96) return launch_mp<96>(a, stream);
+  return launch_mp<128>(a, stream);
+}
+
+}  // namespace fa

@@ -132,3 +132,18 @@ def test_strided_validation_statuses(lib):
     assert fwd(short) == 1    # rows of one head would overlap
     neg = (ctypes.c_int64 * 3)(128, -1, 1)
     assert fwd(neg) == 1
+
+
+def test_w4a16_validation_statuses(lib):
+    vp = ctypes.c_void_p
+    def g(M=4, N=128, K=256, n=1, y=FAKE, ws=0, wsb=0):
+        return lib.fa_w4a16_gemm(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(y), vp(ws), wsb, M, N, K, n, vp(0))
+    assert g(M=129) == 2
+    assert g(N=120) == 2
+    assert g(K=384) == 2
+    assert g(M=-1) == 1
+    assert g(M=0) == 0
+    assert g(y=FAKE + 8) == 3
+    assert g(K=1024, n=4) == 6                    # splits need a workspace
+    assert lib.fa_w4a16_workspace_size(4, 128, 1024, 4) == 4 * 4 * 128 * 4
+    assert lib.fa_w4a16_workspace_size(4, 128, 1024, 1) == 0
