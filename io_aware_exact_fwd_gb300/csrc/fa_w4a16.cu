@@ -37,7 +37,7 @@
 namespace fa {
 namespace {
 
-constexpr int kW4Threads = 384;  // 0 TMA, 1 MMA (+TMEM), 2-3 idle, 4-11 dequantisation
+constexpr int kW4Threads = 384;  // 0 TMA, 1-2 MMA issuers (1 owns TMEM), 3 idle, 4-11 dequantisation
 constexpr int kW4Rows = 128;     // output rows per unit (MMA M, TMEM lanes)
 constexpr int kW4Kc = 256;       // K per chunk: two groups of 128
 constexpr uint32_t kW4TmemCols = 512;
@@ -64,12 +64,16 @@ struct W4Cfg {
   // As many stages as fit next to the barriers (more bytes in flight per SM).
   static constexpr int kStages = (220 * 1024 / kStageBytes) < 8 ? (220 * 1024 / kStageBytes) : 8;
   static constexpr int kBarOff = kStages * kStageBytes;
-  // full[S], empty[S], afull[kA], aempty[kA], dfull, dempty, drain
-  static constexpr int kA = 3;  // A buffers in TMEM (128 columns each)
-  static constexpr int kNumBars = 2 * kStages + 2 * kA + 1 + 1 + 1;
+  // full[S], empty[S], afull[kA][2], aempty[kA], dfull, dempty, drain
+  static constexpr int kA = MP <= 64 ? 3 : 2;  // A buffers in TMEM (128 columns each)
+  static constexpr int kNumBars = 2 * kStages + 3 * kA + 1 + 1 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
-  static constexpr uint32_t kColA = 0, kColD = 384;  // A buffers at 0, 128, 256; D (MP <= 128 columns) at 384
+  // A buffers at 0, 128, ...; then one accumulator per group of the chunk (each group's MMAs
+  // are issued by their own thread, so the two streams overlap in the tensor pipe).
+  static constexpr uint32_t kDCols = MP < 32 ? 32 : MP;
+  static constexpr uint32_t kColA = 0, kColD0 = 128 * kA, kColD1 = 128 * kA + kDCols;
+  static_assert(kColD1 + kDCols <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -89,8 +93,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* bar_full = bars;
   uint64_t* bar_empty = bar_full + C::kStages;
-  uint64_t* bar_afull = bar_empty + C::kStages;  // [kA] A buffer written
-  uint64_t* bar_aempty = bar_afull + C::kA;      // [kA] A buffer consumed by the MMAs
+  uint64_t* bar_afull = bar_empty + C::kStages;  // [kA][2] group g of an A buffer written
+  uint64_t* bar_aempty = bar_afull + 2 * C::kA;  // [kA] A buffer consumed by both issuers' MMAs
   uint64_t* bar_dfull = bar_aempty + C::kA;      // unit's Y^T complete in TMEM
   uint64_t* bar_dempty = bar_dfull + 1;          // Y^T read out
   uint64_t* bar_drain = bar_dempty + 1;
@@ -112,15 +116,16 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 8 + 1);  // eight dequantising warps + the MMA commit
+      mbar_init(&bar_empty[s], 8 + 2);  // eight dequantising warps + both issuers' commits
     }
     for (int b = 0; b < C::kA; ++b) {
-      mbar_init(&bar_afull[b], 8);
-      mbar_init(&bar_aempty[b], 1);
+      mbar_init(&bar_afull[2 * b], 4);
+      mbar_init(&bar_afull[2 * b + 1], 4);
+      mbar_init(&bar_aempty[b], 2);
     }
-    mbar_init(bar_dfull, 1);
+    mbar_init(bar_dfull, 2);
     mbar_init(bar_dempty, 4);
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain, 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -158,10 +163,12 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------- MMA issuers (thread g: group g of each chunk)
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(kW4Rows, MP, 0, 0);  // rows x tokens, K-major B
+      const int g = warp - 1;
+      const uint32_t dcol = g == 0 ? C::kColD0 : C::kColD1;
+      constexpr uint32_t idesc = idesc_f16_f32(kW4Rows, MP < 16 ? 16 : MP, 0, 0);  // rows x tokens, K-major B
       const uint64_t xdesc = sdesc_sw128(smem_u32(smem + C::kOffX), 16, 1024);
       int item = 0, units = 0;
       bool ok = true;
@@ -173,16 +180,18 @@ __global__ void __launch_bounds__(kW4Threads, 1)
           const int slot = item % C::kStages;
           const int b = item % C::kA;
           if (!(ok = mbar_wait(&bar_full[slot], (item / C::kStages) & 1, wc, kSiteW4Mma))) break;
-          if (!(ok = mbar_wait(&bar_afull[b], (item / C::kA) & 1, wc, kSiteW4Mma))) break;
+          if (!(ok = mbar_wait(&bar_afull[2 * b + g], (item / C::kA) & 1, wc, kSiteW4Mma))) break;
           // The unit's first MMA overwrites Y^T: the previous unit's must be read out.
           if (c == c0 && units > 0 && !(ok = mbar_wait(bar_dempty, (units - 1) & 1, wc, kSiteW4Mma))) break;
           tc_fence_after();
           const uint32_t st = slot * C::kStageBytes;
 #pragma unroll
-          for (int kk = 0; kk < kW4Kc / 16; ++kk)  // kind::f16; the descriptor selects fp16 operands
-            mma_bf16_ts(tmem + C::kColD, tmem + C::kColA + 128u * b + 8u * kk,
+          for (int j = 0; j < 8; ++j) {  // kind::f16; the descriptor selects fp16 operands
+            const int kk = 8 * g + j;      // 16-wide K step within the chunk
+            mma_bf16_ts(tmem + dcol, tmem + C::kColA + 128u * b + 8u * kk,
                         sdesc_add(xdesc, st + (kk / 4) * C::kXBox + (kk % 4) * 32), idesc,
-                        (c > c0 || kk > 0) ? 1u : 0u);
+                        (c > c0 || j > 0) ? 1u : 0u);
+          }
           mma_commit(&bar_aempty[b]);
           mma_commit(&bar_empty[slot]);
         }
@@ -248,7 +257,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&bar_afull[b]);
+          mbar_arrive(&bar_afull[2 * b + g]);
           mbar_arrive(&bar_empty[slot]);
         }
       }
@@ -261,9 +270,13 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         const int sp = w / nstrips;
 #pragma unroll 1
         for (int mc = 0; mc < (MP + 31) / 32; ++mc) {  // MP = 16 reads 16 unused columns too
-          uint32_t v[32];
-          tmem_ld32(trow + C::kColD + 32u * mc, v);
+          uint32_t v[32], v1[32];
+          tmem_ld32(trow + C::kColD0 + 32u * mc, v);
+          tmem_ld32(trow + C::kColD1 + 32u * mc, v1);
           tmem_ld_wait32(v);
+          tmem_ld_wait32(v1);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
           if (n < N) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
