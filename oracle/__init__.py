@@ -28,6 +28,10 @@ check it against the pages by eye:
   Source: "FlashAttention-Skalierung, Multi-GPU-Training und
   Gewichtsquantisierung", section 1, bullet "Unterstützung geringer
   FP8-Präzision".
+* ``fp8_backward`` -- the straight-through backward of that FP8 attention: the
+  textbook gradient on the dequantised operands (rounded to bf16), carried back
+  through the rotation (dQ = (dQ' H) * s, dK likewise).  The pages give FP8 for
+  the forward only; this is the plainest reading of its backward.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
 ``--impl reference`` legs of ``bench.py`` may import this package.  The product
@@ -64,6 +68,13 @@ from .fp8 import (
     fp8_dequantize,
     E4M3_MAX,
 )
+from .fp8_backward import (
+    bf16_round,
+    fp8_dequantize_bf16,
+    fp8_operands,
+    fp8_backward_from_operands,
+    fp8_backward,
+)
 
 __all__ = [
     "attention_forward",
@@ -90,4 +101,9 @@ __all__ = [
     "fp8_prepare",
     "fp8_dequantize",
     "E4M3_MAX",
+    "bf16_round",
+    "fp8_dequantize_bf16",
+    "fp8_operands",
+    "fp8_backward_from_operands",
+    "fp8_backward",
 ]
