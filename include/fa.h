@@ -234,11 +234,12 @@ FA_API size_t fa_bwd_noalloc_max_workspace(void);
  *   For Q and K, each row x becomes y = (x * s) H_d (H_d the Sylvester
  *   Walsh-Hadamard matrix, entries +-1, so (QM)(KM)^T = d Q K^T with M = diag(s)
  *   H_d; fa_fwd_fp8 folds the 1/d into its scale).  V rows are unchanged.  Then
- *   per tile of 64 consecutive rows of one head: amax = max|y| (exact), codes =
- *   e4m3(y * (448 / amax)) with round-to-nearest-even and saturation (OCP E4M3,
- *   max 448), scale = amax / 448 (1 for an all-zero tile), so that
+ *   per tile of 64 consecutive rows of one head: amax = max|y| (exact), scale =
+ *   2^e with e the smallest integer such that amax <= 448 * 2^e (e clamped to
+ *   [-126, 126]; scale 1 for an all-zero tile), codes = e4m3(y * 2^-e) with
+ *   round-to-nearest-even and saturation (OCP E4M3, max 448), so that
  *   y ~= decode(code) * scale.  The transform is fp32 radix-2 butterflies with
- *   spans 1, 2, ..., d/2; 448 / amax and amax / 448 are IEEE fp32 divisions.
+ *   spans 1, 2, ..., d/2; the scaling by 2^-e is one fp32 multiply.
  *   Errors as fa_fwd; FA_ERR_WORKSPACE for a missing or short workspace;
  *   FA_ERR_INVALID_ARG for in_dtype not 0/1 or a NULL signs pointer.
  */
@@ -263,6 +264,60 @@ FA_API int fa_fp8_prepare(const void* q, const void* k, const void* v, int in_dt
  */
 FA_API int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* lse, int B, int H, int N, int d,
                       int causal, float scale, fa_stream_t stream);
+
+/*
+ * Backward pass of the FP8 attention.  The pages give FP8 for the forward only
+ * (same section); its backward is taken straight through the quantisation (the
+ * rounding's derivative taken as 1): the textbook gradient of attention on the
+ * dequantised operands, carried back through the rotation M = diag(s) H_d:
+ *   dQ = (dQ' H_d) * s,   dK = (dK' H_d) * s,   dV = dV'
+ * with dQ', dK', dV' the gradients with respect to Q' = bf16(decode(q8) * sQ),
+ * K' = bf16(decode(k8) * sK), V' = bf16(decode(v8) * sV) under the softmax scale
+ * scale / d (the forward's).  With the power-of-two tile scales of
+ * fa_fp8_prepare the bf16 rounding is exact: the backward sees the forward's
+ * operand values.  The products run on bf16 tensor cores (the bf16
+ * backward's kernels); the operands come from the FP8 workspace.
+ *
+ * fa_fp8_dequantize -- the operands alone: qr, kr, vr (bf16 [B, H, N, d], outputs,
+ *   dense) = bf16_rn(fp32(decode(code)) * scale of the row's 64-row tile), one
+ *   fp32 product then one rounding to nearest even.  d = 64 or 128.  Errors as
+ *   fa_fwd_fp8 (FA_ERR_MISALIGNED: outputs not 16-byte aligned).
+ *
+ * fa_bwd_fp8_workspace_size -- bytes of workspace fa_bwd_fp8 needs (0 if invalid
+ *   or unsupported): the bf16 backward's workspace, the three operands, and the
+ *   recomputed forward's O and LSE.
+ *
+ * fa_bwd_fp8 -- dq, dk, dv (bf16 [B, H, N, d], outputs, dense) from
+ *   fp8_ws     : const, filled by fa_fp8_prepare for these sizes (not modified)
+ *   signs      : const int8 [d] on the device, the signs given to fa_fp8_prepare
+ *   o, lse     : the forward's output and LSE (as from fa_fwd_fp8), dense; read
+ *                only when recompute_forward = 0 (may be NULL otherwise)
+ *   dout       : const bf16 [B, H, N, d]
+ *   workspace  : device memory of fa_bwd_fp8_workspace_size(...) bytes, 256-byte
+ *                aligned; overwritten
+ *   scale      : the softmax scale given to fa_fwd_fp8 (of the unrotated problem)
+ *   deterministic : 0 or 1, as fa_bwd_strided (1: dQ the same bits on every run)
+ *   recompute_forward : 0 or 1.  The gradient needs D_i = dO_i . O_i with O from
+ *                the UNROUNDED probabilities.  fa_fwd_fp8 rounds P to e4m3 for its
+ *                P V product, so its O carries that error into D and from there
+ *                into every dS of the row (a few percent RMS on dQ at N = 1000).
+ *                1: O and LSE are recomputed by the bf16 forward on Q', K', V'
+ *                (about 35 % more time); the result is the straight-through
+ *                gradient to the bf16 backward's accuracy.  0: the caller's o and
+ *                lse are used as given.
+ * Stages on `stream`: dequantise, [bf16 forward,] the bf16 backward (prep, main,
+ * dq), then the inverse rotation of dq and dk in place (fp32 butterflies, bf16
+ * rounding).  d = 128.  Errors as fa_bwd, plus FA_ERR_WORKSPACE for a missing or
+ * short FP8 workspace and FA_ERR_INVALID_ARG for a NULL signs pointer or a flag
+ * not 0/1.
+ */
+FA_API int fa_fp8_dequantize(const void* fp8_ws, size_t fp8_ws_bytes, void* qr, void* kr, void* vr, int B, int H,
+                             int N, int d, fa_stream_t stream);
+FA_API size_t fa_bwd_fp8_workspace_size(int B, int H, int N, int d);
+FA_API int fa_bwd_fp8(const void* fp8_ws, size_t fp8_ws_bytes, const int8_t* signs, const void* o, const void* dout,
+                      const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H,
+                      int N, int d, int causal, float scale, int deterministic, int recompute_forward,
+                      fa_stream_t stream);
 
 /*
  * Split-KV forward ("decode"-shaped attention: few queries, many keys) and the

@@ -88,6 +88,13 @@ def load_library():
     lib.fa_fwd_fp8.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, ctypes.c_size_t, vp, vp, i, i, i, i, i, f, vp]
     lib.fa_bwd_noalloc.restype = i
+    lib.fa_fp8_dequantize.argtypes = [vp, ctypes.c_size_t, vp, vp, vp, i, i, i, i, vp]
+    lib.fa_fp8_dequantize.restype = i
+    lib.fa_bwd_fp8_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd_fp8_workspace_size.restype = ctypes.c_size_t
+    lib.fa_bwd_fp8.argtypes = [vp, ctypes.c_size_t, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, f,
+                               i, i, vp]
+    lib.fa_bwd_fp8.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.fa_bwd_noalloc_max_workspace.restype = ctypes.c_size_t
     lib.fa_bwd_noalloc_max_workspace.argtypes = []
@@ -352,6 +359,67 @@ def fa_fwd_fp8(workspace, shape, o=None, lse=None, causal: bool = False, scale: 
                             int(bool(causal)), float(scale), _stream_handle(stream))
     _check(st, "fa_fwd_fp8")
     return o, lse
+
+
+def fa_fp8_dequantize(workspace, shape, stream=None):
+    """The FP8 backward's bf16 operands (Q', K', V') from a prepared workspace; shape = (B, H, N, d)."""
+    import torch
+
+    lib = load_library()
+    B, H, N, d = shape
+    out = [torch.empty((B, H, N, d), dtype=torch.bfloat16, device=workspace.device) for _ in range(3)]
+    with torch.cuda.device(workspace.device):
+        st = lib.fa_fp8_dequantize(_ptr(workspace), _ws_bytes(workspace), _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+                                   B, H, N, d, _stream_handle(stream))
+    _check(st, "fa_fp8_dequantize")
+    return tuple(out)
+
+
+def fa_bwd_fp8_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    """Bytes of device workspace fa_bwd_fp8 needs (0 if unsupported)."""
+    return int(load_library().fa_bwd_fp8_workspace_size(B, H, N, d))
+
+
+def fa_bwd_fp8(fp8_workspace, signs, o, do, lse, dq=None, dk=None, dv=None, workspace=None, causal: bool = False,
+               scale: float | None = None, deterministic: bool = False, recompute_forward: bool = False,
+               stream=None):
+    """Straight-through backward of the FP8 attention (d = 128): returns (dq, dk, dv), bf16.
+
+    fp8_workspace: filled by fa_fp8_prepare; signs: the int8 [d] signs given to it;
+    o, lse: the forward's outputs (bf16 [B, H, N, d], fp32 [B, H, N]), ignored and
+    may be None when ``recompute_forward`` (O and LSE recomputed in bf16 from the
+    FP8 operands, so that D uses the unrounded probabilities); do: bf16
+    [B, H, N, d]; scale: the softmax scale given to fa_fwd_fp8.
+    """
+    import torch
+
+    lib = load_library()
+    B, H, N, d = do.shape
+    _check_bhnd("do", do, (B, H, N, d), torch.bfloat16)
+    if not recompute_forward:
+        _check_bhnd("o", o, (B, H, N, d), torch.bfloat16)
+        if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+            raise ValueError("lse must be a contiguous float32 tensor [B, H, N]")
+    if signs.dtype != torch.int8 or tuple(signs.shape) != (d,) or not signs.is_cuda:
+        raise ValueError("signs must be an int8 CUDA tensor of shape [d]")
+    dense = lambda: torch.empty((B, H, N, d), dtype=torch.bfloat16, device=do.device)
+    dq = dense() if dq is None else dq
+    dk = dense() if dk is None else dk
+    dv = dense() if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_bhnd(name, t, (B, H, N, d), torch.bfloat16)
+    if workspace is None:
+        workspace = torch.empty(max(fa_bwd_fp8_workspace_size(B, H, N, d), 1), dtype=torch.uint8, device=do.device)
+    if scale is None:
+        scale = d ** -0.5
+    with torch.cuda.device(do.device):
+        st = lib.fa_bwd_fp8(_ptr(fp8_workspace), _ws_bytes(fp8_workspace), _ptr(signs),
+                            None if recompute_forward else _ptr(o), _ptr(do),
+                            None if recompute_forward else _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                            _ws_bytes(workspace), B, H, N, d, int(bool(causal)), float(scale),
+                            int(bool(deterministic)), int(bool(recompute_forward)), _stream_handle(stream))
+    _check(st, "fa_bwd_fp8")
+    return dq, dk, dv
 
 
 def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal: bool = False, scale: float | None = None,

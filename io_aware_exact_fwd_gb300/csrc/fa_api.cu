@@ -648,6 +648,95 @@ int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* lse, int 
                                                                                                   : FA_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Workspace of fa_bwd_fp8: the bf16 backward's workspace, then the bf16 operands
+// Q', K', V' [BH, N, d], then the recomputed forward's O [BH, N, d] (bf16) and LSE
+// [BH, N] (fp32); every region on a 256-byte boundary.
+struct Fp8BwdLayout {
+  size_t off_qr, off_kr, off_vr, off_o, off_lse, total;
+};
+
+Fp8BwdLayout fp8_bwd_layout(int B, int H, int N, int d) {
+  auto a256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t op = a256(static_cast<size_t>(B) * H * N * d * 2);
+  Fp8BwdLayout l{};
+  l.off_qr = a256(fa::bwd_workspace_layout(B, H, N, d).total);
+  l.off_kr = l.off_qr + op;
+  l.off_vr = l.off_kr + op;
+  l.off_o = l.off_vr + op;
+  l.off_lse = l.off_o + op;
+  l.total = l.off_lse + a256(static_cast<size_t>(B) * H * N * 4);
+  return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fp8_dequantize(const void* fp8_ws, size_t fp8_ws_bytes, void* qr, void* kr, void* vr, int B, int H, int N,
+                      int d, fa_stream_t stream) {
+  const int vs = validate_shape(B, H, N, d, 0, 1.f);
+  if (vs < 0) return FA_OK;
+  if (vs != FA_OK) return vs;
+  if (!fp8_ws) return FA_ERR_WORKSPACE;
+  if (fp8_ws_bytes < fa::fp8_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
+  if (!qr || !kr || !vr) return FA_ERR_INVALID_ARG;
+  if (!aligned(fp8_ws, 256) || !aligned(qr, 16) || !aligned(kr, 16) || !aligned(vr, 16)) return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  const int st = device_state(&ds);
+  if (st != FA_OK) return st;
+  return status_of(fa::launch_fp8_dequant(fp8_ws, qr, kr, vr, B, H, N, d, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t fa_bwd_fp8_workspace_size(int B, int H, int N, int d) {
+  if (validate_shape(B, H, N, d, 0, 1.f) != FA_OK || d != 128) return 0;
+  return fp8_bwd_layout(B, H, N, d).total;
+}
+
+int fa_bwd_fp8(const void* fp8_ws, size_t fp8_ws_bytes, const int8_t* signs, const void* o, const void* dout,
+               const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N,
+               int d, int causal, float scale, int deterministic, int recompute_forward, fa_stream_t stream) {
+  if (deterministic != 0 && deterministic != 1) return FA_ERR_INVALID_ARG;
+  if (recompute_forward != 0 && recompute_forward != 1) return FA_ERR_INVALID_ARG;
+  const int vs = validate_shape(B, H, N, d, causal, scale);
+  if (vs < 0) return FA_OK;
+  if (vs != FA_OK) return vs;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!fp8_ws || fp8_ws_bytes < fa::fp8_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
+  if (!signs) return FA_ERR_INVALID_ARG;
+  const Fp8BwdLayout l = fp8_bwd_layout(B, H, N, d);
+  if (!workspace || ws_bytes < l.total) return FA_ERR_WORKSPACE;
+  if (!aligned(fp8_ws, 256) || !aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  char* ws = static_cast<char*>(workspace);
+  void* qr = ws + l.off_qr;
+  void* kr = ws + l.off_kr;
+  void* vr = ws + l.off_vr;
+  if (recompute_forward) {
+    o = ws + l.off_o;
+    lse = reinterpret_cast<const float*>(ws + l.off_lse);
+  }
+  // The operands carry the unnormalised rotation's factor d in Q' K'^T.
+  const float op_scale = scale / static_cast<float>(d);
+  fa::BwdArgs a;
+  int st = bwd_setup(a, kUseQKV | kUseO | kUseDout | kUseLse | kUseDq | kUseDkDv, qr, kr, vr, o, dout, lse, dq, dk,
+                     dv, workspace, ws_bytes, B, H, N, d, causal, op_scale);
+  if (st < 0) return FA_OK;
+  if (st != FA_OK) return st;
+  a.deterministic = deterministic;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fa::launch_fp8_dequant(fp8_ws, qr, kr, vr, B, H, N, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (recompute_forward) {
+    st = fa_fwd(qr, kr, vr, const_cast<void*>(o), const_cast<float*>(lse), B, H, N, d, causal, op_scale, stream);
+    if (st != FA_OK) return st;
+  }
+  cudaError_t e = fa::launch_bwd_bf16(a, s);
+  if (e == cudaSuccess) e = fa::launch_fp8_unrotate(dq, dk, signs, static_cast<long long>(B) * H * N, s);
+  return status_of(e);
+}
+
 int fa_sync_check(fa_stream_t stream) {
   DeviceState* ds = nullptr;
   const int st = device_state(&ds);

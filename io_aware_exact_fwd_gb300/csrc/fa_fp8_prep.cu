@@ -13,9 +13,11 @@
 //    subtract; spans below the per-thread width in registers, the rest across
 //    lanes with shuffles).  The 1/sqrt(d) normalisation of the orthogonal
 //    matrix is left to the attention kernel's score scale.  V is not rotated.
-//  * amax = max |x| over the tile (exact), inv = 448 / amax (one IEEE fp32
-//    division), codes = e4m3_rn_satfinite(x * inv), sigma = amax / 448
-//    (sigma = inv = 1 for an all-zero tile).
+//  * amax = max |x| over the tile (exact); sigma = 2^e, the smallest power of
+//    two with amax <= 448 sigma (1 for an all-zero tile), inv = 2^-e; codes =
+//    e4m3_rn_satfinite(x * inv), an exact scaling.  e4m3 being floating point, a
+//    power-of-two scale loses no relative precision, and decode(code) * sigma is
+//    exact in fp32 and bf16 (the FP8 backward's operands).
 //  * Q and K codes are written row-major [BH, N, d]; V codes transposed,
 //    [BH, d, npad] with keys contiguous (npad = N rounded up to 128, a whole
 //    attention key block), so that V is a K-major operand of the P V MMA.
@@ -107,6 +109,20 @@ __device__ __forceinline__ float block_amax(float amax, float* s_amax, int warp,
   return amax;
 }
 
+// Power-of-two tile scale: e = the smallest integer with amax <= 448 * 2^e, read
+// from amax's fp32 bits (amax = m 2^e0, m in [1, 2): e = e0 - 8, plus 1 when
+// m > 1.75), clamped to [-126, 126]; e = 0 for amax = 0.  sigma = 2^e and
+// inv = 2^-e are exact normal fp32 numbers.
+__device__ __forceinline__ void pow2_scale(float amax, float& sigma, float& inv) {
+  const uint32_t b = __float_as_uint(amax);
+  const int field = static_cast<int>((b >> 23) & 0xFFu);
+  int e = field == 0 ? -126 : field - 135 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  if (amax == 0.f) e = 0;
+  e = max(-126, min(126, e));
+  sigma = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+  inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* __restrict__ q,
                                                                    const void* __restrict__ k,
@@ -145,8 +161,8 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
       }
     }
     amax = block_amax(amax, s_amax, warp, lane);
-    const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
-    const float sigma = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    float sigma, inv;
+    pow2_scale(amax, sigma, inv);
     if (threadIdx.x == 0 && tile < ntiles)
       reinterpret_cast<float*>(ws + lay.off_sv)[static_cast<size_t>(bh) * ntiles + tile] = sigma;
 #pragma unroll
@@ -197,8 +213,8 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
     for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(x[r][i]));
   }
   amax = block_amax(amax, s_amax, warp, lane);
-  const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
-  const float sigma = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  float sigma, inv;
+  pow2_scale(amax, sigma, inv);
   if (threadIdx.x == 0)
     reinterpret_cast<float*>(ws + (which == 0 ? lay.off_sq : lay.off_sk))[static_cast<size_t>(bh) * ntiles + tile] =
         sigma;

@@ -132,6 +132,14 @@ Fp8Layout fp8_layout(int B, int H, int N, int d);
 // FwdArgs unused), writes bf16 O and fp32 LSE; d = 128.
 cudaError_t launch_fwd_fp8(const FwdArgs& a, const void* workspace, cudaStream_t stream);
 
+// FP8 backward helpers (fa_fp8_bwd.cu).  launch_fp8_dequant: bf16 operands
+// bf16_rn(decode(code) * tile scale) of the rotated Q, K and of V, dense [BH, N, d],
+// from a prepared FP8 workspace.  launch_fp8_unrotate: rows of 128 of dq and dk
+// (dense, `rows` each) replaced in place by bf16((x H_128) * s).
+cudaError_t launch_fp8_dequant(const void* fp8_ws, void* qr, void* kr, void* vr, int B, int H, int N, int d,
+                               cudaStream_t stream);
+cudaError_t launch_fp8_unrotate(void* dq, void* dk, const int8_t* signs, long long rows, cudaStream_t stream);
+
 struct Fp8PrepArgs {
   const void* q;
   const void* k;

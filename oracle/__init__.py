@@ -66,6 +66,7 @@ from .fp8 import (
     e4m3_round,
     fp8_prepare,
     fp8_dequantize,
+    pow2_scale_exponent,
     E4M3_MAX,
 )
 from .fp8_backward import (
@@ -100,6 +101,7 @@ __all__ = [
     "e4m3_round",
     "fp8_prepare",
     "fp8_dequantize",
+    "pow2_scale_exponent",
     "E4M3_MAX",
     "bf16_round",
     "fp8_dequantize_bf16",

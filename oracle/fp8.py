@@ -18,15 +18,20 @@ matrix, the tile, the FP8 format nor the rounding; the readings taken here are:
 * Format: OCP FP8 E4M3 ("fn": bias 7, no infinities, one NaN pattern per sign,
   largest finite 448).  Rounding: round-to-nearest, ties to even, saturating
   to +-448.
-* Per tile: amax = max |x|; codes = e4m3(x * (448 / amax)); dequantisation
-  scale sigma = amax / 448 (sigma = 1 and inverse scale 1 for an all-zero tile).
+* Per tile: amax = max |x|; the dequantisation scale is the power of two
+  sigma = 2^e with e the smallest integer such that amax <= 448 * 2^e (e kept in
+  [-126, 126] so that sigma and 1/sigma are normal fp32 numbers); codes =
+  e4m3(x * 2^-e).  An all-zero tile has sigma = 1.  Because e4m3 is a
+  floating-point format, a power-of-two scale costs no relative precision
+  (amax / sigma lies in (224, 448]); it makes the scaling exact, and the
+  dequantised values decode(code) * sigma exact in fp32 and bf16.
 
 Because these codes are integers decided by floating point, the decision is made
 in the kernel's precision (IEEE fp32) with the kernel's order of operations:
 the rotation is the radix-2 fast Walsh-Hadamard transform with butterfly spans
 1, 2, 4, ..., d/2 (each butterfly is one fp32 add and one fp32 subtract),
-amax is exact, ``448 / amax`` is one fp32 division and ``x * inv`` one fp32
-multiply.  The transform is pinned against the float64 matrix product
+amax is exact, e is read from amax's fp32 bits, and ``x * 2^-e`` is one fp32
+multiply (exact unless it leaves the normal range).  The transform is pinned against the float64 matrix product
 ``x @ diag(s) @ H`` within fp32 rounding bounds.
 """
 
@@ -123,6 +128,23 @@ def e4m3_decode(codes) -> np.ndarray:
     return s * val
 
 
+def pow2_scale_exponent(amax) -> np.ndarray:
+    """Smallest integer e with amax <= 448 * 2^e, clamped to [-126, 126]; 0 where amax == 0.
+
+    amax (fp32, >= 0) = m * 2^e0 with m in [1, 2): 448 * 2^(e0-8) = 1.75 * 2^e0, so
+    e = e0 - 8 when m <= 1.75 and e0 - 7 otherwise.  e0 and m come from the fp32
+    bits (a subnormal amax gives e <= -134, clamped to -126).
+    """
+    a = np.asarray(amax, dtype=np.float32)
+    bits = a.view(np.uint32).astype(np.int64)
+    field = (bits >> 23) & 0xFF
+    mant = bits & 0x7FFFFF
+    e = field - 127 - 8 + (mant > 0x600000)
+    e = np.where(field == 0, -126, e)
+    e = np.clip(e, -126, 126)
+    return np.where(a == 0, 0, e).astype(np.int64)
+
+
 def _quantise_tiles(x32: np.ndarray, tile: int):
     """Per-tile e4m3 codes and dequantisation scales of an fp32 array [..., N, d].
 
@@ -136,12 +158,12 @@ def _quantise_tiles(x32: np.ndarray, tile: int):
     for t in range(nt):
         blk = x32[..., t * tile:(t + 1) * tile, :]
         amax = np.abs(blk).max(axis=(-2, -1)).astype(np.float32)
-        zero = amax == 0
-        safe = np.where(zero, np.float32(1), amax).astype(np.float32)
-        inv = np.where(zero, np.float32(1), np.float32(E4M3_MAX) / safe).astype(np.float32)
+        e = pow2_scale_exponent(amax)
+        sig = np.ldexp(np.float32(1), e).astype(np.float32)
+        inv = np.ldexp(np.float32(1), -e).astype(np.float32)
         y = (blk * inv[..., None, None]).astype(np.float32)
         codes[..., t * tile:(t + 1) * tile, :] = e4m3_encode(y)
-        sigma[..., t] = np.where(zero, np.float32(1), safe / np.float32(E4M3_MAX)).astype(np.float32)
+        sigma[..., t] = sig
     return codes, sigma
 
 

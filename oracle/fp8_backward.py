@@ -28,7 +28,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .attention import attention_backward, attention_forward
+from .attention import attention_backward, attention_backward_sampled, attention_forward
 from .fp8 import e4m3_decode, sylvester_hadamard
 
 
@@ -92,4 +92,19 @@ def fp8_backward(prep: dict, signs, do, scale: float, causal: bool, tile: int = 
     return dq, dk, dv, o, lse
 
 
-__all__ = ["bf16_round", "fp8_dequantize_bf16", "fp8_operands", "fp8_backward_from_operands", "fp8_backward"]
+def fp8_backward_sampled(qr_head, kr_head, v_head, do_head, signs, scale: float, causal: bool, rows, keys):
+    """dQ at selected rows and dK, dV at selected keys of ONE head, from its operands.
+
+    The same definition as ``fp8_backward_from_operands`` evaluated for the chosen
+    rows and keys only (``attention_backward_sampled``), then carried back through
+    the rotation.  Returns (dQ[len(rows), d], dK[len(keys), d], dV[len(keys), d]).
+    """
+    d = np.asarray(qr_head).shape[-1]
+    dqr, dkr, dv = attention_backward_sampled(qr_head, kr_head, v_head, do_head, scale / d, causal, rows, keys)
+    hd = sylvester_hadamard(d)
+    s = np.asarray(signs, dtype=np.float64).reshape(-1)
+    return (dqr @ hd) * s, (dkr @ hd) * s, dv
+
+
+__all__ = ["bf16_round", "fp8_dequantize_bf16", "fp8_operands", "fp8_backward_from_operands", "fp8_backward",
+           "fp8_backward_sampled"]

@@ -147,3 +147,27 @@ def test_w4a16_validation_statuses(lib):
     assert g(K=1024, n=4) == 6                    # splits need a workspace
     assert lib.fa_w4a16_workspace_size(4, 128, 1024, 4) == 4 * 4 * 128 * 4
     assert lib.fa_w4a16_workspace_size(4, 128, 1024, 1) == 0
+
+
+def test_fp8_backward_validation_statuses(lib):
+    vp = ctypes.c_void_p
+    B, H, N, d = 1, 2, 100, 128
+    f8 = lib.fa_fp8_workspace_size(B, H, N, d)
+    need = lib.fa_bwd_fp8_workspace_size(B, H, N, d)
+    assert need >= lib.fa_bwd_workspace_size(B, H, N, d) + 4 * B * H * N * d * 2 + B * H * N * 4
+    assert lib.fa_bwd_fp8_workspace_size(B, H, N, 64) == 0
+
+    def g(det=0, rec=0, dd=d, ws8=FAKE, f8b=f8, signs=FAKE, ws=FAKE, wsb=need, n=N):
+        return lib.fa_bwd_fp8(vp(ws8), f8b, vp(signs), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                              vp(ws), wsb, B, H, n, dd, 0, 0.1, det, rec, vp(0))
+    assert g(det=2) == 1
+    assert g(rec=-1) == 1
+    assert g(dd=64) == 2
+    assert g(ws8=0) == 6
+    assert g(f8b=f8 - 1) == 6
+    assert g(signs=0) == 1
+    assert g(wsb=need - 1) == 6
+    assert g(ws=FAKE + 16) == 3
+    assert g(n=0) == 0
+    assert lib.fa_fp8_dequantize(vp(FAKE), f8, vp(FAKE + 8), vp(FAKE), vp(FAKE), B, H, N, d, vp(0)) == 3
+    assert lib.fa_fp8_dequantize(vp(0), f8, vp(FAKE), vp(FAKE), vp(FAKE), B, H, N, d, vp(0)) == 6

@@ -16,6 +16,7 @@ from oracle import (
     fp8_dequantize,
     fp8_prepare,
     fwht_f32,
+    pow2_scale_exponent,
     sylvester_hadamard,
 )
 from synth import normal_qkv, outlier_qkv, rotation_signs
@@ -122,13 +123,33 @@ def test_fp8_prepare_tiles_scales_and_error_bounds():
         for t in range(4):
             blk = ref[..., t * 64:(t + 1) * 64, :]
             amax = np.abs(blk).max(axis=(-2, -1))
-            np.testing.assert_allclose(sig[..., t], amax / 448.0, rtol=2 ** -23)
-            # Every tile reaches the top code in magnitude (its amax maps to 448).
-            assert (np.abs(e4m3_decode(codes[..., t * 64:(t + 1) * 64, :])).max(axis=(-2, -1)) == 448).all()
+            # sigma is a power of two and the tile's amax lands in the top binade (224, 448].
+            m, _ = np.frexp(sig[..., t].astype(np.float64))
+            assert (m == 0.5).all()
+            ratio = amax / sig[..., t]
+            assert ((ratio > 224) & (ratio <= 448)).all()
+            # The scaling is exact, so the largest code is the e4m3 rounding of amax / sigma.
+            top = np.abs(e4m3_decode(codes[..., t * 64:(t + 1) * 64, :])).max(axis=(-2, -1))
+            np.testing.assert_array_equal(top, e4m3_round(ratio))
             err = np.abs(deq[..., t * 64:(t + 1) * 64, :] - blk)
             # 3 mantissa bits: relative error <= 2^-4 for normals, absolute <= 2^-10 * sigma for subnormals.
             bound = np.maximum(np.abs(blk) * 2.0 ** -4, 2.0 ** -10 * sig[..., t][..., None, None]) * 1.001
             assert (err <= bound).all()
+
+
+def test_pow2_scale_exponent_by_cases():
+    # Smallest e with amax <= 448 * 2^e.  448 = 1.75 * 2^8 sits exactly on the rule's edge.
+    cases = [
+        (448.0, 0), (448.0 * (1 + 2 ** -23), 1), (224.0, -1), (224.0 * (1 + 2 ** -23), 0),
+        (1.0, -8), (1.75, -8), (1.75 * (1 + 2 ** -23), -7), (1.9999999, -7), (2.0 ** -20, -28),
+        (3.4e38, 120), (1e-45, -126), (2.0 ** -130, -126), (0.0, 0),
+    ]
+    for amax, want in cases:
+        got = int(pow2_scale_exponent(np.float32(amax)))
+        assert got == want, (amax, got, want)
+        if amax > 0 and -126 < want:
+            a = float(np.float32(amax))
+            assert a <= 448.0 * 2.0 ** want and a > 448.0 * 2.0 ** (want - 1)
 
 
 def test_fp8_prepare_zero_tile():

@@ -134,3 +134,32 @@ def test_fp8_backward_uses_the_dequantised_operands():
                                      x["v"].numpy().astype(np.float64), do, d ** -0.5, True)
     assert np.abs(dv - dvx).max() <= 0.2 * np.abs(dvx).max()
     assert np.abs(dq - dqx).max() <= 0.5 * np.abs(dqx).max()
+
+
+def test_operands_are_the_exact_dequantised_values():
+    # Power-of-two tile scales: decode(code) * sigma has at most 4 significant bits,
+    # so its bf16 rounding is exact and the backward sees the forward's operands.
+    from oracle import fp8_dequantize
+
+    x = outlier_qkv(2, 2, 300, 128, seed=21)
+    s = rotation_signs(128, seed=21).numpy()
+    prep = fp8_prepare(x["q"], x["k"], x["v"], s)
+    for name, op in zip(("q", "k", "v"), fp8_operands(prep)):
+        np.testing.assert_array_equal(op, fp8_dequantize(prep[name + "8"], prep["s" + name]))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_equals_full(causal):
+    from oracle.fp8_backward import fp8_backward_sampled
+
+    B, H, N, d = 1, 1, 150, 64
+    x = outlier_qkv(B, H, N, d, seed=30)
+    do = torch.randn(B, H, N, d, generator=torch.Generator().manual_seed(2)).numpy().astype(np.float64)
+    s = rotation_signs(d, seed=30).numpy()
+    prep = fp8_prepare(x["q"], x["k"], x["v"], s)
+    dq, dk, dv, _, _ = fp8_backward(prep, s, do, 0.2, causal)
+    qr, kr, vr = fp8_operands(prep)
+    idx = np.array([0, 5, 63, 64, 149])
+    sq, sk, sv = fp8_backward_sampled(qr[0, 0], kr[0, 0], vr[0, 0], do[0, 0], s, 0.2, causal, idx, idx)
+    for got, full in ((sq, dq), (sk, dk), (sv, dv)):
+        np.testing.assert_allclose(got, full[0, 0, idx], rtol=1e-10, atol=1e-12 * np.abs(full).max())
