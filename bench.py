@@ -284,7 +284,8 @@ def run_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
     d2h = sum(t.numel() * t.element_size() for t in houts)
 
-    nxt = next_rows(fa, q, k, v, g, o, lse, dq, dk, dv, ws, causal, scale, stage_ms) if rank == 0 else None
+    nxt = (next_rows(fa, q, k, v, g, o, lse, dq, dk, dv, ws, causal, scale, stage_ms, (ws8, signs, o8, lse8))
+           if rank == 0 else None)
 
     if rank != 0:
         if world > 1:
@@ -370,8 +371,10 @@ def run_ours(args):
 
 
 # Rows past the hot path, timed after the step (not part of `value`): the split-KV
-# decode forward on its own workload, and the deterministic backward on the step's.
+# decode forward and the 4-bit-weight GEMV on their own workloads; the
+# deterministic backward and the FP8 backward on the step's.
 DECODE = {"B": 8, "H": 16, "Nq": 1, "Nk": 32768, "d": 128, "causal": False, "seed": 5}
+W4A16 = {"M": 1, "N": 28672, "K": 8192, "seed": 6}
 
 
 def _median_ms(fn, reps, flush=None):
@@ -390,10 +393,10 @@ def _median_ms(fn, reps, flush=None):
     return sorted(x.elapsed_time(y) for x, y in ts)[reps // 2]
 
 
-def next_rows(fa, q, k, v, g, o, lse, dq, dk, dv, ws, causal, scale, stage_ms):
+def next_rows(fa, q, k, v, g, o, lse, dq, dk, dv, ws, causal, scale, stage_ms, fp8):
     import torch
 
-    from synth import normal_qkv
+    from synth import normal_qkv, w4a16_inputs
 
     out = {}
     w = DECODE
@@ -423,6 +426,36 @@ def next_rows(fa, q, k, v, g, o, lse, dq, dk, dv, ws, causal, scale, stage_ms):
     out["bwd_deterministic"] = {"ms": round(ms_det, 5),
                                 "ms_atomic": round(stage_ms["bwd_prep"] + stage_ms["bwd_main"] + stage_ms["bwd_dq"], 5),
                                 "launches": 4}
+    # FP8 backward on the step's FP8 workspace and dO, both modes.
+    ws8, signs, o8, lse8 = fp8
+    B, H, N, d = q.shape
+    wsb = torch.empty(fa.fa_bwd_fp8_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    for rec in (False, True):
+        call = lambda: fa.fa_bwd_fp8(ws8, signs, o8, g, lse8, dq, dk, dv, wsb, causal=causal, scale=scale,
+                                     recompute_forward=rec)
+        for _ in range(3):
+            call()
+        out["bwd_fp8_recompute" if rec else "bwd_fp8"] = {"ms": round(_median_ms(call, 20, flush), 5),
+                                                          "launches": 6 if rec else 5}
+    fa.fa_sync_check()
+    del wsb
+    # W4A16 decode GEMV: 28672 x 8192 packed weights (117 MB, beyond L2) times one activation row.
+    w = W4A16
+    xin = w4a16_inputs(w["M"], w["N"], w["K"], w["seed"])
+    x, wq, sc, zr = (xin[n].cuda() for n in ("x", "wq", "scales", "zeros"))
+    nsp = fa.fa_w4a16_default_splits(w["M"], w["N"], w["K"])
+    wsw = torch.empty(max(fa.fa_w4a16_workspace_size(w["M"], w["N"], w["K"], nsp), 1), dtype=torch.uint8,
+                      device="cuda")
+    y = torch.empty(w["M"], w["N"], dtype=torch.float16, device="cuda")
+    call = lambda: fa.fa_w4a16_gemm(x, wq, sc, zr, y, wsw, n_split=nsp)
+    for _ in range(3):
+        call()
+    ms_w = _median_ms(call, 20, flush)
+    fa.fa_sync_check()
+    M_, N_, K_ = w["M"], w["N"], w["K"]
+    byts = N_ * K_ // 2 + 3 * N_ * K_ // 128 + 2 * M_ * K_ + 2 * M_ * N_
+    out["w4a16_gemv"] = {"config": dict(w, n_split=nsp), "ms": round(ms_w, 5), "bytes": byts,
+                         "gbs": byts / ms_w / 1e6, "launches": 2 if nsp > 1 else 1}
     return out
 
 
@@ -441,6 +474,18 @@ def finish_next_rows(nxt, peaks):
         "bwd_deterministic": {"workload": "bf16 backward with order-free dQ, the step's configuration",
                               "ms": bd["ms"], "tflops": round(f_bwd / (bd["ms"] * 1e-3) / 1e12, 1),
                               "ms_atomic_dq": bd["ms_atomic"], "gpu_launches": bd["launches"]},
+        "bwd_fp8": {"workload": "FP8 backward (straight-through; dequantise, bf16 backward, inverse rotation), "
+                                "the step's configuration, with fa_fwd_fp8's O and LSE",
+                    "ms": nxt["bwd_fp8"]["ms"], "tflops": round(f_bwd / (nxt["bwd_fp8"]["ms"] * 1e-3) / 1e12, 1),
+                    "ms_recompute_forward": nxt["bwd_fp8_recompute"]["ms"],
+                    "tflops_recompute_forward": round(f_bwd / (nxt["bwd_fp8_recompute"]["ms"] * 1e-3) / 1e12, 1),
+                    "gpu_launches": nxt["bwd_fp8"]["launches"]},
+        "w4a16_gemv": {"workload": "W4A16 dequantising GEMV (4-bit weights, group 128, fp16 activations)",
+                       "config": nxt["w4a16_gemv"]["config"], "ms": nxt["w4a16_gemv"]["ms"], "bound": "hbm",
+                       "achieved": round(nxt["w4a16_gemv"]["gbs"], 1), "unit": "GB/s", "peak": peaks["hbm_gbs"],
+                       "frac": round(nxt["w4a16_gemv"]["gbs"] / peaks["hbm_gbs"], 4),
+                       "algorithmic_bytes": nxt["w4a16_gemv"]["bytes"],
+                       "gpu_launches": nxt["w4a16_gemv"]["launches"]},
     }
 
 
