@@ -391,7 +391,8 @@ FA_API int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, 
  * section 3, "Wie spezielle CUDA-Kernels während der Ausführung dequantisieren
  * (W4A16)": packed 4-bit weights are read from memory, unpacked in registers with
  * shifts and masks, given their scale and zero point, and fed as fp16 with the
- * fp16 activations to the tensor cores, never written back unpacked).
+ * fp16 activations to the tensor cores, never written back unpacked; for a
+ * matrix-vector product the CUDA cores take that role, see Paths).
  *
  *   Y[m, n] = sum_k X[m, k] * W[n, k],   W[n, k] = fp16((q[n, k] - z[g, n]) * s[g, n]),  g = k / 128
  *
@@ -401,11 +402,15 @@ FA_API int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, 
  *            4i+16..4i+19 (i = 0..3), so one shift and one mask give a pair
  *   scales : const fp16 [K / 128, N]     zeros : const uint8 [K / 128, N] (0..15)
  * Limits: 1 <= M <= 128 (decode-sized batches; the product is then bound by
- * reading the weights), N a multiple of 16, K a multiple of 256.  n_split cuts K
- * into ranges computed in parallel whose fp32 partials are summed in a fixed order
+ * reading the weights), N a multiple of 16, K a multiple of 256.
+ * Paths: M = 1 (with K <= 65536) is a matrix-vector stream; it runs on the CUDA
+ * cores (mixed-precision FMAs, fp16 products summed in fp32), one pass over K per
+ * output row: n_split is ignored and no workspace is used.  Larger M runs on the
+ * tensor cores (tcgen05 kind::f16, fp32 accumulation); there n_split cuts K into
+ * ranges computed in parallel whose fp32 partials are summed in a fixed order
  * (the same bits on every run); n_split <= 0 selects fa_w4a16_default_splits.
  * Numerics: each weight is the fp16 rounding of (q - z) s; products accumulate in
- * fp32 on the tensor cores; Y is rounded to fp16 once.
+ * fp32; Y is rounded to fp16 once.
  * Errors: FA_ERR_UNSUPPORTED for sizes outside the limits, FA_ERR_WORKSPACE when
  * a split needs fa_w4a16_workspace_size(...) bytes of workspace (256-byte
  * aligned) that were not given, FA_ERR_MISALIGNED for a tensor not 16-byte aligned.

@@ -371,6 +371,7 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 
 size_t fa_w4a16_workspace_size(int M, int N, int K, int n_split) {
   if (M < 1 || M > 128 || N < 16 || N % 16 != 0 || K < 256 || K % 256 != 0 || n_split < 1 || n_split > 1024) return 0;
+  if (fa::w4a16_uses_gemv(M, K)) return 0;  // one pass over K per row: no partials
   const int cps = fa::w4a16_chunks_per_split(K, n_split);
   const int nsplit = (K / 256 + cps - 1) / cps;
   return nsplit > 1 ? static_cast<size_t>(nsplit) * M * N * sizeof(float) : 0;
@@ -378,6 +379,7 @@ size_t fa_w4a16_workspace_size(int M, int N, int K, int n_split) {
 
 int fa_w4a16_default_splits(int M, int N, int K) {
   if (M < 1 || M > 128 || N < 16 || N % 16 != 0 || K < 256 || K % 256 != 0) return 0;
+  if (fa::w4a16_uses_gemv(M, K)) return 1;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                  cudaSuccess || sms < 1)

@@ -174,6 +174,9 @@ struct W4a16Args {
   DebugKnobs dbg;
 };
 int w4a16_chunks_per_split(int K, int n_split);
+// True when M (and K) select the CUDA-core matrix-vector path: one pass over K per
+// output row, no split and no workspace.
+bool w4a16_uses_gemv(int M, int K);
 cudaError_t launch_w4a16(const W4a16Args& a, cudaStream_t stream);
 
 cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int cols,

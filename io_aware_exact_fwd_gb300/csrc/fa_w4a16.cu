@@ -17,17 +17,21 @@
 //  * warp 0 loads, by TMA, the packed 128 x 256 weight tile (16 KB), the chunk's
 //    activations X[:, k0:k0+256] (four 64-column boxes, rows past M zero-filled)
 //    and the two groups' scales and zero points into a ring of stages;
-//  * eight dequantising warps (thread = weight row = TMEM lane; warpgroup g takes
-//    group g of the chunk) turn each word into four fp16 pairs -- one shift, one
-//    mask-and-or with 0x6400 (1024 + code as fp16), one subtraction of 1024 + z
-//    (exact), one multiplication by s (the only rounding) -- and store them to
-//    TMEM, two fp16 per column, as the A operand of the MMA;
-//  * one thread issues tcgen05.mma kind::f16 with A from TMEM (128 rows x 16 k)
-//    and B = X from shared memory (K-major, 128-byte swizzle), accumulating
-//    Y^T[128 rows x M] in TMEM; three A buffers let the dequantisation of the
-//    next chunks overlap the MMAs of this one;
-//  * after the unit's last chunk, warpgroup 0 reads Y^T out of TMEM and writes
-//    fp16 Y (one split) or fp32 partials (several), coalesced along n.
+//  * two sets of eight dequantising warps take alternate chunks (thread = weight
+//    row = TMEM lane; warpgroup g of a set takes group g of the chunk).  Each word
+//    becomes four fp16 pairs: the pair's two codes are masked into the mantissa
+//    of 1024.0 (bits 0-3 and 16-19) or of 64.0 (bits 4-7 and 20-23, whose weight
+//    there is 1), so one shift serves the word's upper byte pair; then one exact
+//    subtraction of 1024 + z or 64 + z and one multiplication by s (the only
+//    rounding).  The pairs go to TMEM, two fp16 per column, as the MMA's A operand;
+//  * two threads issue tcgen05.mma kind::f16, one per 128-wide group of the chunk,
+//    A from TMEM (128 rows x 16 k) and B = X from shared memory (K-major, 128-byte
+//    swizzle), each accumulating its share of Y^T[128 rows x M] in its own TMEM
+//    columns; three A buffers let the dequantisation of the next chunks overlap
+//    the MMAs of this one;
+//  * after the unit's last chunk, warpgroup 0 of the set that unpacked it adds the
+//    two accumulators and writes fp16 Y (one split) or fp32 partials (several),
+//    coalesced along n.
 // Every wait is bounded, as in the attention kernels.
 #include <cuda_fp16.h>
 
@@ -37,7 +41,8 @@
 namespace fa {
 namespace {
 
-constexpr int kW4Threads = 384;  // 0 TMA, 1-2 MMA issuers (1 owns TMEM), 3 idle, 4-11 dequantisation
+constexpr int kW4Sets = 2;       // dequantising warp sets, alternate chunks
+constexpr int kW4Threads = 128 + 256 * kW4Sets;  // 0 TMA, 1-2 MMA issuers (1 owns TMEM), 3 idle, then the sets
 constexpr int kW4Rows = 128;     // output rows per unit (MMA M, TMEM lanes)
 constexpr int kW4Kc = 256;       // K per chunk: two groups of 128
 constexpr uint32_t kW4TmemCols = 512;
@@ -116,7 +121,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 8 + 2);  // eight dequantising warps + both issuers' commits
+      mbar_init(&bar_empty[s], 8 + 2);  // the eight dequantising warps of the item's set + both issuers' commits
     }
     for (int b = 0; b < C::kA; ++b) {
       mbar_init(&bar_afull[2 * b], 4);
@@ -205,7 +210,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------ dequantisation (thread = weight row)
-    const int g = (warp - 4) >> 2;           // group of the chunk this warpgroup unpacks
+    const int set = (warp - 4) >> 3;         // this set unpacks items with item % kW4Sets == set
+    const int g = ((warp - 4) >> 2) & 1;     // group of the chunk this warpgroup unpacks
     const int r = ((warp & 3) << 5) + lane;  // row within the 128-row tile
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     int item = 0, units = 0;
@@ -215,6 +221,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       unit_range(w, strip, c0, c1);
       if (c1 <= c0) continue;
       for (int c = c0; ok && c < c1; ++c, ++item) {
+        if (item % kW4Sets != set) continue;
         const int slot = item % C::kStages;
         const int b = item % C::kA;
         if (!(ok = w4_warp_wait(&bar_full[slot], (item / C::kStages) & 1, wc, kSiteW4Deq))) break;
@@ -225,8 +232,10 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         const __half s = reinterpret_cast<const __half*>(st + C::kOffS)[g * kW4Rows + r];
         const int z = st[C::kOffZ + g * kW4Rows + r];
         const __half2 s2 = __halves2half2(s, s);
-        const __half zb = __int2half_rn(1024 + z);  // exact: an integer below 2048
+        const __half zb = __int2half_rn(1024 + z);  // exact: integers below 2048
         const __half2 zb2 = __halves2half2(zb, zb);
+        const __half zs = __int2half_rn(64 + z);
+        const __half2 zs2 = __halves2half2(zs, zs);
         // This warpgroup's 16 words of the row: 16-byte chunks 4g .. 4g+3 of the
         // 128-byte swizzled row.
         const uint8_t* wrow = st + r * 128;
@@ -242,10 +251,12 @@ __global__ void __launch_bounds__(kW4Threads, 1)
             for (int e = 0; e < 4; ++e) {
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                // Codes of k = 8w + 2i (bits 4i..) and 8w + 2i + 1 (bits 4i + 16..) as
-                // fp16 1024 + code, then (code - z) exactly, then times s.
-                const uint32_t t = ((wd[e] >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
-                const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&t), zb2);
+                // Codes of k = 8w + 2i (bits 4i..) and 8w + 2i + 1 (bits 4i + 16..).
+                // Even i: mantissa bits 0-3 of 1024.0 (value 1024 + code); odd i: bits
+                // 4-7 of 64.0 (value 64 + code).  Then (code - z) exactly, then times s.
+                const uint32_t src = i < 2 ? wd[e] : (wd[e] >> 8);
+                const uint32_t t = (i & 1) ? ((src & 0x00F000F0u) | 0x54005400u) : ((src & 0x000F000Fu) | 0x64006400u);
+                const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&t), (i & 1) ? zs2 : zb2);
                 const __half2 wv = __hmul2(d, s2);
                 out[(ch * 4 + e) * 4 + i] = *reinterpret_cast<const uint32_t*>(&wv);
               }
@@ -262,8 +273,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         }
       }
       if (!ok) break;
-      if (g == 0) {
-        // ------------------------------------------------- epilogue (warpgroup 0)
+      if (g == 0 && (item - 1) % kW4Sets == set) {
+        // ------------------- epilogue (warpgroup 0 of the set that unpacked the last chunk)
         if (!(ok = w4_warp_wait(bar_dfull, units & 1, wc, kSiteW4Epi))) break;
         tc_fence_after();
         const int n = strip * kW4Rows + r;
@@ -305,6 +316,163 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kW4TmemCols);
   }
+}
+
+// ------------------------------------------------------------------------------
+// One token (M = 1): the product is a matrix-vector stream, HBM-bound work that the
+// tensor cores only slow down here (each M=128 x K=16 MMA covers 2048 weights and
+// its dequantised A operand has to pass through TMEM; measured, that path issues
+// one MMA per ~96 cycles per SM while the TMEM stores run, below the HBM rate).
+// Here the dequantised weights go straight from registers into mixed-precision
+// FMAs (fp16 x fp16 products, exact in fp32, summed in fp32).
+//
+// CTA = 8 warps x 4 rows = 32 output rows; it stages the rows' scales and zero
+// points for all groups in shared memory (one coalesced pass), then each warp
+// streams its 4 rows: per step, lane l takes words 4l .. 4l+3 of a 128-word block
+// of every row (one 16-byte streaming load per row) and the 32 activations they
+// multiply (16-byte loads, L1-resident, shared by the 4 rows).  The dequantisation
+// is the tensor path's, bit for bit.  A warp reduction finishes each row.
+constexpr int kGvWarps = 8;
+constexpr int kGvRowsPerWarp = 4;
+constexpr int kGvRows = kGvWarps * kGvRowsPerWarp;
+constexpr int kGvMaxM = 1;  // measured: from M = 2 the tensor-core path is faster
+
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// acc += lo(w) * lo(x) + hi(w) * hi(x): fp16 operands, fp32 product and sum.
+__device__ __forceinline__ float fma2_f16_f32(uint32_t w, uint32_t x, float acc) {
+  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %1;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.f16 %0, wh, xh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w), "r"(x));
+  return acc;
+}
+
+template <int MP>
+__global__ void __launch_bounds__(kGvWarps * 32) w4a16_gemv_kernel(const __half* __restrict__ x,
+                                                                    const uint32_t* __restrict__ wq,
+                                                                    const __half* __restrict__ scales,
+                                                                    const uint8_t* __restrict__ zeros,
+                                                                    __half* __restrict__ y, int M, int N, int K) {
+  extern __shared__ __align__(16) uint8_t gv_smem[];
+  const int G = K / 128;
+  __half* s_sm = reinterpret_cast<__half*>(gv_smem);  // [G][32]
+  uint8_t* z_sm = gv_smem + static_cast<size_t>(G) * kGvRows * 2;  // [G][32]
+  const int n0 = blockIdx.x * kGvRows;
+  for (int i = threadIdx.x; i < G * kGvRows; i += blockDim.x) {
+    const int g = i / kGvRows, r = i % kGvRows, n = n0 + r;
+    s_sm[i] = n < N ? scales[static_cast<size_t>(g) * N + n] : __float2half(0.f);
+    z_sm[i] = n < N ? zeros[static_cast<size_t>(g) * N + n] : 0;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rb = warp * kGvRowsPerWarp;  // first of this warp's rows within the CTA
+  const int W = K / 8;                   // words per row (a multiple of 32)
+  const uint32_t* wrow[kGvRowsPerWarp];
+#pragma unroll
+  for (int r = 0; r < kGvRowsPerWarp; ++r)  // rows past N (N % 32 == 16) re-read row N - 1, never stored
+    wrow[r] = wq + static_cast<size_t>(min(n0 + rb + r, N - 1)) * W;
+  float acc[kGvRowsPerWarp][MP];
+#pragma unroll
+  for (int r = 0; r < kGvRowsPerWarp; ++r)
+#pragma unroll
+    for (int m = 0; m < MP; ++m) acc[r][m] = 0.f;
+
+  // Lane l's words of block j are 128 j + 4 l .. +3 (the last block of a row may be
+  // short: W is a multiple of 32).  The next block's words are loaded before this
+  // block's arithmetic, so every lane keeps one block of loads in flight.
+  uint4 nxt[kGvRowsPerWarp];
+  if (4 * lane < W) {
+#pragma unroll
+    for (int r = 0; r < kGvRowsPerWarp; ++r) nxt[r] = ldg_stream16(wrow[r] + 4 * lane);
+  }
+  for (int wi = 4 * lane; wi < W; wi += 128) {
+    uint4 wv[kGvRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kGvRowsPerWarp; ++r) wv[r] = nxt[r];
+    if (wi + 128 < W) {
+#pragma unroll
+      for (int r = 0; r < kGvRowsPerWarp; ++r) nxt[r] = ldg_stream16(wrow[r] + wi + 128);
+    }
+    uint32_t xv[MP][16];  // x[m][8 wi .. 8 wi + 31] as fp16 pairs
+#pragma unroll
+    for (int m = 0; m < MP; ++m) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 t = make_uint4(0u, 0u, 0u, 0u);
+        if (m < M) t = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(m) * K + 8 * wi) + q);
+        xv[m][4 * q] = t.x;
+        xv[m][4 * q + 1] = t.y;
+        xv[m][4 * q + 2] = t.z;
+        xv[m][4 * q + 3] = t.w;
+      }
+    }
+    const int g = wi / 16;  // the 4 words share one group of 128
+#pragma unroll
+    for (int r = 0; r < kGvRowsPerWarp; ++r) {
+      const __half s = s_sm[g * kGvRows + rb + r];
+      const int z = z_sm[g * kGvRows + rb + r];
+      const __half2 s2 = __halves2half2(s, s);
+      const __half zb = __int2half_rn(1024 + z), zs = __int2half_rn(64 + z);
+      const __half2 zb2 = __halves2half2(zb, zb), zs2 = __halves2half2(zs, zs);
+      const uint32_t wd[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t src = i < 2 ? wd[e] : (wd[e] >> 8);
+          const uint32_t t = (i & 1) ? ((src & 0x00F000F0u) | 0x54005400u) : ((src & 0x000F000Fu) | 0x64006400u);
+          const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&t), (i & 1) ? zs2 : zb2);
+          const __half2 wh = __hmul2(d, s2);
+          const uint32_t w2 = *reinterpret_cast<const uint32_t*>(&wh);
+#pragma unroll
+          for (int m = 0; m < MP; ++m) acc[r][m] = fma2_f16_f32(w2, xv[m][4 * e + i], acc[r][m]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kGvRowsPerWarp; ++r) {
+#pragma unroll
+    for (int m = 0; m < MP; ++m) {
+      float v = acc[r][m];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      acc[r][m] = v;
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int r = 0; r < kGvRowsPerWarp; ++r) {
+      const int n = n0 + rb + r;
+#pragma unroll
+      for (int m = 0; m < MP; ++m)
+        if (n < N && m < M) y[static_cast<size_t>(m) * N + n] = __float2half_rn(acc[r][m]);
+    }
+  }
+}
+
+template <int MP>
+cudaError_t launch_gemv(const W4a16Args& a, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(a.K / 128) * kGvRows * 3;
+  auto kern = w4a16_gemv_kernel<MP>;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)))) return e;
+  const unsigned blocks = static_cast<unsigned>((a.N + kGvRows - 1) / kGvRows);
+  kern<<<blocks, kGvWarps * 32, smem, stream>>>(static_cast<const __half*>(a.x), static_cast<const uint32_t*>(a.wq),
+                                               static_cast<const __half*>(a.scales),
+                                               static_cast<const uint8_t*>(a.zeros), static_cast<__half*>(a.y), a.M,
+                                               a.N, a.K);
+  return cudaGetLastError();
 }
 
 // Y = fp16(sum_s partials[s]), in split order (the same bits on every run).
@@ -360,7 +528,10 @@ int w4a16_chunks_per_split(int K, int n_split) {
   return (kchunks + n_split - 1) / n_split;
 }
 
+bool w4a16_uses_gemv(int M, int K) { return M <= kGvMaxM && K <= 65536; }
+
 cudaError_t launch_w4a16(const W4a16Args& a, cudaStream_t stream) {
+  if (w4a16_uses_gemv(a.M, a.K)) return launch_gemv<1>(a, stream);
   if (a.M <= 16) return launch_mp<16>(a, stream);
   if (a.M <= 32) return launch_mp<32>(a, stream);
   if (a.M <= 64) return launch_mp<64>(a, stream);

@@ -144,9 +144,12 @@ def test_w4a16_validation_statuses(lib):
     assert g(M=-1) == 1
     assert g(M=0) == 0
     assert g(y=FAKE + 8) == 3
-    assert g(K=1024, n=4) == 6                    # splits need a workspace
-    assert lib.fa_w4a16_workspace_size(4, 128, 1024, 4) == 4 * 4 * 128 * 4
-    assert lib.fa_w4a16_workspace_size(4, 128, 1024, 1) == 0
+    assert g(M=2, K=1024, n=4) == 6               # splits of the tensor-core path need a workspace
+    assert lib.fa_w4a16_workspace_size(8, 128, 1024, 4) == 4 * 8 * 128 * 4
+    assert lib.fa_w4a16_workspace_size(8, 128, 1024, 1) == 0
+    # M = 1: the matrix-vector path, one pass over K per row, never a workspace.
+    assert lib.fa_w4a16_workspace_size(1, 128, 1024, 4) == 0
+    assert lib.fa_w4a16_default_splits(1, 28672, 8192) == 1
 
 
 def test_fp8_backward_validation_statuses(lib):

@@ -60,6 +60,26 @@ def test_matches_oracle(M, N, K, n_split):
     _check(y, d, K)
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 16, 256), (1, 48, 768), (1, 272, 1280), (1, 1024, 4096), (1, 32, 65536),
+                                   (2, 80, 65536), (1, 96, 65792), (3, 272, 1280), (4, 48, 768)])
+def test_matrix_vector_path_matches_oracle(M, N, K):
+    # M = 1 runs on the CUDA cores (K <= 65536): ragged last row block (N % 32 == 16),
+    # rows shorter than one 128-word step (K = 256, 768) and of one step plus a part
+    # (K = 1280), the largest K of the path and one K just past it (tensor-core path);
+    # small M > 1 on the tensor-core path beside them.
+    y, d = _run(M, N, K, 7 * M + N + K)
+    _check(y, d, K)
+
+
+def test_matrix_vector_path_is_deterministic():
+    d = w4a16_inputs(1, 4096, 8192, 9)
+    dev = {k: v.cuda() for k, v in d.items()}
+    a = fa.fa_w4a16_gemm(dev["x"], dev["wq"], dev["scales"], dev["zeros"])
+    b = fa.fa_w4a16_gemm(dev["x"], dev["wq"], dev["scales"], dev["zeros"], n_split=5)
+    fa.fa_sync_check()
+    assert torch.equal(a, b)
+
+
 def test_deterministic_with_splits():
     d = w4a16_inputs(16, 1024, 8192, 7)
     dev = {k: v.cuda() for k, v in d.items()}
