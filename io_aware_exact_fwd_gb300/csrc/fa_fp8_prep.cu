@@ -40,43 +40,43 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   return r;
 }
 
-// Load 4 (d=128) or 2 (d=64) consecutive elements of one row as fp32.
-template <int D>
-__device__ __forceinline__ void load_row(const void* base, size_t elem0, int in_bf16, float (&x)[D / 32]) {
-  constexpr int E = D / 32;
+// Load 16 consecutive elements of one row as fp32 (bf16: two 16-byte loads; fp32: four).
+__device__ __forceinline__ void load16(const void* base, size_t elem0, int in_bf16, float (&x)[16]) {
   if (in_bf16) {
-    const __nv_bfloat16* p = static_cast<const __nv_bfloat16*>(base) + elem0;
-    if (E == 4) {
-      const uint2 u = *reinterpret_cast<const uint2*>(p);
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-      x[0] = a.x; x[1] = a.y; x[2 % E] = b.x; x[3 % E] = b.y;
-    } else {
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
-      x[0] = a.x; x[1 % E] = a.y;
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + elem0);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 u = p[h];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+        x[8 * h + 2 * j] = f.x;
+        x[8 * h + 2 * j + 1] = f.y;
+      }
     }
   } else {
-    const float* p = static_cast<const float*>(base) + elem0;
-    if (E == 4) {
-      const float4 a = *reinterpret_cast<const float4*>(p);
-      x[0] = a.x; x[1] = a.y; x[2 % E] = a.z; x[3 % E] = a.w;
-    } else {
-      const float2 a = *reinterpret_cast<const float2*>(p);
-      x[0] = a.x; x[1 % E] = a.y;
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem0);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float4 f = p[h];
+      x[4 * h] = f.x;
+      x[4 * h + 1] = f.y;
+      x[4 * h + 2] = f.z;
+      x[4 * h + 3] = f.w;
     }
   }
 }
 
-// In-place unnormalised Walsh-Hadamard transform of one row held as E = D/32
-// consecutive elements per lane (lane t holds elements E*t .. E*t+E-1).
+// In-place unnormalised Walsh-Hadamard transform of one row spread over D/16 lanes
+// of 16 consecutive elements (sl = the lane's index within its row): spans 1..8 in
+// the lane, then spans 16..D/2 with the partner lane sl ^ (span / 16).
 template <int D>
-__device__ __forceinline__ void fwht_row(float (&x)[D / 32], int lane) {
-  constexpr int E = D / 32;
-  // spans inside the lane
+__device__ __forceinline__ void fwht16(float (&x)[16], int sl) {
 #pragma unroll
-  for (int span = 1; span < E; span <<= 1) {
+  for (int span = 1; span < 16; span <<= 1) {
 #pragma unroll
-    for (int i = 0; i < E; ++i) {
+    for (int i = 0; i < 16; ++i) {
       if ((i & span) == 0) {
         const float a = x[i], b = x[i + span];
         x[i] = a + b;
@@ -84,13 +84,12 @@ __device__ __forceinline__ void fwht_row(float (&x)[D / 32], int lane) {
       }
     }
   }
-  // spans across lanes: partner lane = lane ^ (span / E)
 #pragma unroll
-  for (int span = E; span < D; span <<= 1) {
-    const int m = span / E;
-    const bool upper = (lane & m) != 0;  // this lane holds the "b" half
+  for (int span = 16; span < D; span <<= 1) {
+    const int m = span / 16;
+    const bool upper = (sl & m) != 0;  // this lane holds the "b" half
 #pragma unroll
-    for (int i = 0; i < E; ++i) {
+    for (int i = 0; i < 16; ++i) {
       const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
       x[i] = upper ? (other - x[i]) : (x[i] + other);
     }
@@ -188,29 +187,38 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
   }
 
   // ------------------------------------------------------ Q, K: rotate, then quantise
+  // A row is held by kL = d/16 lanes, 16 consecutive elements each (32-byte bf16 or
+  // 64-byte fp32 loads, one 16-byte store of codes): butterfly spans 1..8 stay in
+  // the lane, spans 16..d/2 pair lane l with lane l ^ (span / 16) of the same row.
   if (tile >= ntiles) return;  // blocks past the last tile exist only to pad V^T
-  float sgn[E];
+  constexpr int kE = 16;
+  constexpr int kL = D / kE;                            // lanes per row: 8 (d=128), 4 (d=64)
+  constexpr int kRowsPerPass = 32 / kL;                 // rows a warp holds at once
+  constexpr int kPasses = kRowsPerWarp / kRowsPerPass;  // 2 (d=128), 1 (d=64)
+  const int sl = lane % kL, rg = lane / kL;
+  float sg[kE];
 #pragma unroll
-  for (int i = 0; i < E; ++i) sgn[i] = signs[E * lane + i] < 0 ? -1.f : 1.f;
+  for (int i = 0; i < kE; ++i) sg[i] = signs[kE * sl + i] < 0 ? -1.f : 1.f;
   const void* src = which == 0 ? q : k;
+  float xr[kPasses][kE];
   float amax = 0.f;
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int row = tile * kTileRows + warp * kRowsPerWarp + r;
+  for (int p = 0; p < kPasses; ++p) {
+    const int row = tile * kTileRows + warp * kRowsPerWarp + p * kRowsPerPass + rg;
     if (row < N) {
-      load_row<D>(src, (static_cast<size_t>(bh) * N + row) * D + E * lane, in_bf16, x[r]);
+      load16(src, (static_cast<size_t>(bh) * N + row) * D + kE * sl, in_bf16, xr[p]);
     } else {
 #pragma unroll
-      for (int i = 0; i < E; ++i) x[r][i] = 0.f;
+      for (int i = 0; i < kE; ++i) xr[p][i] = 0.f;
     }
   }
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
+  for (int p = 0; p < kPasses; ++p) {
 #pragma unroll
-    for (int i = 0; i < E; ++i) x[r][i] *= sgn[i];
-    fwht_row<D>(x[r], lane);
+    for (int i = 0; i < kE; ++i) xr[p][i] *= sg[i];
+    fwht16<D>(xr[p], sl);
 #pragma unroll
-    for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(x[r][i]));
+    for (int i = 0; i < kE; ++i) amax = fmaxf(amax, fabsf(xr[p][i]));
   }
   amax = block_amax(amax, s_amax, warp, lane);
   float sigma, inv;
@@ -219,21 +227,18 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
     reinterpret_cast<float*>(ws + (which == 0 ? lay.off_sq : lay.off_sk))[static_cast<size_t>(bh) * ntiles + tile] =
         sigma;
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int row = tile * kTileRows + warp * kRowsPerWarp + r;
+  for (int p = 0; p < kPasses; ++p) {
+    const int row = tile * kTileRows + warp * kRowsPerWarp + p * kRowsPerPass + rg;
     if (row >= N) continue;
-    uint8_t c[E];
+    uint32_t wds[4];
 #pragma unroll
-    for (int i = 0; i < E; i += 2) {
-      const uint16_t two = e4m3x2(__fmul_rn(x[r][i], inv), __fmul_rn(x[r][i + 1], inv));
-      c[i] = static_cast<uint8_t>(two & 0xff);
-      c[i + 1] = static_cast<uint8_t>(two >> 8);
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = e4m3x2(__fmul_rn(xr[p][4 * j], inv), __fmul_rn(xr[p][4 * j + 1], inv));
+      const uint32_t hi = e4m3x2(__fmul_rn(xr[p][4 * j + 2], inv), __fmul_rn(xr[p][4 * j + 3], inv));
+      wds[j] = lo | (hi << 16);
     }
-    uint8_t* dst = ws + (which == 0 ? lay.off_q8 : lay.off_k8) + (static_cast<size_t>(bh) * N + row) * D + E * lane;
-    if (E == 4)
-      *reinterpret_cast<uint32_t*>(dst) = c[0] | (c[1 % E] << 8) | (c[2 % E] << 16) | (c[3 % E] << 24);
-    else
-      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(c[0] | (c[1 % E] << 8));
+    uint8_t* dst = ws + (which == 0 ? lay.off_q8 : lay.off_k8) + (static_cast<size_t>(bh) * N + row) * D + kE * sl;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
   }
 }
 
