@@ -17,7 +17,7 @@
 //      writing dQ', dK', dV into the caller's buffers;
 //   3. unrotate_kernel: dQ' and dK' rows through the fast Walsh-Hadamard
 //      transform in fp32 (butterfly spans 1..d/2), times the signs, back to bf16
-//      in place.
+//      in place (two rows per warp per pass, 16-byte accesses).
 //
 // Stages 1 and 3 are bound by HBM (stage 1 reads 3 N d bytes of codes and writes
 // 6 N d bytes of operands per head; stage 3 reads and writes 4 N d bytes); the
@@ -34,7 +34,7 @@ namespace {
 
 constexpr int kTile = 64;            // rows per quantisation tile (the FP8 prepare's)
 constexpr int kDeqThreads = 256;
-constexpr int kRotThreads = 256;     // 8 rows per block, one warp per row
+constexpr int kRotThreads = 256;
 
 // Two e4m3 codes (low byte -> low half) to two fp16 values: exact, every e4m3
 // value (subnormals included) is an fp16 value.
@@ -78,24 +78,46 @@ __global__ void __launch_bounds__(kDeqThreads) fp8_dequant_kernel(const uint8_t*
   const float sk = reinterpret_cast<const float*>(ws + lay.off_sk)[sidx];
   const float sv = reinterpret_cast<const float*>(ws + lay.off_sv)[sidx];
 
-  // Q and K: the tile's rows are contiguous, rows * D bytes (a multiple of 16).
+  // All of this thread's loads first (Q and K: the tile's rows are contiguous,
+  // rows * D bytes, a multiple of 16; V: 16-byte pieces of the tile's d rows of
+  // codes at v8t[bh][c][r0 ..], Npad >= r0 + 64, zero past N), then the arithmetic.
+  constexpr int kQK = kTile * D / 16 / kDeqThreads;  // 16-byte pieces per thread: 2 (d=128), 1 (d=64)
+  constexpr int kV = D * (kTile / 16) / kDeqThreads;
   const size_t base = (static_cast<size_t>(bh) * N + r0) * D;
-  for (int i = threadIdx.x * 16; i < rows * D; i += kDeqThreads * 16) {
-    dequant16(*reinterpret_cast<const uint4*>(ws + lay.off_q8 + base + i), sq, qr + base + i);
-    dequant16(*reinterpret_cast<const uint4*>(ws + lay.off_k8 + base + i), sk, kr + base + i);
-  }
-
-  // V: codes of columns c, rows r0 .. r0+63 sit at v8t[bh][c][r0 ..] (Npad >= r0 + 64,
-  // zero past N).  Stage [D][64] in shared memory, then read it back by rows.
   const uint8_t* v8t = ws + lay.off_v8t + static_cast<size_t>(bh) * D * lay.npad + r0;
-  for (int i = threadIdx.x; i < D * (kTile / 16); i += kDeqThreads) {
-    const int c = i / (kTile / 16), j = (i % (kTile / 16)) * 16;
-    const uint4 v = *reinterpret_cast<const uint4*>(v8t + static_cast<size_t>(c) * lay.npad + j);
-    *reinterpret_cast<uint4*>(&vt[c][j]) = v;
+  uint4 cq[kQK], ck[kQK], cv[kV];
+#pragma unroll
+  for (int j = 0; j < kQK; ++j) {
+    const int i = (threadIdx.x + j * kDeqThreads) * 16;
+    if (i < rows * D) {
+      cq[j] = *reinterpret_cast<const uint4*>(ws + lay.off_q8 + base + i);
+      ck[j] = *reinterpret_cast<const uint4*>(ws + lay.off_k8 + base + i);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kV; ++j) {
+    const int idx = threadIdx.x + j * kDeqThreads;
+    const int c = idx / (kTile / 16), jj = (idx % (kTile / 16)) * 16;
+    cv[j] = *reinterpret_cast<const uint4*>(v8t + static_cast<size_t>(c) * lay.npad + jj);
+  }
+#pragma unroll
+  for (int j = 0; j < kV; ++j) {
+    const int idx = threadIdx.x + j * kDeqThreads;
+    *reinterpret_cast<uint4*>(&vt[idx / (kTile / 16)][(idx % (kTile / 16)) * 16]) = cv[j];
+  }
+#pragma unroll
+  for (int j = 0; j < kQK; ++j) {
+    const int i = (threadIdx.x + j * kDeqThreads) * 16;
+    if (i < rows * D) {
+      dequant16(cq[j], sq, qr + base + i);
+      dequant16(ck[j], sk, kr + base + i);
+    }
   }
   __syncthreads();
+  // Consecutive lanes take consecutive rows of the same 16 columns, so each byte
+  // load of the warp touches 8 consecutive words of one column (no bank conflict).
   for (int i = threadIdx.x; i < kTile * (D / 16); i += kDeqThreads) {
-    const int r = i / (D / 16), c0 = (i % (D / 16)) * 16;
+    const int r = i % kTile, c0 = (i / kTile) * 16;
     if (r >= rows) continue;
     uint32_t w[4];
 #pragma unroll
@@ -107,42 +129,71 @@ __global__ void __launch_bounds__(kDeqThreads) fp8_dequant_kernel(const uint8_t*
 }
 
 // x <- bf16((x H_128) * s) per row of 128, for two tensors (blockIdx.y selects).
-// Lane l holds columns 4l .. 4l+3: butterfly spans 1 and 2 stay in the lane,
-// spans 4 .. 64 pair lane l with lane l ^ (span / 4).
+// Lane l holds 8 consecutive columns 8 (l % 16) .. +7 of a row (one 16-byte load),
+// so a warp holds two rows per pass; butterfly spans 1, 2, 4 stay in the lane and
+// spans 8 .. 64 pair lane l with lane l ^ (span / 8) of the same half-warp.  Each
+// warp takes kRotPasses passes (2 kRotPasses rows) and issues all their loads
+// before any arithmetic, to keep enough bytes in flight.
+constexpr int kRotPasses = 4;
+constexpr int kRotRowsPerWarp = 2 * kRotPasses;
+
 __global__ void __launch_bounds__(kRotThreads) unrotate_kernel(__nv_bfloat16* __restrict__ x0,
                                                                __nv_bfloat16* __restrict__ x1,
                                                                const int8_t* __restrict__ signs, long long rows) {
-  const long long r = static_cast<long long>(blockIdx.x) * (kRotThreads / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
-  __nv_bfloat16* row = (blockIdx.y == 0 ? x0 : x1) + r * 128 + 4 * lane;
-  const uint2 raw = *reinterpret_cast<const uint2*>(row);
-  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-  float v[4] = {a.x, a.y, b.x, b.y};
-  // span 1
-  float t0 = v[0] + v[1], t1 = v[0] - v[1], t2 = v[2] + v[3], t3 = v[2] - v[3];
-  // span 2
-  v[0] = t0 + t2;
-  v[2] = t0 - t2;
-  v[1] = t1 + t3;
-  v[3] = t1 - t3;
+  const int sl = lane & 15;  // the lane's index within its row
+  const long long r0 = (static_cast<long long>(blockIdx.x) * (kRotThreads / 32) + (threadIdx.x >> 5)) *
+                           kRotRowsPerWarp + (lane >> 4);
+  __nv_bfloat16* base = (blockIdx.y == 0 ? x0 : x1) + 8 * sl;
+  uint4 raw[kRotPasses];
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    const bool upper = (lane & m) != 0;
+  for (int p = 0; p < kRotPasses; ++p) {
+    const long long r = r0 + 2 * p;
+    raw[p] = r < rows ? *reinterpret_cast<const uint4*>(base + r * 128) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float s[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float p = __shfl_xor_sync(0xffffffffu, v[e], m);
-      v[e] = upper ? p - v[e] : v[e] + p;  // (a, b) -> (a + b, a - b), a the lower index
+  for (int e = 0; e < 8; ++e) s[e] = signs[8 * sl + e] < 0 ? -1.f : 1.f;
+#pragma unroll
+  for (int p = 0; p < kRotPasses; ++p) {
+    const uint32_t w[4] = {raw[p].x, raw[p].y, raw[p].z, raw[p].w};
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+      v[2 * j] = f.x;
+      v[2 * j + 1] = f.y;
+    }
+#pragma unroll
+    for (int span = 1; span < 8; span <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if ((e & span) == 0) {
+          const float a = v[e], b = v[e + span];
+          v[e] = a + b;
+          v[e + span] = a - b;
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) {
+      const bool upper = (sl & m) != 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[e], m);
+        v[e] = upper ? o - v[e] : v[e] + o;  // (a, b) -> (a + b, a - b), a the lower index
+      }
+    }
+    const long long r = r0 + 2 * p;
+    if (r < rows) {
+      uint4 out;
+      out.x = pack_bf16x2(v[0] * s[0], v[1] * s[1]);
+      out.y = pack_bf16x2(v[2] * s[2], v[3] * s[3]);
+      out.z = pack_bf16x2(v[4] * s[4], v[5] * s[5]);
+      out.w = pack_bf16x2(v[6] * s[6], v[7] * s[7]);
+      *reinterpret_cast<uint4*>(base + r * 128) = out;
     }
   }
-  float s[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) s[e] = signs[4 * lane + e] < 0 ? -1.f : 1.f;
-  uint2 out;
-  out.x = pack_bf16x2(v[0] * s[0], v[1] * s[1]);
-  out.y = pack_bf16x2(v[2] * s[2], v[3] * s[3]);
-  *reinterpret_cast<uint2*>(row) = out;
 }
 
 }  // namespace
@@ -163,7 +214,7 @@ cudaError_t launch_fp8_dequant(const void* fp8_ws, void* qr, void* kr, void* vr,
 }
 
 cudaError_t launch_fp8_unrotate(void* dq, void* dk, const int8_t* signs, long long rows, cudaStream_t stream) {
-  const int per_block = kRotThreads / 32;
+  const int per_block = (kRotThreads / 32) * kRotRowsPerWarp;
   const dim3 grid(static_cast<unsigned>((rows + per_block - 1) / per_block), 2);
   unrotate_kernel<<<grid, kRotThreads, 0, stream>>>(static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
                                                     signs, rows);
