@@ -17,9 +17,11 @@ Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides.  L2 (129 MB) is flushed before every
 step by writing a 256 MB buffer outside the per-step CUDA-event pairs; device
 time is the sum of the per-step event pairs on the launching stream, max over
-ranks.  `e2e` repeats the step through the same public call with the inputs in
-pinned host memory: the H2D copies of Q, K, V, the kernel and the D2H copies of
-O, LSE, dQ, dK and dV are all inside its timed region.
+ranks.  `e2e` repeats the step through the same public calls with the inputs in
+pinned host memory: every step copies Q, K, V and dO in and O, LSE, dQ, dK, dV and the
+FP8 O and LSE out, all inside its timed region.  The copies run on their own streams
+and overlap the neighbouring steps' kernels (double-buffered), as a serving or
+training loop would overlap them.
 
 Under torchrun (N > 1) every rank runs the same independent replica (the heads
 shard with no exchange, so there is no collective on the data path) and rank 0
@@ -252,37 +254,63 @@ def run_ours(args):
     ms_per_step = dev_ms / args.steps
     value = whole_job_tflops(flops_step, args.steps, world, dev_ms)
 
-    # End to end through the public calls: pinned host inputs in, every output back out.
+    # End to end through the public calls: pinned host inputs in, every output back
+    # out, every step.  Pipelined over three streams: while step i computes, the
+    # inputs of step i + 1 are copied in and the outputs of step i - 1 copied out
+    # (two sets of device inputs, device outputs and pinned host outputs; events
+    # order each set's reuse).  The timed region runs from the first step's first
+    # input copy to the last step's last output copy.
     hq, hk, hv, hg = (t.cpu().pin_memory() for t in (q, k, v, g))
-    dq_in, dk_in, dv_in, dg_in = (torch.empty_like(t) for t in (q, k, v, g))
+    h_in = (hq, hk, hv, hg)
     e2e_steps = max(3, min(args.steps, 50))
-
-    outs = (o, lse, dq, dk, dv, o8, lse8)
-    houts = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
-
-    def e2e_step():
-        for dst, src in zip((dq_in, dk_in, dv_in, dg_in), (hq, hk, hv, hg)):
-            dst.copy_(src, non_blocking=True)
-        fa.fa_fwd(dq_in, dk_in, dv_in, o=o, lse=lse, causal=causal, scale=scale)
-        fa.fa_bwd(dq_in, dk_in, dv_in, o, dg_in, lse, dq, dk, dv, ws, causal=causal, scale=scale)
-        fa.fa_fp8_prepare(dq_in, dk_in, dv_in, signs, ws8)
-        fa.fa_fwd_fp8(ws8, (B, H, N, d), o=o8, lse=lse8, causal=causal, scale=scale)
-        for dst, src in zip(houts, outs):
-            dst.copy_(src, non_blocking=True)
-
+    s_h2d, s_comp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    sets = []
     for _ in range(2):
-        e2e_step()
+        din = [torch.empty_like(t) for t in (q, k, v, g)]
+        dout = [torch.empty_like(q), torch.empty_like(lse), torch.empty_like(q), torch.empty_like(k),
+                torch.empty_like(v), torch.empty_like(q), torch.empty_like(lse)]  # o, lse, dq, dk, dv, o8, lse8
+        hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dout]
+        ev = {n: torch.cuda.Event() for n in ("in_ready", "in_free", "out_ready", "out_free")}
+        sets.append((din, dout, hout, ev))
+
+    def e2e_step(i):
+        din, dout, hout, ev = sets[i % 2]
+        with torch.cuda.stream(s_h2d):
+            if i >= 2:
+                s_h2d.wait_event(ev["in_free"])  # step i - 2 has finished reading these inputs
+            for dst, src in zip(din, h_in):
+                dst.copy_(src, non_blocking=True)
+            ev["in_ready"].record(s_h2d)
+        s_comp.wait_event(ev["in_ready"])
+        if i >= 2:
+            s_comp.wait_event(ev["out_free"])  # step i - 2's outputs have been copied out
+        qi, ki, vi, gi = din
+        o_, lse_, dq_, dk_, dv_, o8_, lse8_ = dout
+        fa.fa_fwd(qi, ki, vi, o=o_, lse=lse_, causal=causal, scale=scale, stream=s_comp)
+        fa.fa_bwd(qi, ki, vi, o_, gi, lse_, dq_, dk_, dv_, ws, causal=causal, scale=scale, stream=s_comp)
+        fa.fa_fp8_prepare(qi, ki, vi, signs, ws8, stream=s_comp)
+        fa.fa_fwd_fp8(ws8, (B, H, N, d), o=o8_, lse=lse8_, causal=causal, scale=scale, stream=s_comp)
+        ev["in_free"].record(s_comp)
+        ev["out_ready"].record(s_comp)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev["out_ready"])
+            for dst, src in zip(hout, dout):
+                dst.copy_(src, non_blocking=True)
+            ev["out_free"].record(s_d2h)
+
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_h2d)
+    for i in range(2, 2 + e2e_steps):
+        e2e_step(i)
+    e1.record(s_d2h)
     torch.cuda.synchronize()
     fa.fa_sync_check()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
-    d2h = sum(t.numel() * t.element_size() for t in houts)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, "cuda")
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in sets[0][2])
 
     nxt = (next_rows(fa, q, k, v, g, o, lse, dq, dk, dv, ws, causal, scale, stage_ms, (ws8, signs, o8, lse8))
            if rank == 0 else None)
