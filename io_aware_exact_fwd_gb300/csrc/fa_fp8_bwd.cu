@@ -14,7 +14,9 @@
 //      rounded to bf16, into dense [BH, N, d] operands; V's codes are stored
 //      transposed ([BH, d, Npad]) and are transposed back through shared memory.
 //   2. the bf16 backward (fa_bwd.cu) on those operands with softmax scale scale/d,
-//      writing dQ', dK', dV into the caller's buffers;
+//      writing dQ', dK', dV into the caller's buffers (on request the bf16 forward
+//      first recomputes O and LSE from the same operands, so that the backward's
+//      D = rowsum(dO * O) uses the unrounded probabilities);
 //   3. unrotate_kernel: dQ' and dK' rows through the fast Walsh-Hadamard
 //      transform in fp32 (butterfly spans 1..d/2), times the signs, back to bf16
 //      in place (two rows per warp per pass, 16-byte accesses).
