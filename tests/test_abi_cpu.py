@@ -150,6 +150,12 @@ def test_w4a16_validation_statuses(lib):
     # M = 1: the matrix-vector path, one pass over K per row, never a workspace.
     assert lib.fa_w4a16_workspace_size(1, 128, 1024, 4) == 0
     assert lib.fa_w4a16_default_splits(1, 28672, 8192) == 1
+    # Tensor-core path: splits of at least 4 chunks of 256, never more than K allows.
+    for M, N, K in ((16, 28672, 8192), (16, 8192, 28672), (128, 4096, 4096), (2, 256, 1024)):
+        n = lib.fa_w4a16_default_splits(M, N, K)
+        assert 1 <= n <= max(1, K // 1024), (M, N, K, n)
+    assert lib.fa_w4a16_default_splits(0, 128, 256) == 0
+    assert lib.fa_w4a16_default_splits(4, 120, 256) == 0
 
 
 def test_fp8_backward_validation_statuses(lib):
