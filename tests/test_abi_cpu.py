@@ -180,3 +180,18 @@ def test_fp8_backward_validation_statuses(lib):
     assert g(n=0) == 0
     assert lib.fa_fp8_dequantize(vp(FAKE), f8, vp(FAKE + 8), vp(FAKE), vp(FAKE), B, H, N, d, vp(0)) == 3
     assert lib.fa_fp8_dequantize(vp(0), f8, vp(FAKE), vp(FAKE), vp(FAKE), B, H, N, d, vp(0)) == 6
+
+
+def test_header_is_plain_c(tmp_path):
+    # The boundary is a C ABI: the header must compile as strict C99 with no C++.
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_fa.c"
+    src.write_text('#include "fa.h"\nint main(void) { return fa_version() == 0; }\n')
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-c", str(src), "-o", str(tmp_path / "use_fa.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
