@@ -140,3 +140,30 @@ def test_fp8_forward_config_sampled_heads(causal):
         assert float(np.abs(lse[b, h, rows].cpu().numpy() - ld).max()) <= 1e-2
     assert max(errs_deq) <= FP8_RMSE_REL, errs_deq
     assert max(errs_exact) <= 1e-1, errs_exact
+
+
+def test_prepare_extreme_tiles_bit_exact():
+    # Tile scales at the ends of the power-of-two rule: an all-zero tile (scale 1), a
+    # tile near the fp32 maximum (V: amax 3e38, exponent 120), a tile whose amax is an
+    # fp32 subnormal (exponent clamped to -126), and huge / tiny rotated Q and K tiles.
+    B, H, N, d = 1, 1, 320, 128
+    g = torch.Generator().manual_seed(11)
+    q, k, v = (torch.randn(B, H, N, d, generator=g) for _ in range(3))
+    for t in (q, k, v):
+        t[..., 0:64, :] = 0.0
+    q[..., 64:128, :] *= 1e30
+    k[..., 128:192, :] *= 1e-30
+    v[..., 64:128, :] = torch.sign(v[..., 64:128, :]) * 3e38
+    v[..., 128:192, :] = torch.sign(v[..., 128:192, :]) * 1e-40
+    s = rotation_signs(d, seed=11)
+    ws = fa.fa_fp8_prepare(q.cuda(), k.cuda(), v.cuda(), s.cuda())
+    fa.fa_sync_check()
+    ref = fp8_prepare(q, k, v, s.numpy())
+    q8, k8, v8t, sq, sk, sv, npad = _regions(ws, B, H, N, d)
+    np.testing.assert_array_equal(sq, ref["sq"])
+    np.testing.assert_array_equal(sk, ref["sk"])
+    np.testing.assert_array_equal(sv, ref["sv"])
+    assert sv[0, 0, 0] == 1.0 and sv[0, 0, 1] == np.float32(2.0 ** 120) and sv[0, 0, 2] == np.float32(2.0 ** -126)
+    np.testing.assert_array_equal(q8, ref["q8"])
+    np.testing.assert_array_equal(k8, ref["k8"])
+    np.testing.assert_array_equal(v8t[..., :N], np.swapaxes(ref["v8"], -1, -2))
