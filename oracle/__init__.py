@@ -7,11 +7,11 @@ check it against the pages by eye:
 * ``attention``  -- the textbook definition O = softmax(scale * Q K^T [+causal]) V,
   the per-row logsumexp, and the analytic backward (dQ, dK, dV).  Source of the
   definition: "FlashAttention-2 (DE)", section "Hintergrund: Das Attention-Problem
-  in Transformern" (standard self-attention, O(N^2) time and memory), and the
-  exactness claim in the article's lead ("exakt identisch ... ohne
-  Genauigkeitsverlust") and in "Leistung und Effizienz" ("exakt und
-  deterministisch").  The tiled method reaches this same result, so the oracle is
-  the definition itself, never an online or tiled softmax.
+  in Transformern" (standard self-attention, O(N^2) time and memory); the
+  article's lead and its section "Leistung und Effizienz" state that the tiled
+  method loses no accuracy against it (the same result up to rounding, and a
+  deterministic one).  So the oracle is the definition itself, never an online or
+  tiled softmax.
 * ``brute``      -- a scalar triple-loop twin of ``attention`` for tiny inputs.
 * ``splitkv``    -- attention partials over key ranges and their exact merge
   (LSE = ln sum_s exp LSE_s, O = sum_s exp(LSE_s - LSE) O_s), with causal
@@ -67,6 +67,8 @@ from .fp8 import (
     fp8_prepare,
     fp8_dequantize,
     pow2_scale_exponent,
+    splitmix64,
+    seeded_rotation_signs,
     E4M3_MAX,
 )
 from .fp8_backward import (
@@ -102,6 +104,8 @@ __all__ = [
     "fp8_prepare",
     "fp8_dequantize",
     "pow2_scale_exponent",
+    "splitmix64",
+    "seeded_rotation_signs",
     "E4M3_MAX",
     "bf16_round",
     "fp8_dequantize_bf16",

@@ -198,3 +198,38 @@ def fp8_dequantize(codes: np.ndarray, sigma: np.ndarray, tile: int = 64) -> np.n
     N = codes.shape[-2]
     rows_tile = np.arange(N) // tile
     return vals * sigma.astype(np.float64)[..., rows_tile][..., None]
+
+
+# --------------------------------------------------- seeded rotation signs
+#
+# When the caller gives a 64-bit seed instead of a sign vector, the signs come
+# from SplitMix64 (G. L. Steele, D. Lea, C. H. Flood, "Fast splittable
+# pseudorandom number generators", OOPSLA 2014; the generator as published in its
+# reference implementation): state x starts at the seed; each output adds the
+# constant 0x9E3779B97F4A7C15 to x (mod 2^64) and returns the mixed value
+#     z = x;  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9;
+#     z = (z ^ (z >> 27)) * 0x94D049BB133111EB;  z ^ (z >> 31)      (mod 2^64).
+# Output c (0-based) thus depends only on (seed, c): the generator is counter-based.
+# Column c's sign is -1 when the top bit of output c is set, else +1.  This is the
+# library's definition of the seeded rotation; the library implements it in its own code.
+
+_MASK64 = (1 << 64) - 1
+_SPLITMIX_GAMMA = 0x9E3779B97F4A7C15
+
+
+def splitmix64(seed: int, count: int) -> list[int]:
+    """The first ``count`` SplitMix64 outputs from state ``seed`` (Python integers, exact)."""
+    x = seed & _MASK64
+    out = []
+    for _ in range(count):
+        x = (x + _SPLITMIX_GAMMA) & _MASK64
+        z = x
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _MASK64
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _MASK64
+        out.append(z ^ (z >> 31))
+    return out
+
+
+def seeded_rotation_signs(seed: int, d: int) -> np.ndarray:
+    """The +-1 signs (int8 [d]) of the seeded rotation: sign of column c from output c's top bit."""
+    return np.array([-1 if (z >> 63) else 1 for z in splitmix64(seed, d)], dtype=np.int8)

@@ -184,3 +184,27 @@ def test_fp8_input_quantisation_error_floor():
     o_v, _ = attention_forward(x["q"], x["k"], vd, scale, False)
     assert 0.015 < _rel_rmse(o_v, o_ref) < 0.035
     assert 0.03 < _rel_rmse(o_q, o_ref) < 0.10
+
+
+def test_splitmix64_reproduces_published_outputs():
+    # The seeded rotation's generator against outputs published for SplitMix64.
+    from oracle import splitmix64
+
+    with open(os.path.join(os.path.dirname(__file__), "golden", "splitmix64.json")) as f:
+        gold = json.load(f)
+    for seq in gold["sequences"]:
+        want = [int(h, 16) for h in seq["outputs_hex"]] if "outputs_hex" in seq else [int(x) for x in seq["outputs_dec"]]
+        assert splitmix64(seq["seed"], len(want)) == want
+
+
+def test_seeded_signs_follow_the_top_bit():
+    from oracle import seeded_rotation_signs, splitmix64
+
+    s = seeded_rotation_signs(0, 5)
+    # 0xe2..., 0x6e..., 0x06..., 0xf8..., 0x1b...: top bits 1, 0, 0, 1, 0.
+    assert s.tolist() == [-1, 1, 1, -1, 1]
+    for seed in (1, 2 ** 63 + 5, 2 ** 64 - 1):
+        s = seeded_rotation_signs(seed, 128)
+        assert s.dtype == np.int8 and set(s.tolist()) <= {-1, 1}
+        assert 32 < int((s < 0).sum()) < 96  # a fair coin: far outside this is a wrong bit
+        assert s.tolist() == [-1 if z >> 63 else 1 for z in splitmix64(seed, 128)]
