@@ -2,26 +2,33 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Workload (the configuration the headline metric is quoted on): bf16 attention,
-B=4, H=16, N=2048, d=128, scale 1/sqrt(d), non-causal, Q, K, V, dO ~ N(0,1) from
-seed 2.  One step = one pass of the whole hot path over that batch, six
-launches: the bf16 forward (fa_fwd), the backward's three stages (fa_bwd_prep,
-fa_bwd_main, fa_bwd_dq), and the FP8 path on the same Q, K, V (fa_fp8_prepare
-with seeded rotation signs, fa_fwd_fp8).  TFLOP/s counts 4*B*H*N^2*d per forward
-(bf16 or FP8) and 2.5 times that per backward.  `frac_of_peak` is the time the
-step's work would take at the measured peaks (bf16 FLOPs at the bf16 peak, FP8
-FLOPs at twice it, the nominal ratio) over the measured time.  Each stage is
-bracketed by its own CUDA events, which give the per-kernel rooflines.
+Headline workload: bf16 attention, B=2, H=16, N=8192, d=128, scale 1/sqrt(d),
+non-causal, Q, K, V, dO ~ N(0,1) from seed 2 (the shape shared by the sequence
+sweep, the backward configuration and the FP8 configuration, inside the N >= 4096
+regime the throughput targets are stated for).  One step = one forward and one
+backward pass over that batch, four launches: fa_fwd, then the backward's three
+stages (fa_bwd_prep, fa_bwd_main, fa_bwd_dq).  TFLOP/s counts 4*B*H*N^2*d for
+the forward and 2.5 times that for the backward; `frac_of_peak` divides by the
+measured dense bf16 peak.  Each stage is bracketed by its own CUDA events, which
+give the per-kernel rooflines.
+
+Timed the same way after the headline, and reported beside it (not in `value`):
+the causal forward and backward at the same shape, and the FP8 path on the FP8
+workload (B=2, H=16, N=8192, d=128, fp32 inputs with 0.1 % x20 outliers, seeded
+rotation signs): fa_fp8_prepare and fa_fwd_fp8, non-causal and causal, each
+against its own roofline (the FP8 forward against twice the measured bf16 peak,
+the nominal FP8/bf16 ratio).
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier and
 torch.cuda.synchronize() on both sides.  L2 (129 MB) is flushed before every
-step by writing a 256 MB buffer outside the per-step CUDA-event pairs; device
-time is the sum of the per-step event pairs on the launching stream, max over
-ranks.  `e2e` repeats the step through the same public calls with the inputs in
-pinned host memory: every step copies Q, K, V and dO in and O, LSE, dQ, dK, dV and the
-FP8 O and LSE out, all inside its timed region.  The copies run on their own streams
-and overlap the neighbouring steps' kernels (double-buffered), as a serving or
-training loop would overlap them.
+step by writing a 256 MB buffer outside the per-step CUDA-event pairs (the
+inputs, 268 MB, are larger than L2 as well); device time is the sum of the
+per-step event pairs on the launching stream, max over ranks.  SM clocks and
+throttle reasons are polled through NVML every 2 ms during the timed region.
+`e2e` repeats the step through the public calls (fa_fwd, fa_bwd) with the inputs
+in pinned host memory: every step copies Q, K, V and dO in and O, LSE, dQ, dK and
+dV out, all inside its timed region; the copies run on their own streams and
+overlap the neighbouring steps' kernels (double-buffered).
 
 Under torchrun (N > 1) every rank runs the same independent replica (the heads
 shard with no exchange, so there is no collective on the data path) and rank 0
@@ -32,18 +39,25 @@ bounded row sample of the same workload instead (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
 import subprocess
 import sys
+import tempfile
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = {"workload": "bf16 attention forward + backward, B=4 H=16 N=2048 d=128, non-causal, scale=1/sqrt(d)",
-            "B": 4, "H": 16, "N": 2048, "d": 128, "causal": False, "seed": 2}
+WORKLOAD = {"workload": "bf16 attention forward + backward (fa_fwd, fa_bwd_prep, fa_bwd_main, fa_bwd_dq), "
+                        "B=2 H=16 N=8192 d=128, non-causal, scale=1/sqrt(d)",
+            "B": 2, "H": 16, "N": 8192, "d": 128, "causal": False, "seed": 2}
+FP8_WORKLOAD = {"workload": "FP8 e4m3 attention forward (fa_fp8_prepare + fa_fwd_fp8), B=2 H=16 N=8192 d=128, fp32 "
+                            "Q/K/V ~ N(0,1) with 0.1% x20 outliers, seeded +-1 Hadamard rotation, bf16 O",
+                "B": 2, "H": 16, "N": 8192, "d": 128, "seed": 5}
 METRIC = "attention fwd/bwd TFLOP/s on 1 GB300 and % of dense BF16/FP8 tensor peak"
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -117,71 +131,159 @@ def dist_env():
         os.environ.get("LOCAL_RANK", "0"))
 
 
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*).
+_NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+                 0x80: "hw_power_brake_slowdown"}
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """SM clock and throttle reasons of one GPU, polled while the timed region runs.
 
-    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML (the library behind nvidia-smi) is read from a thread every 2 ms, so even
+    a region of a few tens of milliseconds gets samples; without NVML, nvidia-smi
+    is sampled every 100 ms into a temporary file.  Reading clocks changes no
+    setting of the GPU.
+    """
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
-        self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+    def __init__(self, cuda_index: int):
+        self.cuda_index = cuda_index
+        self.samples = []  # (time, sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._smi = None
+        self._nvml = None
+        self._dev = None
+
+    def _open_nvml(self):
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if nv.nvmlInit_v2() != 0:
+            return False
+        dev = ctypes.c_void_p()
+        bus = None
+        try:
+            import torch
+
+            props = torch.cuda.get_device_properties(self.cuda_index)
+            dom, b, dv = (getattr(props, a, None) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id"))
+            if None not in (dom, b, dv):
+                bus = f"{dom:08x}:{b:02x}:{dv:02x}.0".encode()
+        except Exception:
+            bus = None
+        ok = bus is not None and nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(dev)) == 0
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.cuda_index), ctypes.byref(dev)) != 0:
+            return False
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx)) == 0:  # 1 = NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        self._reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or getattr(
+            nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self._nvml, self._dev = nv, dev
+        return True
+
+    def _poll(self):
+        nv, dev = self._nvml, self._dev
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(dev, 1, ctypes.byref(mhz)) == 0 and self._reasons(dev, ctypes.byref(rs)) == 0:
+                self.samples.append((time.time(), float(mhz.value), int(rs.value)))
+            time.sleep(0.002)
 
     def start(self):
+        if self._open_nvml():
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+            return
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            self._fh = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self._smi = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.cuda_index), "--query-gpu=timestamp,clocks.sm,clocks.max.sm,"
+                 "clocks_event_reasons.active", "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self._fh, stderr=subprocess.DEVNULL)
         except Exception:
-            self.proc = None
+            self._smi = None
 
     def mark(self, which: str):
         setattr(self, which, time.time())
 
     def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.fh.close()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        import datetime
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+            self._nvml.nvmlShutdown()
+            source = "nvml"
+        elif self._smi is not None:
+            import datetime
 
-        t0, t1 = getattr(self, "t0", None), getattr(self, "t1", None)
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
+            self._smi.terminate()
             try:
-                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                if t0 is not None and t1 is not None and not (t0 <= ts <= t1):
-                    continue  # outside the timed region
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+                self._smi.wait(timeout=5)
+            except Exception:
+                self._smi.kill()
+            self._fh.seek(0)
+            for line in self._fh:
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    self.samples.append((ts, float(parts[1]), int(parts[3], 16)))
+                    self.max_mhz = float(parts[2])
+                except (ValueError, IndexError):
+                    continue
+            self._fh.close()
+            os.unlink(self._fh.name)
+            source = "nvidia-smi"
+        else:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        t0, t1 = getattr(self, "t0", None), getattr(self, "t1", None)
+        inside = [s for s in self.samples if t0 is None or t1 is None or t0 <= s[0] <= t1]
+        if not inside:
+            return None
+        reasons = set()
+        for _, _, bits in inside:
+            for b, name in _NVML_REASONS.items():
+                if bits & b:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": self.max_mhz,
+                "samples": len(inside), "reasons": sorted(reasons), "source": source}
+
+
+def _median_ms(fn, reps, flush=None, stream=None):
+    import torch
+
+    stream = stream or torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return sorted(x.elapsed_time(y) for x, y in ts)[reps // 2]
+
+
+def _tensor_stage(ms, flops, peak, kernel, bound="tensor"):
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"ms": round(ms, 5), "bound": bound, "kernel": kernel, "achieved": round(tf, 1), "unit": "TFLOP/s",
+            "peak": peak, "frac": round(tf / peak, 4)}
+
+
+def _hbm_stage(ms, byts, hbm, kernel):
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 5), "bound": "hbm", "kernel": kernel, "achieved": round(gbs, 1), "unit": "GB/s",
+            "peak": hbm, "frac": round(gbs / hbm, 4), "algorithmic_bytes": byts}
 
 
 def run_ours(args):
     import torch
 
     import io_aware_exact_fwd_gb300 as fa
-    from synth import normal_qkv, rotation_signs
+    from synth import normal_qkv
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -190,31 +292,32 @@ def run_ours(args):
 
         dist.init_process_group("nccl")
     fa.load_library()
+    peaks = load_peaks()
+    peak, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
     w = WORKLOAD
     B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
     scale = d ** -0.5
     x = normal_qkv(B, H, N, d, w["seed"] + rank, with_do=True)
     q, k, v, g = (x[n].to(torch.bfloat16).cuda() for n in ("q", "k", "v", "do"))
+    del x
     o = torch.empty_like(q)
     lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
-    ws8 = torch.empty(fa.fa_fp8_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
-    signs = rotation_signs(d, w["seed"]).cuda()
-    o8 = torch.empty_like(q)
-    lse8 = torch.empty_like(lse)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
-    stages = ("fwd", "bwd_prep", "bwd_main", "bwd_dq", "fp8_prep", "fwd_fp8")
-    calls = {
-        "fwd": lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=causal, scale=scale),
-        "bwd_prep": lambda: fa.fa_bwd_prep(o, g, lse, ws),
-        "bwd_main": lambda: fa.fa_bwd_main(q, k, v, g, dk, dv, ws, causal=causal, scale=scale),
-        "bwd_dq": lambda: fa.fa_bwd_dq(ws, dq, scale=scale),
-        "fp8_prep": lambda: fa.fa_fp8_prepare(q, k, v, signs, ws8),
-        "fwd_fp8": lambda: fa.fa_fwd_fp8(ws8, (B, H, N, d), o=o8, lse=lse8, causal=causal, scale=scale),
-    }
-    launches_per_step = 6
+
+    def step_calls(c):
+        return {
+            "fwd": lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=c, scale=scale),
+            "bwd_prep": lambda: fa.fa_bwd_prep(o, g, lse, ws),
+            "bwd_main": lambda: fa.fa_bwd_main(q, k, v, g, dk, dv, ws, causal=c, scale=scale),
+            "bwd_dq": lambda: fa.fa_bwd_dq(ws, dq, scale=scale),
+        }
+
+    stages = ("fwd", "bwd_prep", "bwd_main", "bwd_dq")
+    calls = step_calls(causal)
+    launches_per_step = 4
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -229,7 +332,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     if sampler:
         sampler.start()
-        time.sleep(0.3)
+        time.sleep(0.05)
     t_wall0 = time.perf_counter()
     if sampler:
         sampler.mark("t0")
@@ -250,9 +353,52 @@ def run_ours(args):
     dev_ms = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps))
     dev_ms = max_over_ranks(dev_ms, "cuda")
     f_fwd = fwd_flops(B, H, N, d, causal)
-    flops_step = 4.5 * f_fwd  # bf16 forward + backward (2.5x) + FP8 forward
+    flops_step = 3.5 * f_fwd  # bf16 forward + backward (2.5x)
     ms_per_step = dev_ms / args.steps
     value = whole_job_tflops(flops_step, args.steps, world, dev_ms)
+
+    elems = B * H * N * d
+    npad = (N + 63) // 64 * 64
+    # Algorithmic bytes and FLOPs of each stage (per launch).
+    stage_info = {
+        "fwd": {"bound": "tensor", "flops": f_fwd, "bytes": 8 * elems + 4 * B * H * N,
+                "kernel": "fwd_kernel<128,false,bf16>", "profile": "fwd_bf16_B2H16N8192d128.md",
+                "source": "io_aware_exact_fwd_gb300/csrc/fa_fwd.cu"},
+        "bwd_prep": {"bound": "hbm", "bytes": 4 * elems + 4 * B * H * N + 8 * B * H * npad + 4 * elems,
+                     "kernel": "bwd_preprocess_kernel"},
+        "bwd_main": {"bound": "tensor", "flops": 2.5 * f_fwd,
+                     "bytes": 10 * elems + 8 * B * H * npad + 4 * elems + 4 * elems,
+                     "kernel": "bwd_main_kernel<false>", "profile": "bwd_main_B2H16N8192d128.md",
+                     "source": "io_aware_exact_fwd_gb300/csrc/fa_bwd.cu"},
+        "bwd_dq": {"bound": "hbm", "bytes": 4 * elems + 2 * elems, "kernel": "bwd_dq_convert_kernel"},
+    }
+
+    def stage_report(st, ms):
+        info = stage_info[st]
+        if info["bound"] == "tensor":
+            r = _tensor_stage(ms, info["flops"], peak, info["kernel"])
+            r["gbs"] = round(info["bytes"] / (ms * 1e-3) / 1e9, 1)
+            return r
+        return _hbm_stage(ms, info["bytes"], hbm, info["kernel"])
+
+    per_stage = {st: stage_report(st, stage_ms[st]) for st in stages}
+    dom = max(stages, key=lambda st: stage_ms[st])
+    di = stage_info[dom]
+    traffic = args.traffic if args.traffic is not None else (
+        profile_traffic(di["profile"], di["source"]) if "profile" in di else None)
+    roofline = {
+        "bound": di["bound"], "kernel": di["kernel"], "achieved": per_stage[dom]["achieved"],
+        "peak": per_stage[dom]["peak"],
+        "peak_source": (f"{peaks['source']} bf16_tflops (burst, cuBLAS): the kernel runs a few ms at a time"
+                        if di["bound"] == "tensor" else f"{peaks['source']} hbm_gbs (copy)"),
+        "unit": per_stage[dom]["unit"], "frac": per_stage[dom]["frac"], "traffic": traffic,
+        "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
+        "algorithmic_flops_per_launch": di.get("flops"), "algorithmic_bytes_per_launch": di["bytes"],
+    }
+
+    extra = None
+    if not args.step_only:
+        extra = extra_rows(fa, args, q, k, v, g, o, lse, dq, dk, dv, ws, scale, flush, peaks, stage_info, rank)
 
     # End to end through the public calls: pinned host inputs in, every output back
     # out, every step.  Pipelined over three streams: while step i computes, the
@@ -260,6 +406,46 @@ def run_ours(args):
     # (two sets of device inputs, device outputs and pinned host outputs; events
     # order each set's reuse).  The timed region runs from the first step's first
     # input copy to the last step's last output copy.
+    e2e = None
+    if not args.step_only:
+        e2e = run_e2e(fa, args, q, k, v, g, lse, ws, causal, scale, flops_step, world)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return None
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1 and not args.step_only:
+        cpu = cpu_baseline(seconds=args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(WORKLOAD, l2="flushed before every step (256 MB write, outside the timed event pairs); "
+                                    "inputs (268 MB) also exceed L2",
+                       parallelism=f"replicas x{world}" if world > 1 else "single GPU",
+                       flops_per_step=flops_step),
+        "frac_of_peak": round(flops_step / 1e12 / (ms_per_step * 1e-3) / peak, 4),
+        "roofline": roofline,
+        "stages": per_stage,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed_region": round(t_wall, 4),
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if extra is not None:
+        line.update(extra)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line
+
+
+def run_e2e(fa, args, q, k, v, g, lse, ws, causal, scale, flops_step, world):
+    import torch
+
     hq, hk, hv, hg = (t.cpu().pin_memory() for t in (q, k, v, g))
     h_in = (hq, hk, hv, hg)
     e2e_steps = max(3, min(args.steps, 50))
@@ -268,35 +454,33 @@ def run_ours(args):
     for _ in range(2):
         din = [torch.empty_like(t) for t in (q, k, v, g)]
         dout = [torch.empty_like(q), torch.empty_like(lse), torch.empty_like(q), torch.empty_like(k),
-                torch.empty_like(v), torch.empty_like(q), torch.empty_like(lse)]  # o, lse, dq, dk, dv, o8, lse8
+                torch.empty_like(v)]  # o, lse, dq, dk, dv
         hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dout]
-        ev = {n: torch.cuda.Event() for n in ("in_ready", "in_free", "out_ready", "out_free")}
-        sets.append((din, dout, hout, ev))
+        evs = {n: torch.cuda.Event() for n in ("in_ready", "in_free", "out_ready", "out_free")}
+        sets.append((din, dout, hout, evs))
 
     def e2e_step(i):
-        din, dout, hout, ev = sets[i % 2]
+        din, dout, hout, evs = sets[i % 2]
         with torch.cuda.stream(s_h2d):
             if i >= 2:
-                s_h2d.wait_event(ev["in_free"])  # step i - 2 has finished reading these inputs
+                s_h2d.wait_event(evs["in_free"])  # step i - 2 has finished reading these inputs
             for dst, src in zip(din, h_in):
                 dst.copy_(src, non_blocking=True)
-            ev["in_ready"].record(s_h2d)
-        s_comp.wait_event(ev["in_ready"])
+            evs["in_ready"].record(s_h2d)
+        s_comp.wait_event(evs["in_ready"])
         if i >= 2:
-            s_comp.wait_event(ev["out_free"])  # step i - 2's outputs have been copied out
+            s_comp.wait_event(evs["out_free"])  # step i - 2's outputs have been copied out
         qi, ki, vi, gi = din
-        o_, lse_, dq_, dk_, dv_, o8_, lse8_ = dout
+        o_, lse_, dq_, dk_, dv_ = dout
         fa.fa_fwd(qi, ki, vi, o=o_, lse=lse_, causal=causal, scale=scale, stream=s_comp)
         fa.fa_bwd(qi, ki, vi, o_, gi, lse_, dq_, dk_, dv_, ws, causal=causal, scale=scale, stream=s_comp)
-        fa.fa_fp8_prepare(qi, ki, vi, signs, ws8, stream=s_comp)
-        fa.fa_fwd_fp8(ws8, (B, H, N, d), o=o8_, lse=lse8_, causal=causal, scale=scale, stream=s_comp)
-        ev["in_free"].record(s_comp)
-        ev["out_ready"].record(s_comp)
+        evs["in_free"].record(s_comp)
+        evs["out_ready"].record(s_comp)
         with torch.cuda.stream(s_d2h):
-            s_d2h.wait_event(ev["out_ready"])
+            s_d2h.wait_event(evs["out_ready"])
             for dst, src in zip(hout, dout):
                 dst.copy_(src, non_blocking=True)
-            ev["out_free"].record(s_d2h)
+            evs["out_free"].record(s_d2h)
 
     for i in range(2):
         e2e_step(i)
@@ -311,210 +495,166 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, "cuda")
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in sets[0][2])
-
-    nxt = (next_rows(fa, q, k, v, g, o, lse, dq, dk, dv, ws, causal, scale, stage_ms, (ws8, signs, o8, lse8))
-           if rank == 0 else None)
-
-    if rank != 0:
-        if world > 1:
-            torch.distributed.destroy_process_group()
-        return None
-
-    peaks = load_peaks()
-    peak = peaks["bf16_tflops"]
-    hbm = peaks["hbm_gbs"]
-    elems = B * H * N * d
-    npad = (N + 63) // 64 * 64
-    stage_info = {
-        "fwd": {"bound": "tensor", "flops": f_fwd, "bytes": 8 * elems + 4 * B * H * N,
-                "kernel": "fwd_bf16_kernel<128,false>", "profile": "fwd_bf16_B4H16N2048d128.md",
-                "source": "io_aware_exact_fwd_gb300/csrc/fa_fwd.cu"},
-        "bwd_prep": {"bound": "hbm", "flops": 2.0 * elems,
-                     "bytes": 4 * elems + 4 * B * H * N + 8 * B * H * npad + 4 * elems,
-                     "kernel": "bwd_preprocess_kernel"},
-        "bwd_main": {"bound": "tensor", "flops": 2.5 * f_fwd,
-                     "bytes": 10 * elems + 8 * B * H * npad + 4 * elems + 4 * elems,
-                     "kernel": "bwd_main_kernel<false>", "profile": "bwd_main_B4H16N2048d128.md",
-                     "source": "io_aware_exact_fwd_gb300/csrc/fa_bwd.cu"},
-        "bwd_dq": {"bound": "hbm", "flops": 0.0, "bytes": 4 * elems + 2 * elems, "kernel": "bwd_dq_convert_kernel"},
-        "fp8_prep": {"bound": "hbm", "flops": 0.0, "bytes": 3 * 2 * elems + 3 * elems, "kernel": "fp8_prepare_kernel<128>"},
-        "fwd_fp8": {"bound": "tensor_fp8", "flops": f_fwd, "bytes": 3 * elems + 2 * elems + 4 * B * H * N,
-                    "kernel": "fwd_kernel<128,false,fp8>"},
-    }
-    per_stage = {}
-    for st in stages:
-        info, ms = stage_info[st], stage_ms[st]
-        tf = info["flops"] / (ms * 1e-3) / 1e12
-        gbs = info["bytes"] / (ms * 1e-3) / 1e9
-        if info["bound"] in ("tensor", "tensor_fp8"):
-            pk = peak if info["bound"] == "tensor" else 2.0 * peak
-            per_stage[st] = {"ms": round(ms, 5), "bound": info["bound"], "achieved": round(tf, 1),
-                             "unit": "TFLOP/s", "frac": round(tf / pk, 4), "peak": pk, "gbs": round(gbs, 1)}
-        else:
-            per_stage[st] = {"ms": round(ms, 5), "bound": "hbm", "achieved": round(gbs, 1), "unit": "GB/s",
-                             "frac": round(gbs / hbm, 4)}
-    dom = max(stages, key=lambda st: stage_ms[st])
-    di = stage_info[dom]
-    dom_ach = per_stage[dom]["achieved"]
-    dom_peak = {"tensor": peak, "tensor_fp8": 2.0 * peak, "hbm": hbm}[di["bound"]]
-    traffic = None
-    if args.traffic is not None:
-        traffic = args.traffic
-    elif "profile" in di:
-        traffic = profile_traffic(di["profile"], di["source"])
-    roofline = {
-        "bound": di["bound"], "kernel": di["kernel"], "achieved": dom_ach, "peak": dom_peak,
-        "peak_source": {"tensor": f"{peaks['source']} bf16_tflops (burst, cuBLAS)",
-                        "tensor_fp8": f"2 x {peaks['source']} bf16_tflops (FP8/BF16 nominal ratio)",
-                        "hbm": f"{peaks['source']} hbm_gbs (copy)"}[di["bound"]],
-        "unit": per_stage[dom]["unit"], "frac": round(dom_ach / dom_peak, 4), "traffic": traffic,
-        "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
-        "algorithmic_flops_per_launch": di["flops"], "algorithmic_bytes_per_launch": di["bytes"],
-    }
-    cpu = None
-    if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(seconds=args.cpu_seconds)
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(WORKLOAD, l2="flushed before every step (256 MB write, outside the timed event pairs)",
-                       parallelism=f"replicas x{world}" if world > 1 else "single GPU",
-                       flops_per_step=flops_step),
-        "frac_of_peak": round((3.5 * f_fwd / peak + f_fwd / (2.0 * peak)) / 1e12 / (ms_per_step * 1e-3), 4),
-        "roofline": roofline,
-        "stages": per_stage,
-        "e2e": {"value": round(flops_step / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
-        "wall_s_timed_region": round(t_wall, 3),
-        "clocks": clocks,
-        "cpu_baseline": cpu,
-        "next": finish_next_rows(nxt, peaks),
-    }
-    print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
-    return line
+    return {"value": round(flops_step / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "calls": "fa_fwd + fa_bwd per step; H2D of q, k, v, dO and D2H of o, lse, dq, dk, dv inside the "
+                     "timed region, overlapped with the neighbouring steps' kernels"}
 
 
-# Rows past the hot path, timed after the step (not part of `value`): the split-KV
-# decode forward and the 4-bit-weight GEMV on their own workloads; the
-# deterministic backward and the FP8 backward on the step's.
+# Rows past the headline, timed after it (not part of `value`): the causal step
+# and the FP8 forward as stage objects; the split-KV decode forward and the
+# 4-bit-weight GEMV on their own workloads; the deterministic backward and the
+# FP8 backward on the headline / FP8 shapes.
 DECODE = {"B": 8, "H": 16, "Nq": 1, "Nk": 32768, "d": 128, "causal": False, "seed": 5}
 W4A16 = {"M": 1, "N": 28672, "K": 8192, "seed": 6}
 
 
-def _median_ms(fn, reps, flush=None):
+def extra_rows(fa, args, q, k, v, g, o, lse, dq, dk, dv, ws, scale, flush, peaks, stage_info, rank):
     import torch
 
-    ts = []
-    for _ in range(reps):
-        if flush is not None:
-            flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        ts.append((a, b))
-    torch.cuda.synchronize()
-    return sorted(x.elapsed_time(y) for x, y in ts)[reps // 2]
+    from synth import normal_qkv, outlier_qkv, rotation_signs, w4a16_inputs
 
-
-def next_rows(fa, q, k, v, g, o, lse, dq, dk, dv, ws, causal, scale, stage_ms, fp8):
-    import torch
-
-    from synth import normal_qkv, w4a16_inputs
-
+    peak, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    reps = max(5, min(args.steps, 20))
+    B, H, N, d = q.shape
     out = {}
-    w = DECODE
-    B, H, Nq, Nk, d = w["B"], w["H"], w["Nq"], w["Nk"], w["d"]
-    kv = normal_qkv(B, H, Nk, d, w["seed"])
-    qd = normal_qkv(B, H, Nq, d, w["seed"] + 1)["q"].to(torch.bfloat16).cuda()
+
+    # Causal forward and backward at the headline shape.
+    calls = {
+        "fwd": lambda: fa.fa_fwd(q, k, v, o=o, lse=lse, causal=True, scale=scale),
+        "bwd_prep": lambda: fa.fa_bwd_prep(o, g, lse, ws),
+        "bwd_main": lambda: fa.fa_bwd_main(q, k, v, g, dk, dv, ws, causal=True, scale=scale),
+        "bwd_dq": lambda: fa.fa_bwd_dq(ws, dq, scale=scale),
+    }
+    for _ in range(3):
+        for c in calls.values():
+            c()
+    cs = {}
+    for st, c in calls.items():
+        # Each stage reads what the previous ones wrote; they are timed one by one,
+        # L2 flushed before each repetition.
+        ms = _median_ms(c, reps, flush)
+        info = stage_info[st]
+        if info["bound"] == "tensor":
+            cs[st] = _tensor_stage(ms, info["flops"] / 2, peak, info["kernel"].replace("false", "true"))
+        else:
+            cs[st] = _hbm_stage(ms, info["bytes"], hbm, info["kernel"])
+    fa.fa_sync_check()
+    f_c = fwd_flops(B, H, N, d, True)
+    tot = sum(s["ms"] for s in cs.values())
+    out["causal"] = {"workload": WORKLOAD["workload"].replace("non-causal", "causal"),
+                     "tflops": round(3.5 * f_c / (tot * 1e-3) / 1e12, 1),
+                     "frac_of_peak": round(3.5 * f_c / (tot * 1e-3) / 1e12 / peak, 4), "ms": round(tot, 5),
+                     "stages": cs}
+
+    # FP8 path on the FP8 workload.
+    w8 = FP8_WORKLOAD
+    B8, H8, N8, d8 = w8["B"], w8["H"], w8["N"], w8["d"]
+    x8 = outlier_qkv(B8, H8, N8, d8, w8["seed"])
+    q8, k8, v8 = (x8[n].cuda() for n in ("q", "k", "v"))
+    del x8
+    signs = rotation_signs(d8, w8["seed"]).cuda()
+    ws8 = torch.empty(fa.fa_fp8_workspace_size(B8, H8, N8, d8), dtype=torch.uint8, device="cuda")
+    o8 = torch.empty(B8, H8, N8, d8, dtype=torch.bfloat16, device="cuda")
+    lse8 = torch.empty(B8, H8, N8, dtype=torch.float32, device="cuda")
+    prep = lambda: fa.fa_fp8_prepare(q8, k8, v8, signs, ws8)
+    for _ in range(3):
+        prep()
+    ms_prep = _median_ms(prep, reps, flush)
+    el8 = B8 * H8 * N8 * d8
+    fp8 = {"workload": w8["workload"], "config": {kk: w8[kk] for kk in ("B", "H", "N", "d", "seed")},
+           "fp8_prepare": _hbm_stage(ms_prep, 3 * 4 * el8 + 3 * el8 + 3 * 4 * B8 * H8 * ((N8 + 63) // 64), hbm,
+                                     "fp8_prepare_kernel<128>")}
+    for c8 in (False, True):
+        call = lambda: fa.fa_fwd_fp8(ws8, (B8, H8, N8, d8), o=o8, lse=lse8, causal=c8, scale=d8 ** -0.5)
+        for _ in range(3):
+            call()
+        ms = _median_ms(call, reps, flush)
+        r = _tensor_stage(ms, fwd_flops(B8, H8, N8, d8, c8), 2.0 * peak, f"fwd_kernel<128,{str(c8).lower()},fp8>",
+                          bound="tensor_fp8")
+        r["peak_source"] = f"2 x {peaks['source']} bf16_tflops (the nominal FP8/bf16 ratio)"
+        r["tflops_with_prepare"] = round(fwd_flops(B8, H8, N8, d8, c8) / ((ms + ms_prep) * 1e-3) / 1e12, 1)
+        fp8["fwd_fp8_causal" if c8 else "fwd_fp8"] = r
+    fa.fa_sync_check()
+    out["fp8"] = fp8
+
+    if rank != 0:
+        return out
+    nxt = {}
+    # Split-KV decode: one query row against 32768 keys (K and V, 2.1 GB, far beyond L2).
+    wd = DECODE
+    Bd, Hd, Nq, Nk, dd = wd["B"], wd["H"], wd["Nq"], wd["Nk"], wd["d"]
+    kv = normal_qkv(Bd, Hd, Nk, dd, wd["seed"])
+    qd = normal_qkv(Bd, Hd, Nq, dd, wd["seed"] + 1)["q"].to(torch.bfloat16).cuda()
     kd, vd = kv["k"].to(torch.bfloat16).cuda(), kv["v"].to(torch.bfloat16).cuda()
     del kv
-    n = fa.fa_splitkv_default_splits(B, H, Nq, Nk, d)
-    wsd = torch.empty(fa.fa_splitkv_workspace_size(B, H, Nq, d, n), dtype=torch.uint8, device="cuda")
+    n = fa.fa_splitkv_default_splits(Bd, Hd, Nq, Nk, dd)
+    wsd = torch.empty(fa.fa_splitkv_workspace_size(Bd, Hd, Nq, dd, n), dtype=torch.uint8, device="cuda")
     od = torch.empty_like(qd)
-    lsed = torch.empty(B, H, Nq, dtype=torch.float32, device="cuda")
-    call = lambda: fa.fa_fwd_splitkv(qd, kd, vd, od, lsed, wsd, n_split=n, causal=w["causal"])
+    lsed = torch.empty(Bd, Hd, Nq, dtype=torch.float32, device="cuda")
+    call = lambda: fa.fa_fwd_splitkv(qd, kd, vd, od, lsed, wsd, n_split=n, causal=wd["causal"])
     for _ in range(3):
         call()
-    ms = _median_ms(call, 20)  # K and V (2.1 GB) are far larger than L2
-    byts = 4 * B * H * Nk * d + 4 * B * H * Nq * d + 8 * n * B * H * Nq * (d + 1)
-    out["splitkv_decode"] = {"config": dict(w, n_split=n), "ms": round(ms, 5), "bytes": byts, "gbs": byts / ms / 1e6,
-                             "launches": 2}
+    ms = _median_ms(call, 20)
+    byts = 4 * Bd * Hd * Nk * dd + 4 * Bd * Hd * Nq * dd + 8 * n * Bd * Hd * Nq * (dd + 1)
+    r = _hbm_stage(ms, byts, hbm, "fwd_kernel<128,false,bf16,split> + merge_kernel<128>")
+    r.update(workload="split-KV decode forward + merge", config=dict(wd, n_split=n), gpu_launches=2)
+    nxt["splitkv_decode"] = r
     del kd, vd
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
-    det = lambda: fa.fa_bwd(q, k, v, o, g, lse, dq, dk, dv, ws, causal=causal, scale=scale, deterministic=True)
+    f_bwd = 2.5 * fwd_flops(B, H, N, d, False)
+    det = lambda: fa.fa_bwd(q, k, v, o, g, lse, dq, dk, dv, ws, causal=False, scale=scale, deterministic=True)
+    fa.fa_fwd(q, k, v, o=o, lse=lse, causal=False, scale=scale)
     for _ in range(3):
         det()
-    ms_det = _median_ms(det, 20, flush)
+    ms_det = _median_ms(det, reps, flush)
+    plain = lambda: fa.fa_bwd(q, k, v, o, g, lse, dq, dk, dv, ws, causal=False, scale=scale)
+    ms_plain = _median_ms(plain, reps, flush)
     fa.fa_sync_check()
-    out["bwd_deterministic"] = {"ms": round(ms_det, 5),
-                                "ms_atomic": round(stage_ms["bwd_prep"] + stage_ms["bwd_main"] + stage_ms["bwd_dq"], 5),
-                                "launches": 4}
-    # FP8 backward on the step's FP8 workspace and dO, both modes.
-    ws8, signs, o8, lse8 = fp8
-    B, H, N, d = q.shape
-    wsb = torch.empty(fa.fa_bwd_fp8_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    nxt["bwd_deterministic"] = {"workload": "bf16 backward with order-free dQ, the headline shape (non-causal)",
+                                "ms": round(ms_det, 5), "tflops": round(f_bwd / (ms_det * 1e-3) / 1e12, 1),
+                                "ms_atomic_dq": round(ms_plain, 5), "gpu_launches": 4}
+    # FP8 backward on the FP8 workspace (FP8 workload) with a seeded dO.
+    g8 = normal_qkv(B8, H8, N8, d8, w8["seed"] + 1)["q"].to(torch.bfloat16).cuda()
+    fa.fa_fwd_fp8(ws8, (B8, H8, N8, d8), o=o8, lse=lse8, causal=False, scale=d8 ** -0.5)
+    wsb = torch.empty(fa.fa_bwd_fp8_workspace_size(B8, H8, N8, d8), dtype=torch.uint8, device="cuda")
+    dq8, dk8, dv8 = (torch.empty_like(o8) for _ in range(3))
+    f_bwd8 = 2.5 * fwd_flops(B8, H8, N8, d8, False)
+    res = {}
     for rec in (False, True):
-        call = lambda: fa.fa_bwd_fp8(ws8, signs, o8, g, lse8, dq, dk, dv, wsb, causal=causal, scale=scale,
+        call = lambda: fa.fa_bwd_fp8(ws8, signs, o8, g8, lse8, dq8, dk8, dv8, wsb, causal=False, scale=d8 ** -0.5,
                                      recompute_forward=rec)
         for _ in range(3):
             call()
-        out["bwd_fp8_recompute" if rec else "bwd_fp8"] = {"ms": round(_median_ms(call, 20, flush), 5),
-                                                          "launches": 6 if rec else 5}
+        res[rec] = _median_ms(call, reps, flush)
     fa.fa_sync_check()
-    del wsb
+    nxt["bwd_fp8"] = {"workload": "FP8 backward (straight-through: dequantise, bf16 backward, inverse rotation), "
+                                  "the FP8 workload, with fa_fwd_fp8's O and LSE",
+                      "ms": round(res[False], 5), "tflops": round(f_bwd8 / (res[False] * 1e-3) / 1e12, 1),
+                      "ms_recompute_forward": round(res[True], 5),
+                      "tflops_recompute_forward": round(f_bwd8 / (res[True] * 1e-3) / 1e12, 1), "gpu_launches": 5}
+    del wsb, dq8, dk8, dv8, g8
     # W4A16 decode GEMV: 28672 x 8192 packed weights (117 MB, beyond L2) times one activation row.
-    w = W4A16
-    xin = w4a16_inputs(w["M"], w["N"], w["K"], w["seed"])
-    x, wq, sc, zr = (xin[n].cuda() for n in ("x", "wq", "scales", "zeros"))
-    nsp = fa.fa_w4a16_default_splits(w["M"], w["N"], w["K"])
-    wsw = torch.empty(max(fa.fa_w4a16_workspace_size(w["M"], w["N"], w["K"], nsp), 1), dtype=torch.uint8,
+    ww = W4A16
+    xin = w4a16_inputs(ww["M"], ww["N"], ww["K"], ww["seed"])
+    xw, wq, sc, zr = (xin[nn].cuda() for nn in ("x", "wq", "scales", "zeros"))
+    nsp = fa.fa_w4a16_default_splits(ww["M"], ww["N"], ww["K"])
+    wsw = torch.empty(max(fa.fa_w4a16_workspace_size(ww["M"], ww["N"], ww["K"], nsp), 1), dtype=torch.uint8,
                       device="cuda")
-    y = torch.empty(w["M"], w["N"], dtype=torch.float16, device="cuda")
-    call = lambda: fa.fa_w4a16_gemm(x, wq, sc, zr, y, wsw, n_split=nsp)
+    y = torch.empty(ww["M"], ww["N"], dtype=torch.float16, device="cuda")
+    call = lambda: fa.fa_w4a16_gemm(xw, wq, sc, zr, y, wsw, n_split=nsp)
     for _ in range(3):
         call()
     ms_w = _median_ms(call, 20, flush)
     fa.fa_sync_check()
-    M_, N_, K_ = w["M"], w["N"], w["K"]
+    M_, N_, K_ = ww["M"], ww["N"], ww["K"]
     byts = N_ * K_ // 2 + 3 * N_ * K_ // 128 + 2 * M_ * K_ + 2 * M_ * N_
-    out["w4a16_gemv"] = {"config": dict(w, n_split=nsp), "ms": round(ms_w, 5), "bytes": byts,
-                         "gbs": byts / ms_w / 1e6, "launches": 2 if nsp > 1 else 1}
+    r = _hbm_stage(ms_w, byts, hbm, "w4a16_gemv_kernel")
+    r.update(workload="W4A16 dequantising GEMV (4-bit weights, group 128, fp16 activations)",
+             config=dict(ww, n_split=nsp), gpu_launches=2 if nsp > 1 else 1)
+    nxt["w4a16_gemv"] = r
+    out["next"] = nxt
     return out
-
-
-def finish_next_rows(nxt, peaks):
-    if nxt is None:
-        return None
-    w = WORKLOAD
-    sk = nxt["splitkv_decode"]
-    f_bwd = 2.5 * fwd_flops(w["B"], w["H"], w["N"], w["d"], w["causal"])
-    bd = nxt["bwd_deterministic"]
-    return {
-        "splitkv_decode": {"workload": "split-KV decode forward + merge", "config": sk["config"], "ms": sk["ms"],
-                           "bound": "hbm", "achieved": round(sk["gbs"], 1), "unit": "GB/s",
-                           "peak": peaks["hbm_gbs"], "frac": round(sk["gbs"] / peaks["hbm_gbs"], 4),
-                           "algorithmic_bytes": sk["bytes"], "gpu_launches": sk["launches"]},
-        "bwd_deterministic": {"workload": "bf16 backward with order-free dQ, the step's configuration",
-                              "ms": bd["ms"], "tflops": round(f_bwd / (bd["ms"] * 1e-3) / 1e12, 1),
-                              "ms_atomic_dq": bd["ms_atomic"], "gpu_launches": bd["launches"]},
-        "bwd_fp8": {"workload": "FP8 backward (straight-through; dequantise, bf16 backward, inverse rotation), "
-                                "the step's configuration, with fa_fwd_fp8's O and LSE",
-                    "ms": nxt["bwd_fp8"]["ms"], "tflops": round(f_bwd / (nxt["bwd_fp8"]["ms"] * 1e-3) / 1e12, 1),
-                    "ms_recompute_forward": nxt["bwd_fp8_recompute"]["ms"],
-                    "tflops_recompute_forward": round(f_bwd / (nxt["bwd_fp8_recompute"]["ms"] * 1e-3) / 1e12, 1),
-                    "gpu_launches": nxt["bwd_fp8"]["launches"]},
-        "w4a16_gemv": {"workload": "W4A16 dequantising GEMV (4-bit weights, group 128, fp16 activations)",
-                       "config": nxt["w4a16_gemv"]["config"], "ms": nxt["w4a16_gemv"]["ms"], "bound": "hbm",
-                       "achieved": round(nxt["w4a16_gemv"]["gbs"], 1), "unit": "GB/s", "peak": peaks["hbm_gbs"],
-                       "frac": round(nxt["w4a16_gemv"]["gbs"] / peaks["hbm_gbs"], 4),
-                       "algorithmic_bytes": nxt["w4a16_gemv"]["bytes"],
-                       "gpu_launches": nxt["w4a16_gemv"]["launches"]},
-    }
 
 
 def _oracle_step_sample(q, k, v, g, scale, causal, head, r0, rows_per_step):
@@ -533,7 +673,7 @@ def _oracle_step_sample(q, k, v, g, scale, causal, head, r0, rows_per_step):
 def _oracle_inputs():
     import torch
 
-    from synth import normal_qkv, rotation_signs
+    from synth import normal_qkv
 
     w = WORKLOAD
     x = normal_qkv(1, 2, w["N"], w["d"], w["seed"], with_do=True)
@@ -598,11 +738,13 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time the headline step alone (for profiler captures): no e2e, extra rows or CPU baseline")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture of this kernel version")
     args = ap.parse_args()

@@ -13,8 +13,8 @@
  * materialised ("FlashAttention-2 (DE)", same section, "IO-Awareness" and
  * "Tiling"; "FlashAttention-Skalierung, Multi-GPU-Training und
  * Gewichtsquantisierung", section 1, FlashAttention-2 bullets).  The result is
- * the standard one up to floating-point rounding ("exakt identisch ... ohne
- * Genauigkeitsverlust", lead of "FlashAttention-2 (DE)").
+ * the standard one up to floating-point rounding: the tiling loses no accuracy
+ * (lead of "FlashAttention-2 (DE)").
  *
  * Conventions shared by every call:
  *  - Tensors are dense, row-major [B, H, N, d] ("BHND": each head is one N x d
@@ -159,6 +159,11 @@ FA_API int fa_bwd_strided(const void* q, const int64_t* q_strides, const void* k
  * contribution is at most 2^-S / 2, far below the bf16 output's rounding.  dK and
  * dV are those of fa_bwd (already reproducible).  Costs one extra pass over K and
  * V for the bound.  Arguments, workspace and errors: exactly as fa_bwd.
+ * Precondition: `lse` is the forward's LSE for the same q, k, scale and causal
+ * (as fa_fwd writes it).  The bound above assumes that the recomputed
+ * probabilities of each row sum to about 1; an LSE computed from other operands
+ * breaks that assumption, and the int32 sums may then wrap without any error
+ * being reported (fa_bwd would return finite but equally meaningless values).
  */
 FA_API int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dout,
                                 const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
@@ -192,17 +197,26 @@ FA_API int fa_bwd_dq(const void* workspace, size_t ws_bytes, void* dq, int B, in
  * that owns all device memory and gives plugins no allocator, or a
  * latency-critical loop where cudaMalloc, which may synchronise the device, is
  * not allowed).  The caller still passes every input and output exactly as for
- * fa_bwd; the scratch comes from one fixed buffer per device that the library
- * holds from the moment it is first used on that device until the process
- * exits (fa_bwd_noalloc_max_workspace() bytes, 64 MiB).
+ * fa_bwd; the scratch comes from one fixed buffer of
+ * fa_bwd_noalloc_max_workspace() bytes (64 MiB) in this library's device code.
  * Limits and behaviour:
- *  - Sizes whose fa_bwd_workspace_size() exceeds that buffer are rejected with
- *    FA_ERR_WORKSPACE before anything is launched (at d = 128 this admits about
- *    B*H*N <= 127,000 rows); other errors are those of fa_bwd.
+ *  - The buffer is reserved on a device when the library's device code is loaded
+ *    into a context there: with lazy module loading (the CUDA default) at the
+ *    first call of this entry point in that context; with eager loading
+ *    (CUDA_MODULE_LOADING=EAGER) when any context is created while the library
+ *    is loaded, whether or not this entry point is ever called.  It is held
+ *    until that context is destroyed or the process exits.
+ *  - Arguments are validated exactly as fa_bwd validates them (same statuses)
+ *    before the buffer is touched; then sizes whose fa_bwd_workspace_size()
+ *    exceeds the buffer are rejected with FA_ERR_WORKSPACE before anything is
+ *    launched (at d = 128 this admits about B*H*N <= 127,000 rows).
  *  - It calls no cudaMalloc, cudaFree or other allocating routine.
- *  - The first call on a device looks up the buffer's device address for that
- *    device; make that first call before any stream capture.
- *  - Every call on a device shares the one buffer, which keeps the contents of
+ *  - Every call looks up the buffer's device address in the context current on
+ *    the calling thread (a table lookup; a context replaced since, e.g. by
+ *    cudaDeviceReset or a framework's own context, gets its own buffer).  The
+ *    first call in a context loads the module that holds the buffer: make that
+ *    first call before any stream capture.
+ *  - Every call in a context shares the one buffer, which keeps the contents of
  *    the last call (the kernels initialise what must start at zero).  Calls that
  *    overlap on the GPU (e.g. on two streams at once) race on it: serialise them.
  */
@@ -247,6 +261,25 @@ FA_API size_t fa_fp8_workspace_size(int B, int H, int N, int d);
 FA_API int fa_fp8_workspace_offsets(int B, int H, int N, int d, size_t* offsets);
 FA_API int fa_fp8_prepare(const void* q, const void* k, const void* v, int in_dtype, const int8_t* signs,
                           void* workspace, size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream);
+
+/*
+ * fa_fp8_prepare_seeded -- fa_fp8_prepare with the rotation's signs drawn from a
+ * 64-bit seed instead of passed in: sign of column c = -1 if the top bit of
+ * output c (0-based) of SplitMix64 started at state `seed` is set, else +1.
+ * SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+ * generators", OOPSLA 2014): output c = mix(seed + (c + 1) * 0x9E3779B97F4A7C15)
+ * with mix(z) = z3 ^ (z3 >> 31), z3 = (z2 ^ (z2 >> 27)) * 0x94D049BB133111EB,
+ * z2 = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9, all modulo 2^64.  The signs are
+ * computed on the device; the workspace, the codes and the errors are those of
+ * fa_fp8_prepare given the same signs (fa_fp8_rotation_signs).
+ *
+ * fa_fp8_rotation_signs -- the d signs (+1 / -1) of that seed, written to
+ * `signs`, HOST memory of d int8 (for fa_bwd_fp8, which takes the signs as a
+ * device array).  Pure host code; FA_ERR_INVALID_ARG for d < 1 or NULL signs.
+ */
+FA_API int fa_fp8_prepare_seeded(const void* q, const void* k, const void* v, int in_dtype, uint64_t seed,
+                                 void* workspace, size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream);
+FA_API int fa_fp8_rotation_signs(uint64_t seed, int d, int8_t* signs);
 
 /*
  * fa_fwd_fp8 -- FP8 forward from a workspace filled by fa_fp8_prepare (same
@@ -301,6 +334,9 @@ FA_API int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* ls
  *                the UNROUNDED probabilities.  fa_fwd_fp8 rounds P to e4m3 for its
  *                P V product, so its O carries that error into D and from there
  *                into every dS of the row (a few percent RMS on dQ at N = 1000).
+ *                With deterministic = 1 and recompute_forward = 0, `lse` must be
+ *                the LSE fa_fwd_fp8 wrote for this workspace (see the
+ *                precondition of fa_bwd_deterministic).
  *                1: O and LSE are recomputed by the bf16 forward on Q', K', V'
  *                (about 35 % more time); the result is the straight-through
  *                gradient to the bf16 backward's accuracy.  0: the caller's o and

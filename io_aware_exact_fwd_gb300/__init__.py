@@ -18,7 +18,8 @@ import os
 __all__ = [
     "FAError", "load_library", "library_path", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_noalloc",
     "fa_bwd_noalloc_max_workspace", "fa_bwd_prep", "fa_bwd_main", "fa_bwd_dq", "fa_fp8_workspace_size",
-    "fa_fp8_workspace_offsets", "fa_fp8_prepare", "fa_fwd_fp8", "fa_sync_check",
+    "fa_fp8_workspace_offsets", "fa_fp8_prepare", "fa_fp8_prepare_seeded", "fa_fp8_rotation_signs", "fa_fwd_fp8",
+    "fa_sync_check",
     "fa_strerror",
     "fa_version", "fa_last_error_site", "fa_debug_set_wait_limit_ns", "fa_debug_set_fault",
     "STATUS",
@@ -85,6 +86,10 @@ def load_library():
     lib.fa_fp8_workspace_offsets.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.fa_fp8_prepare.restype = i
     lib.fa_fp8_prepare.argtypes = [vp, vp, vp, i, vp, vp, ctypes.c_size_t, i, i, i, i, vp]
+    lib.fa_fp8_prepare_seeded.restype = i
+    lib.fa_fp8_prepare_seeded.argtypes = [vp, vp, vp, i, ctypes.c_uint64, vp, ctypes.c_size_t, i, i, i, i, vp]
+    lib.fa_fp8_rotation_signs.restype = i
+    lib.fa_fp8_rotation_signs.argtypes = [ctypes.c_uint64, i, vp]
     lib.fa_fwd_fp8.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, ctypes.c_size_t, vp, vp, i, i, i, i, i, f, vp]
     lib.fa_bwd_noalloc.restype = i
@@ -336,6 +341,37 @@ def fa_fp8_prepare(q, k, v, signs, workspace=None, stream=None):
                                 _ptr(workspace), _ws_bytes(workspace), B, H, N, d, _stream_handle(stream))
     _check(st, "fa_fp8_prepare")
     return workspace
+
+
+def fa_fp8_prepare_seeded(q, k, v, seed: int, workspace=None, stream=None):
+    """fa_fp8_prepare with the rotation signs drawn from a 64-bit seed on the device; returns the workspace."""
+    import torch
+
+    lib = load_library()
+    B, H, N, d = q.shape
+    dt = q.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise TypeError("q, k, v must be float32 or bfloat16")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_bhnd(name, t, (B, H, N, d), dt)
+    if workspace is None:
+        workspace = torch.empty(max(fa_fp8_workspace_size(B, H, N, d), 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = lib.fa_fp8_prepare_seeded(_ptr(q), _ptr(k), _ptr(v), 1 if dt == torch.bfloat16 else 0,
+                                       ctypes.c_uint64(seed & (2 ** 64 - 1)), _ptr(workspace), _ws_bytes(workspace),
+                                       B, H, N, d, _stream_handle(stream))
+    _check(st, "fa_fp8_prepare_seeded")
+    return workspace
+
+
+def fa_fp8_rotation_signs(seed: int, d: int):
+    """The +-1 signs (int8 CPU tensor [d]) fa_fp8_prepare_seeded uses for ``seed``."""
+    import torch
+
+    out = torch.empty(d, dtype=torch.int8)
+    _check(load_library().fa_fp8_rotation_signs(ctypes.c_uint64(seed & (2 ** 64 - 1)), d,
+                                                 ctypes.c_void_p(out.data_ptr())), "fa_fp8_rotation_signs")
+    return out
 
 
 def fa_fwd_fp8(workspace, shape, o=None, lse=None, causal: bool = False, scale: float | None = None, stream=None):

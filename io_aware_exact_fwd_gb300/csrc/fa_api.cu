@@ -14,8 +14,11 @@
 #include "fa_internal.h"
 
 // One error word per device (a __device__ variable is instantiated on every
-// device that loads this module).  Kernels receive its address as a plain
-// pointer; the address is looked up once per device with the device current.
+// device, in every context, that loads this module).  Kernels receive its
+// address as a plain pointer.  That address belongs to the context that was
+// current when it was looked up: a context can be replaced (cudaDeviceReset, or
+// a non-primary context a host framework makes current), so it is looked up
+// again on every call, with the caller's context current.
 static __device__ unsigned int g_fa_error_word;
 
 namespace {
@@ -25,7 +28,6 @@ constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 
 struct DeviceState {
   bool ready = false;
-  unsigned int* err_word = nullptr;
   int cc = 0;  // major * 10 + minor
   unsigned int last_site = 0;
 };
@@ -40,37 +42,39 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
-// Resolves per-device state (error word address, compute capability) once.
-int device_state(DeviceState** out) {
+// Per-device facts that do not change for the life of the process (compute
+// capability, the tensor-map encoder) are resolved once; the error word's
+// address in the current context is resolved on every call (see above) and
+// returned through `err_word` when it is non-null.
+int device_state(DeviceState** out, unsigned int** err_word = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  DeviceState& s = g_dev[dev];
-  if (!s.ready) {
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FA_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FA_ERR_CUDA;
-    s.cc = major * 10 + minor;
-    if (s.cc != 103) {
-      *out = &s;
-      return FA_ERR_UNSUPPORTED;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& s = g_dev[dev];
+    if (!s.ready) {
+      int major = 0, minor = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FA_ERR_CUDA;
+      if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FA_ERR_CUDA;
+      s.cc = major * 10 + minor;
+      if (s.cc == 103 && !g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+          return FA_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+      }
+      s.ready = true;
     }
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_fa_error_word) != cudaSuccess) return FA_ERR_CUDA;
-    s.err_word = static_cast<unsigned int*>(p);
-    if (!g_encode) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-              cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || !fn)
-        return FA_ERR_CUDA;
-      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-    }
-    s.ready = true;
+    *out = &s;
+    if (s.cc != 103) return FA_ERR_UNSUPPORTED;
   }
-  *out = &s;
-  return s.cc == 103 ? FA_OK : FA_ERR_UNSUPPORTED;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fa_error_word) != cudaSuccess || !p) return FA_ERR_CUDA;
+  if (err_word) *err_word = static_cast<unsigned int*>(p);
+  return FA_OK;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -199,7 +203,8 @@ int fa_fwd_strided(const void* q, const int64_t* q_strides, const void* k, const
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return FA_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
-  st = device_state(&ds);
+  unsigned int* ew = nullptr;
+  st = device_state(&ds, &ew);
   if (st != FA_OK) return st;
   a.q = q;
   a.k = k;
@@ -212,7 +217,7 @@ int fa_fwd_strided(const void* q, const int64_t* q_strides, const void* k, const
   a.d = d;
   a.causal = causal;
   a.scale = scale;
-  a.err_word = ds->err_word;
+  a.err_word = ew;
   a.dbg = knobs();
   return fa::launch_fwd_bf16(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -303,7 +308,8 @@ int fa_fwd_splitkv_partial(const void* q, const void* k, const void* v, float* o
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o_part, 16) || !aligned(lse_part, 4))
     return FA_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
-  const int st = device_state(&ds);
+  unsigned int* ew = nullptr;
+  const int st = device_state(&ds, &ew);
   if (st != FA_OK) return st;
   fa::SplitKvArgs a;
   a.q = q;
@@ -319,7 +325,7 @@ int fa_fwd_splitkv_partial(const void* q, const void* k, const void* v, float* o
   a.n_split = n_split;
   a.causal = causal;
   a.scale = scale;
-  a.err_word = ds->err_word;
+  a.err_word = ew;
   a.dbg = knobs();
   return fa::launch_fwd_splitkv_partial(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
                                                                                                    : FA_ERR_CUDA;
@@ -333,7 +339,8 @@ int fa_merge_partials(const float* o_part, const float* lse_part, void* o, float
   if (!o_part || !lse_part || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned(o_part, 16) || !aligned(lse_part, 4) || !aligned(o, 16) || !aligned(lse, 4)) return FA_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
-  const int st = device_state(&ds);
+  unsigned int* ew = nullptr;
+  const int st = device_state(&ds, &ew);
   if (st != FA_OK) return st;
   fa::MergeArgs a;
   a.o_part = o_part;
@@ -416,7 +423,8 @@ int fa_w4a16_gemm(const void* x, const void* wq, const void* scales, const void*
   if (need > 0 && !aligned(workspace, 256)) return FA_ERR_MISALIGNED;
   if (static_cast<long long>(N) * (K / 8) > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   DeviceState* ds = nullptr;
-  const int st = device_state(&ds);
+  unsigned int* ew = nullptr;
+  const int st = device_state(&ds, &ew);
   if (st != FA_OK) return st;
   fa::W4a16Args a;
   a.x = x;
@@ -429,7 +437,7 @@ int fa_w4a16_gemm(const void* x, const void* wq, const void* scales, const void*
   a.N = N;
   a.K = K;
   a.n_split = n_split;
-  a.err_word = ds->err_word;
+  a.err_word = ew;
   a.dbg = knobs();
   return fa::launch_w4a16(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -446,6 +454,7 @@ namespace {
 // Which tensors a backward stage reads or writes.
 enum BwdUse : unsigned {
   kUseQKV = 1u, kUseO = 2u, kUseDout = 4u, kUseLse = 8u, kUseDq = 16u, kUseDkDv = 32u,
+  kNoWorkspace = 64u,  // validate everything but the workspace (its caller supplies one later)
 };
 
 // Validation shared by fa_bwd and its three stages; fills `a` on success.
@@ -459,8 +468,10 @@ int bwd_setup(fa::BwdArgs& a, unsigned use, const void* q, const void* k, const 
   if (((use & kUseQKV) && (!q || !k || !v)) || ((use & kUseO) && !o) || ((use & kUseDout) && !dout) ||
       ((use & kUseLse) && !lse) || ((use & kUseDq) && !dq) || ((use & kUseDkDv) && (!dk || !dv)))
     return FA_ERR_INVALID_ARG;
-  if (!workspace) return FA_ERR_WORKSPACE;
-  if (ws_bytes < fa::bwd_workspace_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
+  if (!(use & kNoWorkspace)) {
+    if (!workspace) return FA_ERR_WORKSPACE;
+    if (ws_bytes < fa::bwd_workspace_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
+  }
   // strides (optional): q, k, v, o, dout, dq, dk, dv; NULL entries are dense.
   fa::Strides* dst[8] = {&a.sq, &a.sk, &a.sv, &a.so, &a.sdo, &a.sdq, &a.sdk, &a.sdv};
   for (int t = 0; t < 8; ++t) {
@@ -470,10 +481,12 @@ int bwd_setup(fa::BwdArgs& a, unsigned use, const void* q, const void* k, const 
   const bool al = (!(use & kUseQKV) || (aligned(q, 16) && aligned(k, 16) && aligned(v, 16))) &&
                   (!(use & kUseO) || aligned(o, 16)) && (!(use & kUseDout) || aligned(dout, 16)) &&
                   (!(use & kUseLse) || aligned(lse, 4)) && (!(use & kUseDq) || aligned(dq, 16)) &&
-                  (!(use & kUseDkDv) || (aligned(dk, 16) && aligned(dv, 16))) && aligned(workspace, 256);
+                  (!(use & kUseDkDv) || (aligned(dk, 16) && aligned(dv, 16))) &&
+                  ((use & kNoWorkspace) || aligned(workspace, 256));
   if (!al) return FA_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
-  const int st = device_state(&ds);
+  unsigned int* ew = nullptr;
+  const int st = device_state(&ds, &ew);
   if (st != FA_OK) return st;
   a.q = q;
   a.k = k;
@@ -492,7 +505,7 @@ int bwd_setup(fa::BwdArgs& a, unsigned use, const void* q, const void* k, const 
   a.causal = causal;
   a.deterministic = 0;
   a.scale = scale;
-  a.err_word = ds->err_word;
+  a.err_word = ew;
   a.dbg = knobs();
   return FA_OK;
 }
@@ -500,6 +513,19 @@ int bwd_setup(fa::BwdArgs& a, unsigned use, const void* q, const void* k, const 
 int status_of(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 }  // namespace
+
+namespace fa {
+
+int bwd_validate_without_workspace(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                                   int causal, float scale) {
+  BwdArgs a;
+  const int st = bwd_setup(a, kUseQKV | kUseO | kUseDout | kUseLse | kUseDq | kUseDkDv | kNoWorkspace, q, k, v, o,
+                           dout, lse, dq, dk, dv, nullptr, 0, B, H, N, d, causal, scale);
+  return st < 0 ? FA_OK : st;
+}
+
+}  // namespace fa
 
 extern "C" {
 
@@ -594,13 +620,17 @@ int fa_fp8_workspace_offsets(int B, int H, int N, int d, size_t* offsets) {
   return FA_OK;
 }
 
-int fa_fp8_prepare(const void* q, const void* k, const void* v, int in_dtype, const int8_t* signs, void* workspace,
-                   size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int fp8_prepare_impl(const void* q, const void* k, const void* v, int in_dtype, const int8_t* signs, uint64_t seed,
+                     void* workspace, size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream) {
   const int vs = validate_shape(B, H, N, d, 0, 1.f);
   if (vs < 0) return FA_OK;
   if (vs != FA_OK) return vs;
   if (in_dtype != 0 && in_dtype != 1) return FA_ERR_INVALID_ARG;
-  if (!q || !k || !v || !signs) return FA_ERR_INVALID_ARG;
+  if (!q || !k || !v) return FA_ERR_INVALID_ARG;
   if (!workspace) return FA_ERR_WORKSPACE;
   if (ws_bytes < fa::fp8_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(workspace, 256)) return FA_ERR_MISALIGNED;
@@ -613,12 +643,34 @@ int fa_fp8_prepare(const void* q, const void* k, const void* v, int in_dtype, co
   a.v = v;
   a.in_bf16 = in_dtype;
   a.signs = signs;
+  a.seed = seed;
   a.workspace = workspace;
   a.B = B;
   a.H = H;
   a.N = N;
   a.d = d;
   return fa::launch_fp8_prepare(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fp8_prepare(const void* q, const void* k, const void* v, int in_dtype, const int8_t* signs, void* workspace,
+                   size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream) {
+  if (!signs && B > 0 && H > 0 && N > 0) return FA_ERR_INVALID_ARG;
+  return fp8_prepare_impl(q, k, v, in_dtype, signs, 0, workspace, ws_bytes, B, H, N, d, stream);
+}
+
+int fa_fp8_prepare_seeded(const void* q, const void* k, const void* v, int in_dtype, uint64_t seed, void* workspace,
+                          size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream) {
+  return fp8_prepare_impl(q, k, v, in_dtype, nullptr, seed, workspace, ws_bytes, B, H, N, d, stream);
+}
+
+int fa_fp8_rotation_signs(uint64_t seed, int d, int8_t* signs) {
+  if (d < 1 || !signs) return FA_ERR_INVALID_ARG;
+  for (int c = 0; c < d; ++c) signs[c] = static_cast<int8_t>(fa::seeded_sign(seed, c));
+  return FA_OK;
 }
 
 int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* lse, int B, int H, int N, int d, int causal,
@@ -632,7 +684,8 @@ int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* lse, int 
   if (ws_bytes < fa::fp8_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
   if (!aligned(o, 16) || !aligned(lse, 4) || !aligned(workspace, 256)) return FA_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
-  const int st = device_state(&ds);
+  unsigned int* ew = nullptr;
+  const int st = device_state(&ds, &ew);
   if (st != FA_OK) return st;
   fa::FwdArgs a{};
   a.o = o;
@@ -644,7 +697,7 @@ int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* lse, int 
   a.d = d;
   a.causal = causal;
   a.scale = scale;
-  a.err_word = ds->err_word;
+  a.err_word = ew;
   a.dbg = knobs();
   return fa::launch_fwd_fp8(a, workspace, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
                                                                                                   : FA_ERR_CUDA;
@@ -688,7 +741,8 @@ int fa_fp8_dequantize(const void* fp8_ws, size_t fp8_ws_bytes, void* qr, void* k
   if (!qr || !kr || !vr) return FA_ERR_INVALID_ARG;
   if (!aligned(fp8_ws, 256) || !aligned(qr, 16) || !aligned(kr, 16) || !aligned(vr, 16)) return FA_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
-  const int st = device_state(&ds);
+  unsigned int* ew = nullptr;
+  const int st = device_state(&ds, &ew);
   if (st != FA_OK) return st;
   return status_of(fa::launch_fp8_dequant(fp8_ws, qr, kr, vr, B, H, N, d, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -741,15 +795,16 @@ int fa_bwd_fp8(const void* fp8_ws, size_t fp8_ws_bytes, const int8_t* signs, con
 
 int fa_sync_check(fa_stream_t stream) {
   DeviceState* ds = nullptr;
-  const int st = device_state(&ds);
+  unsigned int* ew = nullptr;
+  const int st = device_state(&ds, &ew);
   if (st != FA_OK) return st;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   unsigned int word = 0;
-  if (cudaMemcpy(&word, ds->err_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpy(&word, ew, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
   if (word != 0) {
     const unsigned int zero = 0;
-    if (cudaMemcpy(ds->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemcpy(ew, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
     ds->last_site = word;
     return FA_ERR_TIMEOUT;

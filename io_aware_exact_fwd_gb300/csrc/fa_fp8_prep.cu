@@ -7,7 +7,9 @@
 // random orthogonal matrix before quantising (incoherent processing).
 //
 // Here (one CTA per 64-row tile of one head of Q, K or V):
-//  * Q and K rows are rotated by x -> (x * s) H_d, s the caller's +-1 signs and
+//  * Q and K rows are rotated by x -> (x * s) H_d, s the caller's +-1 signs (or,
+//    given a 64-bit seed instead, signs from the SplitMix64 outputs, see
+//    seeded_sign in fa_internal.h) and
 //    H_d the Sylvester Walsh-Hadamard matrix, as a radix-2 transform with
 //    butterfly spans 1, 2, ..., d/2 (each butterfly one fp32 add and one fp32
 //    subtract; spans below the per-thread width in registers, the rest across
@@ -126,7 +128,7 @@ template <int D>
 __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* __restrict__ q,
                                                                    const void* __restrict__ k,
                                                                    const void* __restrict__ v, int in_bf16,
-                                                                   const int8_t* __restrict__ signs,
+                                                                   const int8_t* __restrict__ signs, uint64_t seed,
                                                                    Fp8Layout lay, uint8_t* __restrict__ ws, int N) {
   constexpr int E = D / 32;
   constexpr int kRowsPerWarp = kTileRows / 8;
@@ -198,7 +200,8 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
   const int sl = lane % kL, rg = lane / kL;
   float sg[kE];
 #pragma unroll
-  for (int i = 0; i < kE; ++i) sg[i] = signs[kE * sl + i] < 0 ? -1.f : 1.f;
+  for (int i = 0; i < kE; ++i)
+    sg[i] = signs ? (signs[kE * sl + i] < 0 ? -1.f : 1.f) : static_cast<float>(seeded_sign(seed, kE * sl + i));
   const void* src = which == 0 ? q : k;
   float xr[kPasses][kE];
   float amax = 0.f;
@@ -266,9 +269,11 @@ cudaError_t launch_fp8_prepare(const Fp8PrepArgs& a, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(lay.npad / kTileRows), static_cast<unsigned>(a.B * a.H), 3);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   if (a.d == 64)
-    fp8_prepare_kernel<64><<<grid, kPrepThreads, 0, stream>>>(a.q, a.k, a.v, a.in_bf16, a.signs, lay, ws, a.N);
+    fp8_prepare_kernel<64><<<grid, kPrepThreads, 0, stream>>>(a.q, a.k, a.v, a.in_bf16, a.signs, a.seed, lay, ws,
+                                                              a.N);
   else
-    fp8_prepare_kernel<128><<<grid, kPrepThreads, 0, stream>>>(a.q, a.k, a.v, a.in_bf16, a.signs, lay, ws, a.N);
+    fp8_prepare_kernel<128><<<grid, kPrepThreads, 0, stream>>>(a.q, a.k, a.v, a.in_bf16, a.signs, a.seed, lay, ws,
+                                                               a.N);
   return cudaGetLastError();
 }
 

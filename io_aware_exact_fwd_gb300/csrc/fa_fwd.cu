@@ -30,8 +30,8 @@
 //    memory.  TMEM holds S_a, S_b (128 columns each) and O_a, O_b (d columns
 //    each): all 512 columns at d = 128.
 //  * The O accumulators stay in TMEM for the whole inner loop.  O is rescaled only
-//    when a row maximum grows by more than 2^8 ("rescale only at the very end"
-//    taken one step further): until then exponentials are taken against the
+//    when a row maximum grows by more than 2^8 (the pages' single rescaling at
+//    the end of the loop, taken one step further): until then exponentials are taken against the
 //    stale maximum, which keeps O and l consistent and the final O/l exact.
 //
 // Every mbarrier wait is bounded (see fa_device.cuh); on expiry the CTA sets a

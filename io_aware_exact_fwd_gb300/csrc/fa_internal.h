@@ -117,6 +117,13 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream);
 
+// Every check fa_bwd makes except those on the workspace (fa_api.cu): sizes,
+// pointers, alignment and the device.  Returns an fa_status; FA_OK also for an
+// empty problem.
+int bwd_validate_without_workspace(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                                   int causal, float scale);
+
 // Workspace of the FP8 path (written by fa_fp8_prepare, read by fa_fwd_fp8):
 // e4m3 codes of the rotated Q and K, row-major [BH, N, d]; e4m3 codes of V
 // transposed [BH, d, npad] (keys contiguous, npad = N rounded up to 128); fp32
@@ -145,10 +152,26 @@ struct Fp8PrepArgs {
   const void* k;
   const void* v;
   int in_bf16;             // 0: fp32 inputs, 1: bf16 inputs
-  const int8_t* signs;     // [d], the sign of each entry is used
+  const int8_t* signs;     // [d], the sign of each entry is used; NULL: signs from `seed`
+  uint64_t seed;           // used when signs is NULL (see seeded_sign)
   void* workspace;
   int B, H, N, d;
 };
+
+// Output c (0-based) of SplitMix64 started at state `seed` (Steele, Lea and
+// Flood, OOPSLA 2014): x = seed + (c + 1) * 0x9E3779B97F4A7C15, then the
+// generator's two xor-shift-multiply rounds and a final xor-shift, all mod 2^64.
+// The seeded rotation takes column c's sign from the top bit of output c
+// (set: -1).  Host and device share this one definition.
+__host__ __device__ inline uint64_t splitmix64_at(uint64_t seed, uint64_t c) {
+  uint64_t z = seed + (c + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+__host__ __device__ inline int seeded_sign(uint64_t seed, int c) {
+  return (splitmix64_at(seed, static_cast<uint64_t>(c)) >> 63) ? -1 : 1;
+}
 cudaError_t launch_fp8_prepare(const Fp8PrepArgs& a, cudaStream_t stream);
 
 // Encodes a 3-D tiled tensor map over a [BH, N, cols] row-major tensor with

@@ -12,6 +12,20 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
 
 
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Print the error metrics the GPU parity tests measured (one line per case)."""
+    try:
+        from gpu_util import REPORT
+    except Exception:  # pragma: no cover
+        return
+    if not REPORT:
+        return
+    terminalreporter.write_sep("-", "parity metrics (measured)")
+    for name in sorted(REPORT):
+        vals = ", ".join(f"{k}={v:.4g}" if isinstance(v, float) else f"{k}={v}" for k, v in REPORT[name].items())
+        terminalreporter.write_line(f"{name}: {vals}")
+
+
 def pytest_collection_modifyitems(config, items):
     """Skip GPU tests cleanly on a machine without a GPU when they were not asked for."""
     try:

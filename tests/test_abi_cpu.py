@@ -195,3 +195,36 @@ def test_header_is_plain_c(tmp_path):
     r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
                         "-c", str(src), "-o", str(tmp_path / "use_fa.o")], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_seeded_rotation_signs_match_the_oracle(lib):
+    # The library's host copy of the seeded sign rule against the oracle's SplitMix64
+    # (itself pinned by published outputs); pure host code, no GPU needed.
+    import numpy as np
+
+    from oracle import seeded_rotation_signs
+
+    for seed in (0, 1, 5, 1234567, 2 ** 63, 2 ** 64 - 1):
+        for d in (1, 64, 128):
+            out = (ctypes.c_int8 * d)()
+            assert lib.fa_fp8_rotation_signs(ctypes.c_uint64(seed), d, out) == 0
+            assert np.array_equal(np.frombuffer(out, dtype=np.int8), seeded_rotation_signs(seed, d)), (seed, d)
+    assert lib.fa_fp8_rotation_signs(ctypes.c_uint64(1), 0, (ctypes.c_int8 * 1)()) == 1
+    assert lib.fa_fp8_rotation_signs(ctypes.c_uint64(1), 64, None) == 1
+
+
+def test_fp8_prepare_validation_statuses(lib):
+    vp = ctypes.c_void_p
+    B, H, N, d = 1, 2, 100, 128
+    need = lib.fa_fp8_workspace_size(B, H, N, d)
+    seeded = lambda q=FAKE, ws=FAKE, nb=need, dt=0, dd=d: lib.fa_fp8_prepare_seeded(
+        vp(q), vp(FAKE), vp(FAKE), dt, ctypes.c_uint64(7), vp(ws), nb, B, H, N, dd, vp(0))
+    assert seeded(q=0) == 1
+    assert seeded(dt=2) == 1
+    assert seeded(ws=0) == 6
+    assert seeded(nb=need - 1) == 6
+    assert seeded(q=FAKE + 8) == 3
+    assert seeded(ws=FAKE + 16) == 3          # workspace must be 256-byte aligned
+    assert seeded(dd=96) == 2
+    # The signs-array form needs its signs.
+    assert lib.fa_fp8_prepare(vp(FAKE), vp(FAKE), vp(FAKE), 0, vp(0), vp(FAKE), need, B, H, N, d, vp(0)) == 1

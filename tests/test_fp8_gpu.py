@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import io_aware_exact_fwd_gb300 as fa
-from oracle import fp8_prepare
+from oracle import fp8_prepare, seeded_rotation_signs
 from synth import outlier_qkv, rotation_signs
 
 pytestmark = pytest.mark.gpu
@@ -79,7 +79,9 @@ def test_prepare_full_fp8_config_bit_exact():
 # costs 4-7 %, pinned in tests/test_oracle_fp8.py); it is checked against a
 # looser 1e-1 bound as a sanity check.
 
-from oracle import attention_forward, attention_forward_rows, fp8_dequantize  # noqa: E402
+from oracle import attention_forward, fp8_dequantize  # noqa: E402
+
+from gpu_util import edge_heads, host_f64, map_heads, report  # noqa: E402
 
 FP8_RMSE_REL = 3e-2
 
@@ -112,12 +114,18 @@ def test_fp8_forward_small(N, causal):
     assert _rel_rmse(o, o_deq) <= FP8_RMSE_REL
     assert float(np.abs(lse.cpu().numpy() - lse_deq).max()) <= 1e-2
     o_exact, _ = attention_forward(x["q"], x["k"], x["v"], scale, causal)
+    report(f"fp8 fwd B=1 H=2 N={N} d=128 causal={int(causal)}", rmse_vs_dequantised=_rel_rmse(o, o_deq),
+           rmse_vs_unquantised=_rel_rmse(o, o_exact))
     assert _rel_rmse(o, o_exact) <= 1e-1
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_forward_config_sampled_heads(causal):
-    # B=2, H=16, N=8192, d=128, 0.1% outliers x20, seeded rotation; rows of two heads.
+def test_fp8_forward_config_whole_heads(causal):
+    # B=2, H=16, N=8192, d=128, 0.1% outliers x20, seeded rotation; every row of the
+    # first, a middle and the last head.  Graded: RMSE against exact attention on the
+    # dequantised inputs.  Measured and reported beside it: RMSE against exact
+    # attention on the unquantised inputs, the reference the 3e-2 bound is stated
+    # for, which no e4m3 input quantisation can meet (tests/test_oracle_fp8.py).
     B, H, N, d = 2, 16, 8192, 128
     x = outlier_qkv(B, H, N, d, seed=5)
     s = rotation_signs(d, seed=5)
@@ -125,21 +133,27 @@ def test_fp8_forward_config_sampled_heads(causal):
     o, lse = fa.fa_fwd_fp8(ws, (B, H, N, d), causal=causal)
     fa.fa_sync_check()
     scale = d ** -0.5
-    rng = np.random.default_rng(77 + causal)
-    rows = np.unique(np.concatenate([[0, 1, 127, 128, N - 1], rng.integers(0, N, 250)]))
-    errs_deq, errs_exact = [], []
-    for b, h in ((0, 0), (B - 1, H - 1)):
+    oh, lh = host_f64(o), host_f64(lse)
+    heads = edge_heads(B, H)
+
+    def one(b, h):
         sl = (slice(b, b + 1), slice(h, h + 1))
         ref = fp8_prepare(x["q"][sl], x["k"][sl], x["v"][sl], s.numpy())
         qd, kd, vd = _dequantised(ref)
-        od, ld = attention_forward_rows(qd[0, 0], kd[0, 0], vd[0, 0], scale / d, causal, rows)
-        oe, _ = attention_forward_rows(x["q"][b, h], x["k"][b, h], x["v"][b, h], scale, causal, rows)
-        got = o[b, h, rows].float().cpu().numpy().astype(np.float64)
-        errs_deq.append(_rel_rmse(got, od))
-        errs_exact.append(_rel_rmse(got, oe))
-        assert float(np.abs(lse[b, h, rows].cpu().numpy() - ld).max()) <= 1e-2
-    assert max(errs_deq) <= FP8_RMSE_REL, errs_deq
-    assert max(errs_exact) <= 1e-1, errs_exact
+        od, ld = attention_forward(qd, kd, vd, scale / d, causal)
+        oe, _ = attention_forward(x["q"][sl], x["k"][sl], x["v"][sl], scale, causal)
+        return (float(((oh[sl] - od) ** 2).sum()), float((od ** 2).sum()), float(((oh[sl] - oe) ** 2).sum()),
+                float((oe ** 2).sum()), float(np.abs(lh[sl] - ld).max()))
+
+    r = map_heads(one, heads)
+    rmse_deq = np.sqrt(sum(e[0] for e in r) / sum(e[1] for e in r))
+    rmse_exact = np.sqrt(sum(e[2] for e in r) / sum(e[3] for e in r))
+    lse_err = max(e[4] for e in r)
+    report(f"fp8 fwd B=2 H=16 N=8192 d=128 causal={int(causal)}", heads=len(heads), rmse_vs_dequantised=rmse_deq,
+           rmse_vs_unquantised=rmse_exact, lse_vs_dequantised=lse_err)
+    assert rmse_deq <= FP8_RMSE_REL, rmse_deq
+    assert lse_err <= 1e-2, lse_err
+    assert rmse_exact <= 1e-1, rmse_exact
 
 
 def test_prepare_extreme_tiles_bit_exact():
@@ -167,3 +181,42 @@ def test_prepare_extreme_tiles_bit_exact():
     np.testing.assert_array_equal(q8, ref["q8"])
     np.testing.assert_array_equal(k8, ref["k8"])
     np.testing.assert_array_equal(v8t[..., :N], np.swapaxes(ref["v8"], -1, -2))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_prepare_seeded_matches_the_oracle_bit_exact(d, dtype):
+    # Signs drawn on the device from a 64-bit seed (SplitMix64): codes and scales
+    # equal the oracle's for the oracle's own seeded signs.
+    B, H, N = 2, 3, 333
+    x = outlier_qkv(B, H, N, d, seed=700 + d)
+    q, k, v = (x[n].to(dtype) for n in ("q", "k", "v"))
+    seed = 0x9E3779B97F4A7C15 + d
+    ws = fa.fa_fp8_prepare_seeded(q.cuda(), k.cuda(), v.cuda(), seed)
+    fa.fa_sync_check()
+    s = seeded_rotation_signs(seed, d)
+    assert np.array_equal(fa.fa_fp8_rotation_signs(seed, d).numpy(), s)
+    ref = fp8_prepare(q, k, v, s)
+    q8, k8, v8t, sq, sk, sv, npad = _regions(ws, B, H, N, d)
+    np.testing.assert_array_equal(q8, ref["q8"])
+    np.testing.assert_array_equal(k8, ref["k8"])
+    np.testing.assert_array_equal(v8t[..., :N], np.swapaxes(ref["v8"], -1, -2))
+    np.testing.assert_array_equal(sq, ref["sq"])
+    np.testing.assert_array_equal(sk, ref["sk"])
+    np.testing.assert_array_equal(sv, ref["sv"])
+
+
+def test_prepare_seeded_full_fp8_config_bit_exact():
+    # B=2, H=16, N=8192, d=128 fp32 outlier inputs, signs from seed 5.
+    B, H, N, d = 2, 16, 8192, 128
+    x = outlier_qkv(B, H, N, d, seed=5)
+    ws = fa.fa_fp8_prepare_seeded(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), 5)
+    fa.fa_sync_check()
+    ref = fp8_prepare(x["q"], x["k"], x["v"], seeded_rotation_signs(5, d))
+    q8, k8, v8t, sq, sk, sv, npad = _regions(ws, B, H, N, d)
+    np.testing.assert_array_equal(q8, ref["q8"])
+    np.testing.assert_array_equal(k8, ref["k8"])
+    np.testing.assert_array_equal(v8t, np.swapaxes(ref["v8"], -1, -2))
+    np.testing.assert_array_equal(sq, ref["sq"])
+    np.testing.assert_array_equal(sk, ref["sk"])
+    np.testing.assert_array_equal(sv, ref["sv"])
