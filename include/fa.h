@@ -108,7 +108,7 @@ FA_API int fa_fwd_strided(const void* q, const int64_t* q_strides, const void* k
 FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
 /*
- * fa_bwd -- bf16 backward pass of fa_fwd, d = 128.
+ * fa_bwd -- bf16 backward pass of fa_fwd, d = 64 or 128.
  * The gradient follows from the chain rule applied to the definition above
  * (the pages give the forward only): with P = softmax(scale * Q K^T [+mask]),
  *     dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,
@@ -124,9 +124,8 @@ FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  * Numerics: fp32 accumulation on the tensor cores; P and dS are rounded to
  * bf16 as MMA operands; dQ accumulates across key blocks with fp32 atomic adds,
  * so dQ may differ in the last bits from run to run (dK, dV do not).
- * Errors: as fa_fwd; additionally FA_ERR_UNSUPPORTED for d != 128 and
- * FA_ERR_WORKSPACE for a missing or short workspace; the workspace must be
- * 256-byte aligned (FA_ERR_MISALIGNED otherwise).
+ * Errors: as fa_fwd; additionally FA_ERR_WORKSPACE for a missing or short
+ * workspace; the workspace must be 256-byte aligned (FA_ERR_MISALIGNED otherwise).
  */
 FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                   void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes, int B, int H, int N, int d,

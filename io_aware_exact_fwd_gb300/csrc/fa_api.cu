@@ -443,7 +443,7 @@ int fa_w4a16_gemm(const void* x, const void* wq, const void* scales, const void*
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
-  if (validate_shape(B, H, N, d, 0, 1.f) != FA_OK || d != 128) return 0;
+  if (validate_shape(B, H, N, d, 0, 1.f) != FA_OK) return 0;
   return fa::bwd_workspace_layout(B, H, N, d).total;
 }
 
@@ -464,7 +464,6 @@ int bwd_setup(fa::BwdArgs& a, unsigned use, const void* q, const void* k, const 
   const int vs = validate_shape(B, H, N, d, causal, scale);
   if (vs < 0) return -1;
   if (vs != FA_OK) return vs;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
   if (((use & kUseQKV) && (!q || !k || !v)) || ((use & kUseO) && !o) || ((use & kUseDout) && !dout) ||
       ((use & kUseLse) && !lse) || ((use & kUseDq) && !dq) || ((use & kUseDkDv) && (!dk || !dv)))
     return FA_ERR_INVALID_ARG;

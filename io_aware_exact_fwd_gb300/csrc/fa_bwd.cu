@@ -1,4 +1,4 @@
-// Exact attention backward, bf16, d = 128, for sm_103a.
+// Exact attention backward, bf16, d = 64 or 128, for sm_103a.
 //
 // The pages describe only the forward ("FlashAttention-2 (DE)", "Hintergrund";
 // "FlashAttention-Skalierung ...", section 1).  The backward follows from the
@@ -29,6 +29,12 @@
 //     next block overlap this block's math), and two 64-column buffers for
 //     P^T, dS^T and then dQ^T.
 //  3. bwd_dq_convert: dQ = bf16(scale * dQacc).
+//
+// Every MMA has M = 128 (the tcgen05 data path with one TMEM lane per row).  At
+// d = 64 the dQ^T product (M = d) is padded to 128 rows: its A operand, K^T read
+// MN-major in two 64-row groups, takes the second group from a zeroed 16 KB
+// shared-memory box, so rows 64..127 of dQ^T come out zero and are not reduced.
+// That doubles only the dQ^T product (one fifth of the backward's FLOPs).
 #include <math.h>
 
 #include "fa_device.cuh"
@@ -37,7 +43,6 @@
 namespace fa {
 namespace {
 
-constexpr int kD = 128;
 constexpr int kBkB = 128;       // keys per CTA
 constexpr int kBqB = 64;        // query rows per inner step
 constexpr int kThreads = 512;   // 0-7 compute, 8-11 dQ reduction, 12 TMA, 13-14 MMA issuers, 15 spare
@@ -70,35 +75,40 @@ enum : uint32_t {
   kSiteBEpi = 0x313,
 };
 
+template <int D>
 struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kBoxes = D / 64;                 // 128-byte TMA boxes per bf16 row
   static constexpr int kKVBox = kBkB * 64 * 2;          // 16 KB: 128 rows x 128 B
-  static constexpr int kKVTile = kBkB * kD * 2;         // 32 KB
+  static constexpr int kKVTile = kBkB * D * 2;          // 32 KB (d=128), 16 KB (d=64)
   static constexpr int kQBox = kBqB * 64 * 2;           // 8 KB: 64 rows x 128 B
-  static constexpr int kQTile = kBqB * kD * 2;          // 16 KB
+  static constexpr int kQTile = kBqB * D * 2;           // 16 KB (d=128), 8 KB (d=64)
   static constexpr int kStageQ = 0;
   static constexpr int kStageDO = kQTile;
   static constexpr int kStageL = 2 * kQTile;            // 64 floats
   static constexpr int kStageD = 2 * kQTile + 256;      // 64 floats
   static constexpr int kStageTx = 2 * kQTile + 512;     // bytes landing per stage
-  static constexpr int kStageBytes = 34816;             // kStageTx rounded up to 1024
+  static constexpr int kStageBytes = D == 128 ? 34816 : (kStageTx + 1023) / 1024 * 1024;
   static constexpr int kDsBytes = kBkB * kBqB * 2;      // 16 KB: 128 key rows x 128 B
+  // K, then (d = 64) the zero box that pads K^T to the dQ^T MMA's 128 rows, then V.
   static constexpr int kKOff = 0;
-  static constexpr int kVOff = kKVTile;
-  static constexpr int kRingOff = 2 * kKVTile;
+  static constexpr int kZeroOff = kKVTile;
+  static constexpr int kVOff = kKVTile + (D == 64 ? kKVBox : 0);
+  static constexpr int kRingOff = kVOff + kKVTile;
   static constexpr int kDsOff = kRingOff + kStages * kStageBytes;
   static constexpr int kBarOff = kDsOff + 2 * kDsBytes;
   // kv, full[S], empty[S], sdp, sde, comp[2], dqf[2], dqe[2], dkv, epi, drain
   static constexpr int kNumBars = 1 + 2 * kStages + 1 + 1 + 2 + 2 + 2 + 1 + 1 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
-  // TMEM columns: dV, dK accumulators; one S^T, dP^T pair (fp32, read once by
-  // the compute warps, then free for the next query block); two 64-column
-  // buffers that hold P^T | dS^T (bf16, 32 columns each) and then dQ^T (fp32).
+  // TMEM columns: dV, dK accumulators (D columns each); one S^T, dP^T pair (fp32,
+  // read once by the compute warps, then free for the next query block); two
+  // 64-column buffers that hold P^T | dS^T (bf16, 32 columns each) and then dQ^T (fp32).
   static constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 320;
   static __device__ __forceinline__ uint32_t col_pdq(int b) { return 384u + 64u * b; }
+  static_assert(kStageTx <= kStageBytes, "stage layout");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
-static_assert(BwdCfg::kStageTx <= BwdCfg::kStageBytes, "stage layout");
-static_assert(BwdCfg::kSmemBytes <= 227 * 1024, "shared memory budget");
 
 __device__ __forceinline__ bool warp_wait_b(uint64_t* bar, uint32_t parity, const WaitCtl& wc, uint32_t site) {
   const bool ok = mbar_wait(bar, parity, wc, site);
@@ -132,11 +142,12 @@ __device__ __forceinline__ size_t row_offset(const Strides& st, long long bh, in
   return static_cast<size_t>((bh / H) * st.s[2] + (bh % H) * st.s[1] + static_cast<long long>(n) * st.s[0]);
 }
 
-// Stage the 128 x 128 fp32 accumulator row of this thread as bf16 into a
-// 128-byte-swizzled [128 rows][64 cols] x 2 TMA box pair.
+// Stage this thread's D-column fp32 accumulator row as bf16 into 128-byte-swizzled
+// [128 rows][64 cols] TMA boxes (D / 64 of them).
+template <int D>
 __device__ __forceinline__ void stage_row_bf16(uint32_t taddr_row, uint8_t* boxes, int row, float mul) {
 #pragma unroll 1
-  for (int c = 0; c < kD / 32; ++c) {
+  for (int c = 0; c < D / 32; ++c) {
     uint32_t o[32];
     tmem_ld32(taddr_row + c * 32, o);
     tmem_ld_wait32(o);
@@ -144,7 +155,7 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t taddr_row, uint8_t* boxe
 #pragma unroll
     for (int i = 0; i < 16; ++i)
       pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * mul, __uint_as_float(o[2 * i + 1]) * mul);
-    uint8_t* box = boxes + (c / 2) * BwdCfg::kKVBox + row * 128;
+    uint8_t* box = boxes + (c / 2) * BwdCfg<D>::kKVBox + row * 128;
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
       const int chunk = (c % 2) * 4 + q4;
@@ -154,7 +165,7 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t taddr_row, uint8_t* boxe
   }
 }
 
-template <bool CAUSAL, bool DET>
+template <int D, bool CAUSAL, bool DET>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -162,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float* __restrict__ lse2, const float* __restrict__ dvec, float* __restrict__ dq_acc,
                     const float* __restrict__ dq_bmax, const float* __restrict__ kv_max, int N, int Npad, int H,
                     int BH, int nkb, float scale, float scale_log2, unsigned int* err_word, unsigned long long wait_ns) {
-  using C = BwdCfg;
+  using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem + C::kKOff;
@@ -219,6 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if constexpr (D == 64) {
+    // Rows 64..127 of the dQ^T MMA's A operand: zeros, read by the tensor core.
+    uint4* z = reinterpret_cast<uint4*>(smem + C::kZeroOff);
+    for (int i = threadIdx.x; i < C::kKVBox / 16; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   if (warp == kWarpMma) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -234,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       mbar_arrive_expect_tx(bar_kv, 2 * C::kKVTile);
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < C::kBoxes; ++b) {
         tma_load_4d(sK + b * C::kKVBox, &tm_k, bar_kv, b * 64, kb * kBkB, h_idx, b_idx);
         tma_load_4d(sV + b * C::kKVBox, &tm_v, bar_kv, b * 64, kb * kBkB, h_idx, b_idx);
       }
@@ -245,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = i0 + it;
         uint8_t* st = sRing + slot * C::kStageBytes;
         mbar_arrive_expect_tx(&bar_full[slot], C::kStageTx);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::kBoxes; ++b) {
           tma_load_4d(st + C::kStageQ + b * C::kQBox, &tm_q, &bar_full[slot], b * 64, i * kBqB, h_idx, b_idx);
           tma_load_4d(st + C::kStageDO + b * C::kQBox, &tm_do, &bar_full[slot], b * 64, i * kBqB, h_idx, b_idx);
         }
@@ -272,8 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // lands over P^T, dS^T(it) only after dV, dK(it) consumed them.
     if (lane == 0) {
       constexpr uint32_t idesc_sdp = idesc_bf16_f32(kBkB, kBqB, 0, 0);   // keys x queries, K = d
-      constexpr uint32_t idesc_dkv = idesc_bf16_f32(kBkB, kD, 0, 1);     // keys x d, K = queries
-      constexpr uint32_t idesc_dq = idesc_bf16_f32(kD, kBqB, 1, 1);      // d x queries, K = keys
+      constexpr uint32_t idesc_dkv = idesc_bf16_f32(kBkB, D, 0, 1);      // keys x d, K = queries
+      // d x queries, K = keys; M = 128 rows (at d = 64, rows 64..127 read the zero box).
+      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, kBqB, 1, 1);
       const uint64_t k_kmaj = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t v_kmaj = sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t k_mn = sdesc_sw128(smem_u32(sK), C::kKVBox, 1024);
@@ -291,14 +309,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t st = slot * C::kStageBytes;
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
+          for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
             const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
             mma_bf16_ss(tmem + C::kColS, sdesc_add(k_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageQ + offb),
                         idesc_sdp, kk > 0 ? 1u : 0u);
           }
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
+          for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
             const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
             mma_bf16_ss(tmem + C::kColDP, sdesc_add(v_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageDO + offb),
@@ -323,7 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ts(tmem + C::kColDK, tmem + C::col_pdq(b) + 32 + kk * 8,
                         sdesc_add(ring_mn, st + C::kStageQ + kk * 2048), idesc_dkv, (it > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bar_empty[slot]);
-          // dQ_i^T = K^T dS^T : A = K MN-major (d contiguous), B = dS^T rows of 64 queries; 16 keys per MMA.
+          // dQ_i^T = K^T dS^T : A = K MN-major (d contiguous; the second 64-row group is K's
+          // second box at d = 128, the zero box at d = 64), B = dS^T rows of 64 queries;
+          // 16 keys per MMA.
 #pragma unroll
           for (int kk = 0; kk < kBkB / 16; ++kk)
             mma_bf16_ss(tmem + C::col_pdq(b), sdesc_add(k_mn, kk * 2048),
@@ -414,13 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = warp_wait_b(bar_dkv, 0, wc, kSiteBEpi);
     if (ok) {
       tc_fence_after();
-      if (g == 0) stage_row_bf16(trow + C::kColDV, sV, row, 1.f);
-      else stage_row_bf16(trow + C::kColDK, sK, row, scale);
+      if (g == 0) stage_row_bf16<D>(trow + C::kColDV, sV, row, 1.f);
+      else stage_row_bf16<D>(trow + C::kColDK, sK, row, scale);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_epi);
       if (threadIdx.x == 0 && mbar_wait(bar_epi, 0, wc, kSiteBEpi)) {
-        for (int bb = 0; bb < 2; ++bb) {
+        for (int bb = 0; bb < C::kBoxes; ++bb) {
           tma_store_4d(&tm_dv, sV + bb * C::kKVBox, bb * 64, kb * kBkB, h_idx, b_idx);
           tma_store_4d(&tm_dk, sK + bb * C::kKVBox, bb * 64, kb * kBkB, h_idx, b_idx);
         }
@@ -436,6 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; it < n; ++it) {
       const int b = it & 1;
       if (!warp_wait_b(&bar_dqf[b], (it >> 1) & 1, wc, kSiteBDq)) break;
+      if (D == 64 && dcol >= D) {  // the zero-padded rows of dQ^T: nothing to read or add
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_dqe[b]);
+        continue;
+      }
       tc_fence_after();
       uint32_t v[2][32];
       tmem_ld32(trow + C::col_pdq(b), v[0]);
@@ -446,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_dqe[b]);
       const int q0 = (i0 + it) * kBqB;
-      float* dst = dq_acc + (static_cast<size_t>(bh) * N + q0) * kD + dcol;
+      float* dst = dq_acc + (static_cast<size_t>(bh) * N + q0) * D + dcol;
       const int lim = min(kBqB, N - q0);
       if constexpr (DET) {
         const float mul = pow2f(det_shift(dq_bmax[static_cast<size_t>(bh) * (Npad / kBqB) + i0 + it],
@@ -458,14 +483,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (h * 32 + c < lim)
-              atomicAdd(dsti + static_cast<size_t>(h * 32 + c) * kD,
+              atomicAdd(dsti + static_cast<size_t>(h * 32 + c) * D,
                         __float_as_int(fmaf(__uint_as_float(v[h][c]), mul, kMagic)) - 0x4B400000);
       } else {
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            if (h * 32 + c < lim) atomicAdd(dst + static_cast<size_t>(h * 32 + c) * kD, __uint_as_float(v[h][c]));
+            if (h * 32 + c < lim) atomicAdd(dst + static_cast<size_t>(h * 32 + c) * D, __uint_as_float(v[h][c]));
       }
     }
     __syncwarp();
@@ -480,23 +505,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // D_i = sum_c dO_ic O_ic ; LSE2_i = LSE_i * log2(e) (rows >= N: D = 0, LSE2 = +inf);
-// dQacc rows < N are zeroed.  16 threads per row, 8 elements each.
-template <bool DET>
+// dQacc rows < N are zeroed.  D / 8 threads per row, 8 elements each.
+template <int D, bool DET>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              const float* __restrict__ lse, float* __restrict__ dvec,
                                                              float* __restrict__ lse2, float* __restrict__ dq_acc,
                                                              unsigned int* __restrict__ dq_bmax, int N, int Npad,
                                                              long long rows_pad, int H, Strides so, Strides sdo) {
-  const long long r = static_cast<long long>(blockIdx.x) * 16 + (threadIdx.x >> 4);
-  const int t = threadIdx.x & 15;
-  // The grid is exactly rows_pad / 16 blocks (Npad is a multiple of 64), so every
+  constexpr int kTpr = D / 8;          // threads per row
+  constexpr int kRpb = 256 / kTpr;     // rows per block: 16 (d=128) or 32 (d=64)
+  const long long r = static_cast<long long>(blockIdx.x) * kRpb + (threadIdx.x / kTpr);
+  const int t = threadIdx.x % kTpr;
+  // The grid is exactly rows_pad / kRpb blocks (Npad is a multiple of 64), so every
   // thread has a row and all of them reach the shuffles and the barrier below.
   const long long bh = r / Npad;
   const int nrow = static_cast<int>(r - bh * Npad);
   float acc = 0.f, nrm = 0.f;
   if (nrow < N) {
-    const size_t base = (static_cast<size_t>(bh) * N + nrow) * kD + t * 8;  // dense: the dQ accumulator
+    const size_t base = (static_cast<size_t>(bh) * N + nrow) * D + t * 8;  // dense: the dQ accumulator
     const uint4 ov = *reinterpret_cast<const uint4*>(o + row_offset(so, bh, H, nrow) + t * 8);
     const uint4 gv = *reinterpret_cast<const uint4*>(dout + row_offset(sdo, bh, H, nrow) + t * 8);
     const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
@@ -517,24 +544,25 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
-  for (int m = 8; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m, 16);
+  for (int m = kTpr / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m, kTpr);
   if (t == 0) {
     dvec[r] = nrow < N ? acc : 0.f;
     lse2[r] = nrow < N ? lse[static_cast<size_t>(bh) * N + nrow] * kLog2e : INFINITY;
   }
   if (DET) {
-    // The block's 16 rows lie in one 64-row query block (Npad and the block
-    // start are multiples of 16): reduce to one atomic per block.
+    // The block's rows lie in one 64-row query block (Npad and the block start are
+    // multiples of kRpb, which divides 64): reduce to one atomic per block.
 #pragma unroll
-    for (int m = 8; m >= 1; m >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, m, 16);
+    for (int m = kTpr / 2; m >= 1; m >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, m, kTpr);
     float mx = sqrtf(nrm);  // 0 for padded rows
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+#pragma unroll
+    for (int m = kTpr; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
     __shared__ float red[8];
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
     __syncthreads();
     if (threadIdx.x == 0) {
       for (int w = 1; w < 8; ++w) mx = fmaxf(mx, red[w]);
-      const long long r_first = static_cast<long long>(blockIdx.x) * 16;
+      const long long r_first = static_cast<long long>(blockIdx.x) * kRpb;
       const long long bh0 = r_first / Npad;
       atomicMax(dq_bmax + bh0 * (Npad / kBqB) + (r_first - bh0 * Npad) / kBqB, __float_as_uint(mx));
     }
@@ -543,22 +571,25 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
 
 // Deterministic mode: per head, the largest |v_j| and the largest |k_jc| (atomicMax
 // on float bits, both >= 0).  A block of 256 threads covers 256 rows of one head
-// (16 threads per row, 8 elements each, 16 rows per pass) and issues one atomic
-// per value.
+// (D / 8 threads per row, 8 elements each, 256 / (D / 8) rows per pass) and issues
+// one atomic per value.
 constexpr int kBoundRows = 256;
+template <int D>
 __global__ void __launch_bounds__(256) bwd_kv_bound_kernel(const __nv_bfloat16* __restrict__ k,
                                                            const __nv_bfloat16* __restrict__ v,
                                                            unsigned int* __restrict__ kv_max, int N, int H,
                                                            Strides sk, Strides sv) {
+  constexpr int kTpr = D / 8;
+  constexpr int kRpp = 256 / kTpr;  // rows per pass
   const int bh = blockIdx.y;
-  const int t = threadIdx.x & 15;
-  const int r0 = blockIdx.x * kBoundRows + (threadIdx.x >> 4);
+  const int t = threadIdx.x % kTpr;
+  const int r0 = blockIdx.x * kBoundRows + (threadIdx.x / kTpr);
   float km = 0.f, vm = 0.f;
   // Every thread runs all passes (the shuffles below need the whole warp); rows
   // past N contribute zeros.
 #pragma unroll 1
-  for (int pass = 0; pass < kBoundRows / 16; ++pass) {
-    const int r = r0 + pass * 16;
+  for (int pass = 0; pass < kBoundRows / kRpp; ++pass) {
+    const int r = r0 + pass * kRpp;
     uint4 kv4 = make_uint4(0, 0, 0, 0), vv4 = make_uint4(0, 0, 0, 0);
     if (r < N) {
       kv4 = *reinterpret_cast<const uint4*>(k + row_offset(sk, bh, H, r) + t * 8);
@@ -575,7 +606,7 @@ __global__ void __launch_bounds__(256) bwd_kv_bound_kernel(const __nv_bfloat16* 
       vn = fmaf(b.x, b.x, fmaf(b.y, b.y, vn));
     }
 #pragma unroll
-    for (int m = 8; m >= 1; m >>= 1) vn += __shfl_xor_sync(0xffffffffu, vn, m, 16);
+    for (int m = kTpr / 2; m >= 1; m >>= 1) vn += __shfl_xor_sync(0xffffffffu, vn, m, kTpr);
     vm = fmaxf(vm, sqrtf(vn));
   }
 #pragma unroll
@@ -601,7 +632,7 @@ __global__ void __launch_bounds__(256) bwd_kv_bound_kernel(const __nv_bfloat16* 
 
 // dQ = bf16(scale * dQacc), 8 elements per thread.  Deterministic mode: the
 // accumulator holds integers in units of 2^-S of the row block's shift S.
-template <bool DET>
+template <int D, bool DET>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ dq_acc,
                                                              __nv_bfloat16* __restrict__ dq, float scale,
                                                              long long n8, const float* __restrict__ dq_bmax,
@@ -611,7 +642,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
   if (idx >= n8) return;
   float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * idx];
   float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * idx + 1];
-  const long long row = idx * 8 / kD;  // (bh, query row) flattened
+  const long long row = idx * 8 / D;  // (bh, query row) flattened
   const long long bh = row / N;
   const int qrow = static_cast<int>(row - bh * N);
   if (DET) {
@@ -625,7 +656,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
   out.y = pack_bf16x2(a.z * scale, a.w * scale);
   out.z = pack_bf16x2(b.x * scale, b.y * scale);
   out.w = pack_bf16x2(b.z * scale, b.w * scale);
-  *reinterpret_cast<uint4*>(dq + row_offset(sdq, bh, H, qrow) + (idx * 8) % kD) = out;
+  *reinterpret_cast<uint4*>(dq + row_offset(sdq, bh, H, qrow) + (idx * 8) % D) = out;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -646,7 +677,10 @@ BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
   return w;
 }
 
-cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream) {
+namespace {
+
+template <int D>
+cudaError_t launch_bwd_prep_d(const BwdArgs& a, cudaStream_t stream) {
   const int BH = a.B * a.H;
   const BwdWorkspace w = bwd_workspace_layout(a.B, a.H, a.N, a.d);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -656,35 +690,37 @@ cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream) {
     // The block and head maxima are built with atomicMax from zero.
     cudaError_t e = cudaMemsetAsync(ws + w.off_dqmax, 0, w.total - w.off_dqmax, stream);
     if (e) return e;
-    bwd_kv_bound_kernel<<<dim3(static_cast<unsigned>((a.N + kBoundRows - 1) / kBoundRows), BH), 256, 0, stream>>>(
+    bwd_kv_bound_kernel<D><<<dim3(static_cast<unsigned>((a.N + kBoundRows - 1) / kBoundRows), BH), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.v),
         reinterpret_cast<unsigned int*>(ws + w.off_kvmax), a.N, a.H, a.sk, a.sv);
     if ((e = cudaGetLastError())) return e;
   }
-  auto kern = a.deterministic ? bwd_preprocess_kernel<true> : bwd_preprocess_kernel<false>;
-  kern<<<static_cast<unsigned>((rows_pad + 15) / 16), 256, 0, stream>>>(
+  constexpr int kRpb = 256 / (D / 8);
+  auto kern = a.deterministic ? bwd_preprocess_kernel<D, true> : bwd_preprocess_kernel<D, false>;
+  kern<<<static_cast<unsigned>(rows_pad / kRpb), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
       reinterpret_cast<float*>(ws + w.off_d), reinterpret_cast<float*>(ws + w.off_lse2),
       reinterpret_cast<float*>(ws + w.off_dq), dq_bmax, a.N, w.npad, rows_pad, a.H, a.so, a.sdo);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
-  using C = BwdCfg;
+template <int D>
+cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
   const int BH = a.B * a.H;
   const BwdWorkspace w = bwd_workspace_layout(a.B, a.H, a.N, a.d);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   cudaError_t e;
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   constexpr auto kBf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if ((e = make_tmap_4d(&tq, a.q, kBf16, 2, kD, a.N, a.H, a.B, a.sq.s, 64, kBqB))) return e;
-  if ((e = make_tmap_4d(&tdo, a.dout, kBf16, 2, kD, a.N, a.H, a.B, a.sdo.s, 64, kBqB))) return e;
-  if ((e = make_tmap_4d(&tk, a.k, kBf16, 2, kD, a.N, a.H, a.B, a.sk.s, 64, kBkB))) return e;
-  if ((e = make_tmap_4d(&tv, a.v, kBf16, 2, kD, a.N, a.H, a.B, a.sv.s, 64, kBkB))) return e;
-  if ((e = make_tmap_4d(&tdk, a.dk, kBf16, 2, kD, a.N, a.H, a.B, a.sdk.s, 64, kBkB))) return e;
-  if ((e = make_tmap_4d(&tdv, a.dv, kBf16, 2, kD, a.N, a.H, a.B, a.sdv.s, 64, kBkB))) return e;
-  auto kern = a.deterministic ? (a.causal ? bwd_main_kernel<true, true> : bwd_main_kernel<false, true>)
-                              : (a.causal ? bwd_main_kernel<true, false> : bwd_main_kernel<false, false>);
+  if ((e = make_tmap_4d(&tq, a.q, kBf16, 2, D, a.N, a.H, a.B, a.sq.s, 64, kBqB))) return e;
+  if ((e = make_tmap_4d(&tdo, a.dout, kBf16, 2, D, a.N, a.H, a.B, a.sdo.s, 64, kBqB))) return e;
+  if ((e = make_tmap_4d(&tk, a.k, kBf16, 2, D, a.N, a.H, a.B, a.sk.s, 64, kBkB))) return e;
+  if ((e = make_tmap_4d(&tv, a.v, kBf16, 2, D, a.N, a.H, a.B, a.sv.s, 64, kBkB))) return e;
+  if ((e = make_tmap_4d(&tdk, a.dk, kBf16, 2, D, a.N, a.H, a.B, a.sdk.s, 64, kBkB))) return e;
+  if ((e = make_tmap_4d(&tdv, a.dv, kBf16, 2, D, a.N, a.H, a.B, a.sdv.s, 64, kBkB))) return e;
+  auto kern = a.deterministic ? (a.causal ? bwd_main_kernel<D, true, true> : bwd_main_kernel<D, false, true>)
+                              : (a.causal ? bwd_main_kernel<D, true, false> : bwd_main_kernel<D, false, false>);
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes))) return e;
   // The register split assumes the block launches with kLaunchRegs per thread.
   cudaFuncAttributes fattr;
@@ -699,16 +735,31 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream) {
+template <int D>
+cudaError_t launch_bwd_dq_d(const BwdArgs& a, cudaStream_t stream) {
   const BwdWorkspace w = bwd_workspace_layout(a.B, a.H, a.N, a.d);
   const uint8_t* ws = static_cast<const uint8_t*>(a.workspace);
   const float* dq_acc = reinterpret_cast<const float*>(ws + w.off_dq);
-  const long long n8 = static_cast<long long>(a.B) * a.H * a.N * kD / 8;
-  auto kern = a.deterministic ? bwd_dq_convert_kernel<true> : bwd_dq_convert_kernel<false>;
+  const long long n8 = static_cast<long long>(a.B) * a.H * a.N * D / 8;
+  auto kern = a.deterministic ? bwd_dq_convert_kernel<D, true> : bwd_dq_convert_kernel<D, false>;
   kern<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
       dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.scale, n8, reinterpret_cast<const float*>(ws + w.off_dqmax),
       reinterpret_cast<const float*>(ws + w.off_kvmax), a.N, w.npad, a.H, a.sdq);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream) {
+  return a.d == 64 ? launch_bwd_prep_d<64>(a, stream) : launch_bwd_prep_d<128>(a, stream);
+}
+
+cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
+  return a.d == 64 ? launch_bwd_main_d<64>(a, stream) : launch_bwd_main_d<128>(a, stream);
+}
+
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream) {
+  return a.d == 64 ? launch_bwd_dq_d<64>(a, stream) : launch_bwd_dq_d<128>(a, stream);
 }
 
 cudaError_t launch_bwd_bf16(const BwdArgs& a, cudaStream_t stream) {
