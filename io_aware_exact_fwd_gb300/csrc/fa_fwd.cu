@@ -63,8 +63,13 @@ constexpr uint32_t kTmemCols = 512;
 // (then every P <= 2^16, far from fp32 overflow even after accumulation).
 constexpr float kSpeculationSumBound = 65536.0f;
 // FP8 keeps a per-block maximum and moves its reference only when a block's
-// maximum exceeds it by more than 2^8 (log2 units), so P <= 256 < 448 (e4m3).
-constexpr float kRescaleThreshold = 8.0f;
+// maximum exceeds it by more than 8.75 (log2 units), so P <= 2^8.75 = 430.5 < 448,
+// inside e4m3's range.  A unit's first reference is its first block's maximum
+// plus kFirstBlockHeadroom: on inputs with outliers later blocks often exceed the
+// first one's maximum, and each move of the reference costs a rescale of O.  Two
+// binades keep the first block's P <= 1/4, well above e4m3's subnormal range.
+constexpr float kRescaleThreshold = 8.75f;
+constexpr float kFirstBlockHeadroom = 2.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 // Sites recorded in the error word when a wait expires.
@@ -493,6 +498,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         inv_svmax = 1.f / mxv;
         crow = scale_log2 * (qrow < N ? f8.sq[hb + qrow / 64] : 1.f);
       }
+      // FP8: the K and V tile scales of the next key block, loaded one block ahead
+      // so that no global load sits between S becoming ready and the exponentials.
+      float nsk[2] = {1.f, 1.f}, nsv[2] = {svmax, svmax};
+      auto fetch_scales = [&](int jj) {
+        if constexpr (FP8) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int kt = 2 * (span.begin + jj) + h;
+            const bool in = jj < nkt && kt < f8.ntiles;
+            nsk[h] = in ? skh[kt] : 1.f;
+            nsv[h] = in ? svh[kt] : svmax;
+          }
+        }
+      };
+      fetch_scales(0);
 
       for (int j = 0; j < nkt; ++j, ++scnt) {
         if (!warp_wait(&bar_s[t], scnt & 1, wc, kSiteSoftS)) {
@@ -505,17 +525,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need_mask = (kbase + kBlockK > ks.Nk) || (CAUSAL && kbase + kBlockK - 1 > qrow0 + ks.coff);
         // Per 64-key half h: multiplier c[h] of the raw score (FP8: times that key
         // tile's K scale) and lg[h] = log2 of the V-scale fold of P (0 for bf16).
-        float ch[2] = {crow, crow}, lg[2] = {0.f, 0.f}, fv[2] = {1.f, 1.f};
+        // The tile scales are powers of two (fa_fp8_prepare), so the fold
+        // fv = sV / max sV is exact and its log2 is the difference of the two
+        // exponent fields.
+        float ch[2] = {crow, crow}, lg[2] = {0.f, 0.f}, fv[2] = {1.f, 1.f}, inv_fv[2] = {1.f, 1.f};
         if constexpr (FP8) {
   #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int kt = 2 * (span.begin + j) + h;
-            if (kt < f8.ntiles) {
-              ch[h] = crow * skh[kt];
-              fv[h] = svh[kt] * inv_svmax;
-              lg[h] = __log2f(fv[h]);
-            }
+            ch[h] = crow * nsk[h];
+            fv[h] = nsv[h] * inv_svmax;
+            const int lgi = static_cast<int>((__float_as_uint(nsv[h]) >> 23) & 0xFFu) -
+                            static_cast<int>((__float_as_uint(svmax) >> 23) & 0xFFu);  // <= 0
+            lg[h] = static_cast<float>(lgi);
+            // 1 / fv = 2^-lgi, exact.  (Dividing the row sums by fv instead would take
+            // the division's slow path on rows whose sums are tiny after their
+            // reference moved far up.)
+            inv_fv[h] = lgi >= -127 ? __uint_as_float(static_cast<uint32_t>(127 - lgi) << 23) : svmax / nsv[h];
           }
+          fetch_scales(j + 1);
         }
         uint32_t r[4][32];
         auto load_and_mask = [&](int c) {
@@ -575,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto tile_sum = [&]() {
           // l counts the unscaled P: undo the V-scale fold of each half.
-          return (part[0].x + part[0].y) / fv[0] + (part[1].x + part[1].y) / fv[1];
+          return (part[0].x + part[0].y) * inv_fv[0] + (part[1].x + part[1].y) * inv_fv[1];
         };
 
         // O_t is rescaled (in TMEM) by alpha for rows whose reference maximum moves
@@ -598,6 +625,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         };
 
+        // FP8: O rescaled after this block's exponentials (the scores are dead by
+        // then, so all of O_t's columns are loaded at once), before P_t is signalled.
+        auto rescale_o_all = [&](float alpha) {
+          uint32_t o[D / 32][32];
+  #pragma unroll
+          for (int c = 0; c < D / 32; ++c) tmem_ld32(trow + col_o + c * 32, o[c]);
+  #pragma unroll
+          for (int c = 0; c < D / 32; ++c) tmem_ld_wait32(o[c]);
+          const float2 a2 = make_float2(alpha, alpha);
+  #pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+  #pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[c][i]), __uint_as_float(o[c][i + 1])), a2);
+              o[c][i] = __float_as_uint(v.x);
+              o[c][i + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(trow + col_o + c * 32, o[c]);
+          }
+        };
+
         float l_tile;
         if (j == 0 || FP8) {
           // The block's own maximum first.  First block: it is the reference
@@ -613,23 +661,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   #pragma unroll
           for (int c = 0; c < 4; ++c) load_and_mask(c);
           const float mt = tile_max();
+          float alpha = 1.f;
+          bool any_rescale = false;
           if (j == 0) {
-            m_used = (mt == -INFINITY) ? 0.f : mt;
+            m_used = (mt == -INFINITY) ? 0.f : mt + (FP8 ? kFirstBlockHeadroom : 0.f);
           } else {
             const float m_new = fmaxf(m_used, mt);
             const bool need = m_new > m_used + kRescaleThreshold;
-            float alpha = 1.f;
             if (need) {
               alpha = ex2_approx(m_used - m_new);
               m_used = m_new;
             }
             l *= alpha;
-            rescale_o(alpha, __any_sync(0xffffffffu, need));
+            any_rescale = __any_sync(0xffffffffu, need);
           }
           part[0] = part[1] = make_float2(0.f, 0.f);
   #pragma unroll
           for (int c = 0; c < 4; ++c) exp_chunk(c);
           l_tile = tile_sum();
+          if (any_rescale) rescale_o_all(alpha);  // only FP8 reaches here with j > 0
         } else {
           // bf16, later blocks: exponentiate against the running maximum without
           // looking for a new one.  This is exact as long as no P overflows, which
