@@ -39,13 +39,11 @@
 #include <math.h>
 
 #include "fa_device.cuh"
+#include "fa_fwd_units.cuh"
 #include "fa_internal.h"
 
 namespace fa {
 namespace {
-
-constexpr int kTiles = 2;                       // query tiles per CTA
-constexpr int kRowsPerCta = kTiles * kBlockQ;   // 256 query rows
 constexpr int kThreads = 384;                   // warps 0-7 softmax (2 groups), 8 K/V TMA, 9 MMA, 10 Q TMA, 11 spare
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
@@ -64,12 +62,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kSpeculationSumBound = 65536.0f;
 // FP8 keeps a per-block maximum and moves its reference only when a block's
 // maximum exceeds it by more than 8.75 (log2 units), so P <= 2^8.75 = 430.5 < 448,
-// inside e4m3's range.  A unit's first reference is its first block's maximum
-// plus kFirstBlockHeadroom: on inputs with outliers later blocks often exceed the
-// first one's maximum, and each move of the reference costs a rescale of O.  Two
-// binades keep the first block's P <= 1/4, well above e4m3's subnormal range.
+// inside e4m3's range.
 constexpr float kRescaleThreshold = 8.75f;
-constexpr float kFirstBlockHeadroom = 2.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 // Sites recorded in the error word when a wait expires.
@@ -115,70 +109,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   const bool ok = mbar_wait(bar, parity, wc, site);
   return __all_sync(0xffffffffu, ok);
 }
-
-// Key range of a launch and where its results go.  The plain forward has one
-// split covering all Nk = N keys.  The split-KV forward cuts the key blocks into
-// nsplit ranges of kbps blocks (split s: blocks [s kbps, (s+1) kbps)), aligns
-// causal queries with the last keys (query i sees key j iff j <= i + coff,
-// coff = Nk - Nq), and writes each split's normalised O (fp32) and LSE to
-// o_part [nsplit, BH, Nq, d] and lse_part [nsplit, BH, Nq].
-struct KeySplit {
-  int Nk;
-  int nsplit;
-  int kbps;
-  int coff;
-  float* o_part;
-  float* lse_part;
-};
-
-// K/V blocks [begin, begin + count) that query tile t of unit (u, split s) attends
-// to; count = 0 if the tile is past the last query row.
-struct KvSpan {
-  int begin, count;
-};
-template <bool CAUSAL>
-__device__ __forceinline__ KvSpan kv_span(int u, int t, int s, int N, const KeySplit& ks) {
-  const int row0 = u * kRowsPerCta + t * kBlockQ;
-  if (row0 >= N) return {0, 0};
-  const int nkb = (ks.Nk + kBlockK - 1) / kBlockK;
-  const int b = min(s * ks.kbps, nkb);
-  int e = min(b + ks.kbps, nkb);
-  // The tile's last row sees keys up to its index + coff.
-  if (CAUSAL) e = min(e, (min(row0 + kBlockQ - 1, N - 1) + ks.coff) / kBlockK + 1);
-  return {b, max(e - b, 0)};
-}
-
-// Dequantisation scales of the FP8 variant (unused by the bf16 one): per
-// 64-row tile of each head, [BH, ntiles].
-struct Fp8Scales {
-  const float* sq;
-  const float* sk;
-  const float* sv;
-  int ntiles;
-};
-
-// Work unit w -> (256-row query block u, head bh, key split s).  Causal units
-// are numbered heaviest first (largest u first), so the zigzag assignment below
-// hands every CTA a similar total.
-template <bool CAUSAL>
-__device__ __forceinline__ void decode_unit(int w, int nunits, int BH, int nsplit, int& u, int& bh, int& s) {
-  if (CAUSAL) {
-    const int per_u = BH * nsplit;
-    u = nunits - 1 - w / per_u;
-    const int r = w % per_u;
-    bh = r / nsplit;
-    s = r % nsplit;
-  } else {
-    u = w % nunits;
-    const int r = w / nunits;
-    s = r % nsplit;
-    bh = r / nsplit;
-  }
-}
-
-// k-th unit of CTA c out of G persistent CTAs: pass k covers units kG .. kG+G-1,
-// in increasing CTA order on even passes and decreasing on odd ones.
-__device__ __forceinline__ int unit_of(int k, int c, int G) { return k * G + ((k & 1) ? (G - 1 - c) : c); }
 
 template <int D, bool CAUSAL, bool FP8, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -664,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float alpha = 1.f;
           bool any_rescale = false;
           if (j == 0) {
-            m_used = (mt == -INFINITY) ? 0.f : mt + (FP8 ? kFirstBlockHeadroom : 0.f);
+            m_used = (mt == -INFINITY) ? 0.f : mt;
           } else {
             const float m_new = fmaxf(m_used, mt);
             const bool need = m_new > m_used + kRescaleThreshold;
