@@ -12,11 +12,17 @@
 //   dS    = P * (dP - D)    dQ = scale * dS K          dK = scale * dS^T Q
 //
 // Three launches on one stream:
-//  1. bwd_preprocess: D_i, LSE_i * log2(e) (padded rows get +inf so their P is
-//     exactly 0), and zeroing of the fp32 dQ accumulator.
+//  1. bwd_preprocess: D_i and LSE_i * log2(e), written as the per-query operand
+//     tiles of that extra K-step (padded rows get a huge negative LSE term so their
+//     P is exactly 0), and zeroing of the fp32 dQ accumulator.
 //  2. bwd_main: one CTA per (128-key block, head), the K/V-outer loop order.
-//     K_j, V_j stay in shared memory; Q_i, dO_i (64 query rows), LSE_i and D_i
-//     stream through a TMA ring.  Per query block, tcgen05 MMAs compute
+//     K_j, V_j stay in shared memory; Q_i, dO_i (64 query rows) and two small
+//     per-query tiles stream through a TMA ring.  The per-query terms LSE_i and D_i
+//     enter the tensor core instead of the compute warps: S^T and dP^T get one
+//     more K-step of 16 columns whose product is -LSE_i * log2(e) / (scale log2 e)
+//     (resp. -D_i) in every key row, so the accumulators hold scale^-1 log2 P
+//     and dP - D directly and the compute warps read no per-query value from
+//     shared memory.  Per query block, tcgen05 MMAs compute
 //     S^T = K Q_i^T and dP^T = V dO_i^T into TMEM (keys on TMEM lanes, so a
 //     thread owns one key row; two warpgroups split the 64 query columns),
 //     eight warps form P^T and dS^T in registers and write them back to TMEM
@@ -85,16 +91,24 @@ struct BwdCfg {
   static constexpr int kQTile = kBqB * D * 2;           // 16 KB (d=128), 8 KB (d=64)
   static constexpr int kStageQ = 0;
   static constexpr int kStageDO = kQTile;
-  static constexpr int kStageL = 2 * kQTile;            // 64 floats
-  static constexpr int kStageD = 2 * kQTile + 256;      // 64 floats
-  static constexpr int kStageTx = 2 * kQTile + 512;     // bytes landing per stage
-  static constexpr int kStageBytes = D == 128 ? 34816 : (kStageTx + 1023) / 1024 * 1024;
+  // The extra K-step's per-query tiles (64 rows x 32 bytes, 32-byte swizzle):
+  // [a1 a2 a3 a1 a2 a3 a1 a2 a3 0...] with a1 + a2 + a3 = -LSE2 for S^T, then
+  // [d1 d2 d3 0...] with d1 + d2 + d3 = -D for dP^T (three-term bf16 splits).
+  static constexpr int kAugTile = kBqB * 32;           // 2 KB
+  static constexpr int kStageAug = 2 * kQTile;
+  static constexpr int kStageTx = 2 * kQTile + 2 * kAugTile;  // bytes landing per stage
+  static constexpr int kStageBytes = (kStageTx + 1023) / 1024 * 1024;
   static constexpr int kDsBytes = kBkB * kBqB * 2;      // 16 KB: 128 key rows x 128 B
-  // K, then (d = 64) the zero box that pads K^T to the dQ^T MMA's 128 rows, then V.
+  // K, then (d = 64) the zero box that pads K^T to the dQ^T MMA's 128 rows, then V,
+  // then the extra K-step's constant key-side tiles (128 rows x 32 bytes each):
+  // [c1 c1 c1 c2 c2 c2 c3 c3 c3 0...] with c1 + c2 + c3 = 1 / (scale log2 e) for S^T
+  // (so the nine products sum to (c1 + c2 + c3)(a1 + a2 + a3)), [1 1 1 0...] for dP^T.
   static constexpr int kKOff = 0;
   static constexpr int kZeroOff = kKVTile;
   static constexpr int kVOff = kKVTile + (D == 64 ? kKVBox : 0);
-  static constexpr int kRingOff = kVOff + kKVTile;
+  static constexpr int kKAugOff = kVOff + kKVTile;
+  static constexpr int kVAugOff = kKAugOff + kBkB * 32;
+  static constexpr int kRingOff = kVAugOff + kBkB * 32;
   static constexpr int kDsOff = kRingOff + kStages * kStageBytes;
   static constexpr int kBarOff = kDsOff + 2 * kDsBytes;
   // kv, full[S], empty[S], sdp, sde, comp[2], dqf[2], dqe[2], dkv, epi, drain
@@ -107,6 +121,7 @@ struct BwdCfg {
   static constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 320;
   static __device__ __forceinline__ uint32_t col_pdq(int b) { return 384u + 64u * b; }
   static_assert(kStageTx <= kStageBytes, "stage layout");
+  static_assert(kZeroOff % 1024 == 0 && kKAugOff % 1024 == 0 && kRingOff % 1024 == 0, "operand tile alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -136,6 +151,19 @@ __device__ __forceinline__ int det_shift(float dq_block_max, float vmax, float k
   return max(-100, min(100, 22 - e));
 }
 __device__ __forceinline__ float pow2f(int s) { return __int_as_float((s + 127) << 23); }  // -126 <= s <= 127
+
+// Three-term bf16 split of x: t1 = bf16(x), t2 = bf16(x - t1), t3 = bf16(x - t1 - t2)
+// (each difference exact in fp32), so t1 + t2 + t3 carries about 24 significant
+// bits of x.  Returned as raw bf16 bits.
+__device__ __forceinline__ void split3_bf16(float x, uint32_t (&t)[3]) {
+  float r = x;
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(r);
+    t[i] = static_cast<uint32_t>(__bfloat16_as_ushort(h));
+    r -= __bfloat162float(h);
+  }
+}
 
 // Element offset of row n of head (b, h) in a strided [B, H, N, d] tensor.
 __device__ __forceinline__ size_t row_offset(const Strides& st, long long bh, int H, int n) {
@@ -170,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                    const float* __restrict__ lse2, const float* __restrict__ dvec, float* __restrict__ dq_acc,
+                    const uint8_t* __restrict__ aug, float* __restrict__ dq_acc,
                     const float* __restrict__ dq_bmax, const float* __restrict__ kv_max, int N, int Npad, int H,
                     int BH, int nkb, float scale, float scale_log2, unsigned int* err_word, unsigned long long wait_ns) {
   using C = BwdCfg<D>;
@@ -234,6 +262,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Rows 64..127 of the dQ^T MMA's A operand: zeros, read by the tensor core.
     uint4* z = reinterpret_cast<uint4*>(smem + C::kZeroOff);
     for (int i = threadIdx.x; i < C::kKVBox / 16; i += kThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  {
+    // The extra K-step's key-side tiles: one 16-byte half-row per thread (128 rows,
+    // two halves, two tiles = 512 stores), at its 32-byte-swizzle position.
+    const int tile = threadIdx.x >> 8, krow = (threadIdx.x >> 1) & 127, half = threadIdx.x & 1;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (tile == 0) {
+      uint32_t c[3];
+      split3_bf16(1.f / scale_log2, c);
+      // elements 0-7: c1 c1 c1 c2 c2 c2 c3 c3; element 8: c3
+      val = half == 0 ? make_uint4(c[0] | (c[0] << 16), c[0] | (c[1] << 16), c[1] | (c[1] << 16), c[2] | (c[2] << 16))
+                      : make_uint4(c[2], 0u, 0u, 0u);
+    } else if (half == 0) {
+      val = make_uint4(0x3F803F80u, 0x3F80u, 0u, 0u);  // bf16 1.0, 1.0, 1.0
+    }
+    uint8_t* base = smem + (tile == 0 ? C::kKAugOff : C::kVAugOff);
+    *reinterpret_cast<uint4*>(base + krow * 32 + ((half ^ ((krow >> 2) & 1)) << 4)) = val;
     fence_proxy_async_smem();
   }
   if (warp == kWarpMma) tmem_alloc(tmem_slot, kTmemCols);
@@ -242,8 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, err_word, wait_ns};
-  const float* lse2_h = lse2 + static_cast<size_t>(bh) * Npad;
-  const float* dvec_h = dvec + static_cast<size_t>(bh) * Npad;
+  const uint8_t* aug_h = aug + static_cast<size_t>(bh) * (Npad / kBqB) * (2 * C::kAugTile);
 
   if (warp >= kWarpCtl) {
    regs_decrease<kRegsControl>();
@@ -266,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(st + C::kStageQ + b * C::kQBox, &tm_q, &bar_full[slot], b * 64, i * kBqB, h_idx, b_idx);
           tma_load_4d(st + C::kStageDO + b * C::kQBox, &tm_do, &bar_full[slot], b * 64, i * kBqB, h_idx, b_idx);
         }
-        bulk_load(st + C::kStageL, lse2_h + i * kBqB, kBqB * 4, &bar_full[slot]);
-        bulk_load(st + C::kStageD, dvec_h + i * kBqB, kBqB * 4, &bar_full[slot]);
+        bulk_load(st + C::kStageAug, aug_h + static_cast<size_t>(i) * (2 * C::kAugTile), 2 * C::kAugTile,
+                  &bar_full[slot]);
         ++issued;
       }
       if (issued < n) {  // aborted: let the copies already in flight land
@@ -298,6 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t ring_kmaj = sdesc_sw128(smem_u32(sRing), 16, 1024);
       const uint64_t ring_mn = sdesc_sw128(smem_u32(sRing), C::kQBox, 1024);
       const uint64_t ds_mn = sdesc_sw128(smem_u32(sDs), 16, 1024);
+      const uint64_t kaug = sdesc_sw32(smem_u32(smem + C::kKAugOff));
+      const uint64_t vaug = sdesc_sw32(smem_u32(smem + C::kVAugOff));
+      const uint64_t ring_aug = sdesc_sw32(smem_u32(sRing + C::kStageAug));
       bool ok = mbar_wait(bar_kv, 0, wc, kSiteBMmaKV);
       if (warp == kWarpMmaS) {
         // S^T = K Q_i^T and dP^T = V dO_i^T for local step `it`, as soon as the
@@ -315,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ss(tmem + C::kColS, sdesc_add(k_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageQ + offb),
                         idesc_sdp, kk > 0 ? 1u : 0u);
           }
+          mma_bf16_ss(tmem + C::kColS, kaug, sdesc_add(ring_aug, st), idesc_sdp, 1u);  // - LSE2 / (scale log2 e)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
@@ -322,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ss(tmem + C::kColDP, sdesc_add(v_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageDO + offb),
                         idesc_sdp, kk > 0 ? 1u : 0u);
           }
+          mma_bf16_ss(tmem + C::kColDP, vaug, sdesc_add(ring_aug, st + C::kAugTile), idesc_sdp, 1u);  // - D
           mma_commit(bar_sdp);
         }
       } else {
@@ -373,10 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int it = 0; it < n; ++it) {
       const int b = it & 1;
-      const int slot = it % kStages;
       const int i = i0 + it;
       if (!(ok = warp_wait_b(bar_sdp, it & 1, wc, kSiteBComp))) break;
-      if (!(ok = warp_wait_b(&bar_full[slot], (it / kStages) & 1, wc, kSiteBComp))) break;
       tc_fence_after();
       uint32_t s[32], dp[32];
       tmem_ld32(trow + C::kColS + 32 * g, s);
@@ -386,30 +433,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_sde);  // the MMA warp may now overwrite S^T, dP^T
-      const uint8_t* st = sRing + slot * C::kStageBytes;
-      const float4* l4 = reinterpret_cast<const float4*>(st + C::kStageL) + 8 * g;
-      const float4* d4 = reinterpret_cast<const float4*>(st + C::kStageD) + 8 * g;
       const bool diag = CAUSAL && (i * kBqB < kb * kBkB + kBkB);  // some query in this block precedes a key
       const int q0 = i * kBqB + 32 * g;
       uint32_t ppk[16], dpk[16];
 #pragma unroll
-      for (int gg = 0; gg < 8; ++gg) {
-        const float4 lv = l4[gg];
-        const float4 dv = d4[gg];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = gg * 4 + 2 * e;
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2,
-                                      e == 0 ? make_float2(-lv.x, -lv.y) : make_float2(-lv.z, -lv.w));
-          float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          if (!key_valid || (diag && key > q0 + c)) p.x = 0.f;
-          if (!key_valid || (diag && key > q0 + c + 1)) p.y = 0.f;
-          const float2 dd = __fadd2_rn(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
-                                       e == 0 ? make_float2(-dv.x, -dv.y) : make_float2(-dv.z, -dv.w));
-          const float2 ds = __fmul2_rn(p, dd);
-          ppk[2 * gg + e] = pack_bf16x2(p.x, p.y);
-          dpk[2 * gg + e] = pack_bf16x2(ds.x, ds.y);
-        }
+      for (int c2 = 0; c2 < 16; ++c2) {
+        const int c = 2 * c2;
+        // S^T holds S - LSE2 / (scale log2 e) and dP^T holds dP - D (the extra K-step).
+        const float2 x = __fmul2_rn(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2);
+        float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if (!key_valid || (diag && key > q0 + c)) p.x = 0.f;
+        if (!key_valid || (diag && key > q0 + c + 1)) p.y = 0.f;
+        const float2 ds = __fmul2_rn(p, make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])));
+        ppk[c2] = pack_bf16x2(p.x, p.y);
+        dpk[c2] = pack_bf16x2(ds.x, ds.y);
       }
       // P^T, dS^T(it) overwrite dQ^T(it-2) (TMEM) and dS^T(it-2) (shared memory).
       if (it >= 2 && !(ok = warp_wait_b(&bar_dqe[b], ((it - 2) >> 1) & 1, wc, kSiteBComp))) break;
@@ -504,13 +541,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// D_i = sum_c dO_ic O_ic ; LSE2_i = LSE_i * log2(e) (rows >= N: D = 0, LSE2 = +inf);
+// D_i = sum_c dO_ic O_ic and LSE2_i = LSE_i * log2(e), written as row i of the
+// main kernel's per-query operand tiles (64 rows x 32 bytes each, 32-byte swizzle,
+// one pair per 64-row query block): [a1 a2 a3 a1 a2 a3 a1 a2 a3 0...] with
+// a1 + a2 + a3 = -LSE2 and [d1 d2 d3 0...] with d1 + d2 + d3 = -D (three-term bf16
+// splits).  Rows >= N get -LSE2 = -1e30 (their P is exactly 0) and D = 0.
 // dQacc rows < N are zeroed.  D / 8 threads per row, 8 elements each.
 template <int D, bool DET>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                              const __nv_bfloat16* __restrict__ dout,
-                                                             const float* __restrict__ lse, float* __restrict__ dvec,
-                                                             float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                             const float* __restrict__ lse, uint8_t* __restrict__ aug,
+                                                             float* __restrict__ dq_acc,
                                                              unsigned int* __restrict__ dq_bmax, int N, int Npad,
                                                              long long rows_pad, int H, Strides so, Strides sdo) {
   constexpr int kTpr = D / 8;          // threads per row
@@ -546,8 +587,18 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
 #pragma unroll
   for (int m = kTpr / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m, kTpr);
   if (t == 0) {
-    dvec[r] = nrow < N ? acc : 0.f;
-    lse2[r] = nrow < N ? lse[static_cast<size_t>(bh) * N + nrow] * kLog2e : INFINITY;
+    uint32_t a[3], dd[3];
+    split3_bf16(nrow < N ? -lse[static_cast<size_t>(bh) * N + nrow] * kLog2e : -1e30f, a);
+    split3_bf16(nrow < N ? -acc : 0.f, dd);
+    const int rr = nrow % kBqB;
+    uint8_t* tile = aug + (static_cast<size_t>(r / kBqB)) * (2 * kBqB * 32);  // r / 64 = (bh, query block)
+    const int h0 = ((rr >> 2) & 1) << 4, h1 = (1 ^ ((rr >> 2) & 1)) << 4;     // swizzled half-row positions
+    // elements 0-7: a1 a2 a3 a1 a2 a3 a1 a2; element 8: a3
+    *reinterpret_cast<uint4*>(tile + rr * 32 + h0) =
+        make_uint4(a[0] | (a[1] << 16), a[2] | (a[0] << 16), a[1] | (a[2] << 16), a[0] | (a[1] << 16));
+    *reinterpret_cast<uint4*>(tile + rr * 32 + h1) = make_uint4(a[2], 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(tile + kBqB * 32 + rr * 32 + h0) = make_uint4(dd[0] | (dd[1] << 16), dd[2], 0u, 0u);
+    *reinterpret_cast<uint4*>(tile + kBqB * 32 + rr * 32 + h1) = make_uint4(0u, 0u, 0u, 0u);
   }
   if (DET) {
     // The block's rows lie in one 64-row query block (Npad and the block start are
@@ -669,9 +720,8 @@ BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
   const size_t npad = (static_cast<size_t>(N) + kBqB - 1) / kBqB * kBqB;
   w.npad = static_cast<int>(npad);
   w.off_dq = 0;
-  w.off_d = align256(bh * N * d * sizeof(float));
-  w.off_lse2 = w.off_d + align256(bh * npad * sizeof(float));
-  w.off_dqmax = w.off_lse2 + align256(bh * npad * sizeof(float));
+  w.off_aug = align256(bh * N * d * sizeof(float));
+  w.off_dqmax = w.off_aug + align256(bh * npad * 64);  // two 32-byte operand rows per query row
   w.off_kvmax = w.off_dqmax + align256(bh * (npad / kBqB) * sizeof(float));
   w.total = w.off_kvmax + align256(bh * 2 * sizeof(float));
   return w;
@@ -699,8 +749,7 @@ cudaError_t launch_bwd_prep_d(const BwdArgs& a, cudaStream_t stream) {
   auto kern = a.deterministic ? bwd_preprocess_kernel<D, true> : bwd_preprocess_kernel<D, false>;
   kern<<<static_cast<unsigned>(rows_pad / kRpb), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
-      reinterpret_cast<float*>(ws + w.off_d), reinterpret_cast<float*>(ws + w.off_lse2),
-      reinterpret_cast<float*>(ws + w.off_dq), dq_bmax, a.N, w.npad, rows_pad, a.H, a.so, a.sdo);
+      ws + w.off_aug, reinterpret_cast<float*>(ws + w.off_dq), dq_bmax, a.N, w.npad, rows_pad, a.H, a.so, a.sdo);
   return cudaGetLastError();
 }
 
@@ -728,8 +777,7 @@ cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
   if (static_cast<uint32_t>(fattr.numRegs) < kLaunchRegs) return cudaErrorInvalidConfiguration;
   const int nkb = (a.N + kBkB - 1) / kBkB;
   kern<<<static_cast<unsigned>(nkb * BH), kThreads, C::kSmemBytes, stream>>>(
-      tq, tk, tv, tdo, tdk, tdv, reinterpret_cast<const float*>(ws + w.off_lse2),
-      reinterpret_cast<const float*>(ws + w.off_d), reinterpret_cast<float*>(ws + w.off_dq),
+      tq, tk, tv, tdo, tdk, tdv, ws + w.off_aug, reinterpret_cast<float*>(ws + w.off_dq),
       reinterpret_cast<const float*>(ws + w.off_dqmax), reinterpret_cast<const float*>(ws + w.off_kvmax), a.N, w.npad,
       a.H, BH, nkb, a.scale, a.scale * kLog2e, a.err_word, a.dbg.wait_limit_ns);
   return cudaGetLastError();

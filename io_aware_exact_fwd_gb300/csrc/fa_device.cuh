@@ -195,6 +195,20 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// Shared-memory matrix descriptor with the 32-byte swizzle (layout type 6), for
+// K-major tiles whose rows are a single 32-byte K-step (16 bf16): 8-row groups of
+// 256 bytes (SBO); within each group the two 16-byte halves of rows 4-7 swap
+// places (byte-address bit 4 XOR bit 7).  Tiles start on a 256-byte boundary.
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset: unused for swizzled K-major
+  d |= static_cast<uint64_t>(256 >> 4) << 32;             // stride byte offset: 8 rows x 32 bytes
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(6) << 61;
+  return d;
+}
+
 // A descriptor advanced by `bytes` along its start address.  The 14-bit address
 // field holds (address >> 4) of a shared-memory location below 256 KB, so the
 // addition never carries out of the low word: one 32-bit add, no 64-bit math.

@@ -100,12 +100,13 @@ struct BwdArgs {
 };
 
 // Workspace of the backward: fp32 dQ accumulator [BH, N, d] (int32 in the
-// deterministic mode), then D and LSE * log2(e), each [BH, npad] with npad = N
-// rounded up to 64, then (deterministic mode) the largest |dO_i| per 64-row
-// block [BH, npad / 64] and the head's largest |v_j| and |k_jc| [BH, 2].  Every
-// region starts on a 256-byte boundary.
+// deterministic mode), then the main kernel's per-query operand tiles (LSE * log2(e)
+// and D as bf16 hi/lo pairs, 64 bytes per query row, npad = N rounded up to 64
+// rows per head), then (deterministic mode) the largest |dO_i| per 64-row block
+// [BH, npad / 64] and the head's largest |v_j| and |k_jc| [BH, 2].  Every region
+// starts on a 256-byte boundary.
 struct BwdWorkspace {
-  size_t off_dq, off_d, off_lse2, off_dqmax, off_kvmax, total;
+  size_t off_dq, off_aug, off_dqmax, off_kvmax, total;
   int npad;
 };
 BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d);
