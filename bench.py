@@ -364,10 +364,14 @@ def run_ours(args):
         "fwd": {"bound": "tensor", "flops": f_fwd, "bytes": 8 * elems + 4 * B * H * N,
                 "kernel": "fwd_kernel<128,false,bf16>", "profile": "fwd_bf16_B2H16N8192d128.md",
                 "source": "io_aware_exact_fwd_gb300/csrc/fa_fwd.cu"},
-        "bwd_prep": {"bound": "hbm", "bytes": 4 * elems + 4 * B * H * N + 8 * B * H * npad + 4 * elems,
+        # prep: O, dO and LSE read; the LSE/D operand rows (64 B per padded query row) written;
+        # the fp32 dQ accumulator zeroed.
+        "bwd_prep": {"bound": "hbm", "bytes": 4 * elems + 4 * B * H * N + 64 * B * H * npad + 4 * elems,
                      "kernel": "bwd_preprocess_kernel"},
+        # main: Q, K, V, dO read once; dK, dV written; the dQ accumulator read and written once;
+        # the LSE/D operand rows read once.
         "bwd_main": {"bound": "tensor", "flops": 2.5 * f_fwd,
-                     "bytes": 10 * elems + 8 * B * H * npad + 4 * elems + 4 * elems,
+                     "bytes": 8 * elems + 4 * elems + 8 * elems + 64 * B * H * npad,
                      "kernel": "bwd_main_kernel<false>", "profile": "bwd_main_B2H16N8192d128.md",
                      "source": "io_aware_exact_fwd_gb300/csrc/fa_bwd.cu"},
         "bwd_dq": {"bound": "hbm", "bytes": 4 * elems + 2 * elems, "kernel": "bwd_dq_convert_kernel"},
