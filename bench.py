@@ -739,6 +739,151 @@ def run_reference(args):
     return line
 
 
+SWEEP_FWD = ([(1, 2, 128, 64), (4, 16, 2048, 128)]
+             + [(16384 // n, 32, n, 64) for n in (512, 1024, 2048, 4096, 8192, 16384)]
+             + [(16384 // n, 16, n, 128) for n in (512, 1024, 2048, 4096, 8192, 16384)])
+SWEEP_BWD = [(8, 16, 2048, 128), (2, 16, 8192, 128), (8, 32, 2048, 64), (2, 32, 8192, 64)]
+SWEEP_DECODE = [(8, 16, 1, 32768, 128), (1, 16, 1, 131072, 128), (8, 32, 1, 32768, 64), (4, 16, 16, 32768, 128),
+                (1, 16, 128, 65536, 128)]
+SWEEP_W4A16 = [(1, 28672, 8192), (16, 28672, 8192), (64, 28672, 8192), (128, 28672, 8192), (1, 8192, 28672)]
+
+
+def run_sweep(args):
+    """Every configuration of the forward sweep, the backward, FP8, decode and W4A16 rows, one JSON line each.
+
+    Each row is the median of `reps` launches of the public call, with L2 flushed
+    (256 MB write) before each launch, outside the event pair.  Inputs are seeded
+    and synthetic, shaped as the workload names them.  --sweep-filter keeps the
+    rows whose tags (the row's words and key=value pairs of its configuration)
+    contain every token of the filter.
+    """
+    import torch
+
+    import io_aware_exact_fwd_gb300 as fa
+    from synth import normal_qkv, outlier_qkv, rotation_signs, w4a16_inputs
+
+    fa.load_library()
+    peaks = load_peaks()
+    peak, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    reps = max(5, min(args.steps, 20))
+    tokens = (args.sweep_filter or "").split()
+
+    def want(row, cfg):
+        tags = row.split() + [f"{k}={int(v) if isinstance(v, bool) else v}" for k, v in cfg.items()]
+        return all(t in tags for t in tokens)
+
+    def emit(row, cfg, ms, amount, unit, pk, **kw):
+        ach = amount / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+        line = {"row": row, "config": cfg, "ms": round(ms, 5), "achieved": round(ach, 1), "unit": unit, "peak": pk,
+                "frac": round(ach / pk, 4)}
+        line.update(kw)
+        print(json.dumps(line), flush=True)
+
+    def timed(call):
+        for _ in range(3):
+            call()
+        ms = _median_ms(call, reps, flush)
+        fa.fa_sync_check()
+        return ms
+
+    def bf16_inputs(B, H, N, d, seed, with_do=False):
+        x = normal_qkv(B, H, N, d, seed, with_do=with_do)
+        return {n: t.to(torch.bfloat16).cuda() for n, t in x.items()}
+
+    for (B, H, N, d) in SWEEP_FWD:
+        cfgs = [{"B": B, "H": H, "N": N, "d": d, "causal": c} for c in (False, True)]
+        cfgs = [c for c in cfgs if want("bf16 forward", c)]
+        if not cfgs:
+            continue
+        x = bf16_inputs(B, H, N, d, 2)
+        o = torch.empty_like(x["q"])
+        lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+        for cfg in cfgs:
+            c = cfg["causal"]
+            ms = timed(lambda: fa.fa_fwd(x["q"], x["k"], x["v"], o=o, lse=lse, causal=c))
+            emit("bf16 forward", cfg, ms, fwd_flops(B, H, N, d, c), "TFLOP/s", peak)
+        del x, o, lse
+
+    for (B, H, N, d) in SWEEP_BWD:
+        rows = [("bf16 backward" + (" deterministic" if det else ""), {"B": B, "H": H, "N": N, "d": d, "causal": c},
+                 det) for c in (False, True) for det in (False, True)]
+        rows = [r for r in rows if want(r[0], r[1])]
+        if not rows:
+            continue
+        x = bf16_inputs(B, H, N, d, 3, with_do=True)
+        q, k, v, g = x["q"], x["k"], x["v"], x["do"]
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+        for row, cfg, det in rows:
+            c = cfg["causal"]
+            fa.fa_fwd(q, k, v, o=o, lse=lse, causal=c)
+            ms = timed(lambda: fa.fa_bwd(q, k, v, o, g, lse, dq, dk, dv, ws, causal=c, deterministic=det))
+            emit(row, cfg, ms, 2.5 * fwd_flops(B, H, N, d, c), "TFLOP/s", peak, launches=4 if det else 3)
+        del x, q, k, v, g, o, lse, dq, dk, dv, ws
+
+    w8 = FP8_WORKLOAD
+    for d8 in (w8["d"],):
+        B8, H8, N8 = w8["B"], w8["H"], w8["N"]
+        cfg8 = {"B": B8, "H": H8, "N": N8, "d": d8}
+        fwd_cfgs = [dict(cfg8, causal=c) for c in (False, True) if want("FP8 forward", dict(cfg8, causal=c))]
+        if not (want("FP8 prepare (fp32 in)", cfg8) or fwd_cfgs):
+            continue
+        x8 = outlier_qkv(B8, H8, N8, d8, w8["seed"])
+        q8, k8, v8 = (x8[n].cuda() for n in ("q", "k", "v"))
+        del x8
+        signs = rotation_signs(d8, w8["seed"]).cuda()
+        ws8 = torch.empty(fa.fa_fp8_workspace_size(B8, H8, N8, d8), dtype=torch.uint8, device="cuda")
+        o8 = torch.empty(B8, H8, N8, d8, dtype=torch.bfloat16, device="cuda")
+        lse8 = torch.empty(B8, H8, N8, dtype=torch.float32, device="cuda")
+        el8 = B8 * H8 * N8 * d8
+        ms_prep = timed(lambda: fa.fa_fp8_prepare(q8, k8, v8, signs, ws8))
+        if want("FP8 prepare (fp32 in)", cfg8):
+            emit("FP8 prepare (fp32 in)", cfg8, ms_prep,
+                 3 * 4 * el8 + 3 * el8 + 3 * 4 * B8 * H8 * ((N8 + 63) // 64), "GB/s", hbm)
+        for cfg in fwd_cfgs:
+            c = cfg["causal"]
+            ms = timed(lambda: fa.fa_fwd_fp8(ws8, (B8, H8, N8, d8), o=o8, lse=lse8, causal=c, scale=d8 ** -0.5))
+            f = fwd_flops(B8, H8, N8, d8, c)
+            emit("FP8 forward", cfg, ms, f, "TFLOP/s", 2.0 * peak,
+                 tflops_with_prepare=round(f / ((ms + ms_prep) * 1e-3) / 1e12, 1))
+        del q8, k8, v8, ws8, o8, lse8
+
+    for (B, H, Nq, Nk, d) in SWEEP_DECODE:
+        cfg = {"B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d}
+        if not want("split-KV decode + merge", cfg):
+            continue
+        kv = normal_qkv(B, H, Nk, d, 5)
+        k, v = kv["k"].to(torch.bfloat16).cuda(), kv["v"].to(torch.bfloat16).cuda()
+        del kv
+        q = normal_qkv(B, H, Nq, d, 6)["q"].to(torch.bfloat16).cuda()
+        n = fa.fa_splitkv_default_splits(B, H, Nq, Nk, d)
+        ws = torch.empty(fa.fa_splitkv_workspace_size(B, H, Nq, d, n), dtype=torch.uint8, device="cuda")
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, Nq, dtype=torch.float32, device="cuda")
+        ms = timed(lambda: fa.fa_fwd_splitkv(q, k, v, o, lse, ws, n_split=n))
+        byts = 4 * B * H * Nk * d + 4 * B * H * Nq * d + 8 * n * B * H * Nq * (d + 1)
+        emit("split-KV decode + merge", dict(cfg, n_split=n), ms, byts, "GB/s", hbm)
+        del k, v, q, ws, o, lse
+
+    for (M, N, K) in SWEEP_W4A16:
+        cfg = {"M": M, "N": N, "K": K}
+        if not want("W4A16 GEMM", cfg):
+            continue
+        xin = w4a16_inputs(M, N, K, 6)
+        xw, wq, sc, zr = (xin[nn].cuda() for nn in ("x", "wq", "scales", "zeros"))
+        nsp = fa.fa_w4a16_default_splits(M, N, K)
+        wsw = torch.empty(max(fa.fa_w4a16_workspace_size(M, N, K, nsp), 1), dtype=torch.uint8, device="cuda")
+        y = torch.empty(M, N, dtype=torch.float16, device="cuda")
+        ms = timed(lambda: fa.fa_w4a16_gemm(xw, wq, sc, zr, y, wsw, n_split=nsp))
+        byts = N * K // 2 + 3 * N * K // 128 + 2 * M * K + 2 * M * N
+        emit("W4A16 GEMM", dict(cfg, n_split=nsp), ms, byts, "GB/s", hbm,
+             tflops=round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1))
+        del xw, wq, sc, zr, wsw, y
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -749,6 +894,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--step-only", action="store_true",
                     help="time the headline step alone (for profiler captures): no e2e, extra rows or CPU baseline")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every configuration of the sweep tables (one JSON line per row) instead of the step")
+    ap.add_argument("--sweep-filter", default=None,
+                    help="with --sweep: only the rows whose tags contain every token, e.g. 'forward N=8192 d=64'")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture of this kernel version")
     args = ap.parse_args()
@@ -756,6 +905,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_ours(args)
 

@@ -281,8 +281,22 @@ FA_API int fa_fp8_prepare_seeded(const void* q, const void* k, const void* v, in
 FA_API int fa_fp8_rotation_signs(uint64_t seed, int d, int8_t* signs);
 
 /*
+ * fa_fp8_prepare_strided -- fa_fp8_prepare for inputs in other layouts (e.g.
+ * [B, N, H, d] straight from a projection), with the stride rules of
+ * fa_fwd_strided for each of q, k, v (in elements of in_dtype; NULL = dense).
+ * signs: as fa_fp8_prepare, or NULL to draw them from `seed` as
+ * fa_fp8_prepare_seeded does (seed is ignored when signs is given).  The
+ * workspace layout, the codes and the scales are bitwise those of
+ * fa_fp8_prepare on the same values laid out densely.
+ */
+FA_API int fa_fp8_prepare_strided(const void* q, const int64_t* q_strides, const void* k, const int64_t* k_strides,
+                                  const void* v, const int64_t* v_strides, int in_dtype, const int8_t* signs,
+                                  uint64_t seed, void* workspace, size_t ws_bytes, int B, int H, int N, int d,
+                                  fa_stream_t stream);
+
+/*
  * fa_fwd_fp8 -- FP8 forward from a workspace filled by fa_fp8_prepare (same
- * B, H, N, d; d = 128).  Computes O = softmax(scale * Q K^T [+mask]) V and LSE
+ * B, H, N, d; d = 64 or 128).  Computes O = softmax(scale * Q K^T [+mask]) V and LSE
  * like fa_fwd, with both matmuls on e4m3 operands (kind::f8f6f4 tensor cores,
  * fp32 accumulation):
  *   S = (scale / d) * sQ(row tile) * sK(key tile) * (codesQ . codesK^T)
@@ -291,8 +305,8 @@ FA_API int fa_fp8_rotation_signs(uint64_t seed, int d, int8_t* signs);
  *   e4m3 as the A operand of P V; O = acc * max sV / l, rounded to bf16 once.
  *   The row sum l and LSE use the unrounded P.
  *   o   : bf16 [B, H, N, d] (output)      lse : float [B, H, N] (output)
- * Errors as fa_fwd; FA_ERR_UNSUPPORTED for d != 128; FA_ERR_WORKSPACE for a
- * missing or short workspace (256-byte alignment required).
+ * Errors as fa_fwd (FA_ERR_UNSUPPORTED for d not 64 or 128); FA_ERR_WORKSPACE
+ * for a missing or short workspace (256-byte alignment required).
  */
 FA_API int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* lse, int B, int H, int N, int d,
                       int causal, float scale, fa_stream_t stream);
@@ -342,7 +356,7 @@ FA_API int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* ls
  *                lse are used as given.
  * Stages on `stream`: dequantise, [bf16 forward,] the bf16 backward (prep, main,
  * dq), then the inverse rotation of dq and dk in place (fp32 butterflies, bf16
- * rounding).  d = 128.  Errors as fa_bwd, plus FA_ERR_WORKSPACE for a missing or
+ * rounding).  d = 64 or 128.  Errors as fa_bwd, plus FA_ERR_WORKSPACE for a missing or
  * short FP8 workspace and FA_ERR_INVALID_ARG for a NULL signs pointer or a flag
  * not 0/1.
  */
@@ -362,7 +376,8 @@ FA_API int fa_bwd_fp8(const void* fp8_ws, size_t fp8_ws_bytes, const int8_t* sig
  * section 3); one head's keys are then too few work units to fill the GPU, so
  * the key range is cut into splits that run in parallel and are merged.
  *
- * Shapes: q [B, H, Nq, d]; k, v [B, H, Nk, d] (bf16, dense, d contiguous).
+ * Shapes: q [B, H, Nq, d]; k, v [B, H, Nk, d] (bf16, d contiguous; dense, or
+ * strided through fa_fwd_splitkv_strided).
  * Causal (Nq <= Nk required): the queries are the LAST Nq positions, so query i
  * (0-based) sees key j iff j <= i + (Nk - Nq); with Nq == Nk this is fa_fwd's mask.
  * Split rule: keys form nkb = ceil(Nk / 128) blocks of 128; with
@@ -419,6 +434,17 @@ FA_API int fa_merge_partials(const float* o_part, const float* lse_part, void* o
 FA_API int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
                           size_t ws_bytes, int B, int H, int Nq, int Nk, int d, int n_split, int causal, float scale,
                           fa_stream_t stream);
+
+/*
+ * fa_fwd_splitkv_strided -- fa_fwd_splitkv for q, k, v and o in other layouts,
+ * with the stride rules of fa_fwd_strided (strides of q and o count Nq rows, of
+ * k and v Nk rows; NULL = dense).  The partials in the workspace and LSE stay
+ * dense.  Results are bitwise those of fa_fwd_splitkv on dense copies.
+ */
+FA_API int fa_fwd_splitkv_strided(const void* q, const int64_t* q_strides, const void* k, const int64_t* k_strides,
+                                  const void* v, const int64_t* v_strides, void* o, const int64_t* o_strides,
+                                  float* lse, void* workspace, size_t ws_bytes, int B, int H, int Nq, int Nk, int d,
+                                  int n_split, int causal, float scale, fa_stream_t stream);
 
 /*
  * W4A16: 4-bit weights times 16-bit activations, dequantised on the fly

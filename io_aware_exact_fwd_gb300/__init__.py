@@ -88,6 +88,9 @@ def load_library():
     lib.fa_fp8_prepare.argtypes = [vp, vp, vp, i, vp, vp, ctypes.c_size_t, i, i, i, i, vp]
     lib.fa_fp8_prepare_seeded.restype = i
     lib.fa_fp8_prepare_seeded.argtypes = [vp, vp, vp, i, ctypes.c_uint64, vp, ctypes.c_size_t, i, i, i, i, vp]
+    lib.fa_fp8_prepare_strided.restype = i
+    lib.fa_fp8_prepare_strided.argtypes = [vp, vp, vp, vp, vp, vp, i, vp, ctypes.c_uint64, vp, ctypes.c_size_t, i, i,
+                                           i, i, vp]
     lib.fa_fp8_rotation_signs.restype = i
     lib.fa_fp8_rotation_signs.argtypes = [ctypes.c_uint64, i, vp]
     lib.fa_fwd_fp8.restype = i
@@ -113,6 +116,9 @@ def load_library():
     lib.fa_merge_partials.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
     lib.fa_fwd_splitkv.restype = i
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, i, i, f, vp]
+    lib.fa_fwd_splitkv_strided.restype = i
+    lib.fa_fwd_splitkv_strided.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, i,
+                                           i, f, vp]
     lib.fa_w4a16_workspace_size.restype = ctypes.c_size_t
     lib.fa_w4a16_workspace_size.argtypes = [i, i, i, i]
     lib.fa_w4a16_default_splits.restype = i
@@ -227,7 +233,7 @@ def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
 
 def fa_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, workspace=None, causal: bool = False,
            scale: float | None = None, stream=None, deterministic: bool = False):
-    """bf16 attention backward (d = 128): returns (dq, dk, dv).
+    """bf16 attention backward (d = 64 or 128): returns (dq, dk, dv).
 
     q, k, v, o, do: bf16 CUDA tensors [B, H, N, d]; lse: fp32 [B, H, N] from fa_fwd
     with the same causal/scale.  Outputs are allocated if not given; the
@@ -318,11 +324,7 @@ def fa_fp8_workspace_offsets(B: int, H: int, N: int, d: int) -> dict:
     return {kk: int(arr[i]) for i, kk in enumerate(keys)}
 
 
-def fa_fp8_prepare(q, k, v, signs, workspace=None, stream=None):
-    """Rotate Q, K and block-quantise Q, K, V to e4m3 into `workspace` (allocated if None); returns it.
-
-    q, k, v: fp32 or bf16 CUDA tensors [B, H, N, d]; signs: int8 CUDA tensor [d] (+-1).
-    """
+def _fp8_prepare_call(q, k, v, signs, seed, workspace, stream, name):
     import torch
 
     lib = load_library()
@@ -330,38 +332,43 @@ def fa_fp8_prepare(q, k, v, signs, workspace=None, stream=None):
     dt = q.dtype
     if dt not in (torch.float32, torch.bfloat16):
         raise TypeError("q, k, v must be float32 or bfloat16")
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_bhnd(name, t, (B, H, N, d), dt)
-    if signs.dtype != torch.int8 or tuple(signs.shape) != (d,) or not signs.is_cuda:
+    for nm, t in (("q", q), ("k", k), ("v", v)):
+        _check_strided(nm, t, (B, H, N, d), dt)
+    if signs is not None and (signs.dtype != torch.int8 or tuple(signs.shape) != (d,) or not signs.is_cuda):
         raise ValueError("signs must be an int8 CUDA tensor of shape [d]")
     if workspace is None:
         workspace = torch.empty(max(fa_fp8_workspace_size(B, H, N, d), 1), dtype=torch.uint8, device=q.device)
+    in_dtype = 1 if dt == torch.bfloat16 else 0
+    seed64 = ctypes.c_uint64(seed & (2 ** 64 - 1))
     with torch.cuda.device(q.device):
-        st = lib.fa_fp8_prepare(_ptr(q), _ptr(k), _ptr(v), 1 if dt == torch.bfloat16 else 0, _ptr(signs),
-                                _ptr(workspace), _ws_bytes(workspace), B, H, N, d, _stream_handle(stream))
-    _check(st, "fa_fp8_prepare")
+        if not all(t.is_contiguous() for t in (q, k, v)):
+            st = lib.fa_fp8_prepare_strided(_ptr(q), _strides(q), _ptr(k), _strides(k), _ptr(v), _strides(v),
+                                            in_dtype, _ptr(signs) if signs is not None else None, seed64,
+                                            _ptr(workspace), _ws_bytes(workspace), B, H, N, d, _stream_handle(stream))
+        elif signs is not None:
+            st = lib.fa_fp8_prepare(_ptr(q), _ptr(k), _ptr(v), in_dtype, _ptr(signs), _ptr(workspace),
+                                    _ws_bytes(workspace), B, H, N, d, _stream_handle(stream))
+        else:
+            st = lib.fa_fp8_prepare_seeded(_ptr(q), _ptr(k), _ptr(v), in_dtype, seed64, _ptr(workspace),
+                                           _ws_bytes(workspace), B, H, N, d, _stream_handle(stream))
+    _check(st, name)
     return workspace
+
+
+def fa_fp8_prepare(q, k, v, signs, workspace=None, stream=None):
+    """Rotate Q, K and block-quantise Q, K, V to e4m3 into `workspace` (allocated if None); returns it.
+
+    q, k, v: fp32 or bf16 CUDA tensors [B, H, N, d] with contiguous d: dense, or any
+    strided view (fa_fp8_prepare_strided); signs: int8 CUDA tensor [d] (+-1).
+    """
+    if signs is None:
+        raise ValueError("signs must be given (fa_fp8_prepare_seeded draws them from a seed)")
+    return _fp8_prepare_call(q, k, v, signs, 0, workspace, stream, "fa_fp8_prepare")
 
 
 def fa_fp8_prepare_seeded(q, k, v, seed: int, workspace=None, stream=None):
     """fa_fp8_prepare with the rotation signs drawn from a 64-bit seed on the device; returns the workspace."""
-    import torch
-
-    lib = load_library()
-    B, H, N, d = q.shape
-    dt = q.dtype
-    if dt not in (torch.float32, torch.bfloat16):
-        raise TypeError("q, k, v must be float32 or bfloat16")
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_bhnd(name, t, (B, H, N, d), dt)
-    if workspace is None:
-        workspace = torch.empty(max(fa_fp8_workspace_size(B, H, N, d), 1), dtype=torch.uint8, device=q.device)
-    with torch.cuda.device(q.device):
-        st = lib.fa_fp8_prepare_seeded(_ptr(q), _ptr(k), _ptr(v), 1 if dt == torch.bfloat16 else 0,
-                                       ctypes.c_uint64(seed & (2 ** 64 - 1)), _ptr(workspace), _ws_bytes(workspace),
-                                       B, H, N, d, _stream_handle(stream))
-    _check(st, "fa_fp8_prepare_seeded")
-    return workspace
+    return _fp8_prepare_call(q, k, v, None, seed, workspace, stream, "fa_fp8_prepare_seeded")
 
 
 def fa_fp8_rotation_signs(seed: int, d: int):
@@ -419,7 +426,7 @@ def fa_bwd_fp8_workspace_size(B: int, H: int, N: int, d: int) -> int:
 def fa_bwd_fp8(fp8_workspace, signs, o, do, lse, dq=None, dk=None, dv=None, workspace=None, causal: bool = False,
                scale: float | None = None, deterministic: bool = False, recompute_forward: bool = False,
                stream=None):
-    """Straight-through backward of the FP8 attention (d = 128): returns (dq, dk, dv), bf16.
+    """Straight-through backward of the FP8 attention (d = 64 or 128): returns (dq, dk, dv), bf16.
 
     fp8_workspace: filled by fa_fp8_prepare; signs: the int8 [d] signs given to it;
     o, lse: the forward's outputs (bf16 [B, H, N, d], fp32 [B, H, N]), ignored and
@@ -558,26 +565,37 @@ def fa_fwd_splitkv(q, k, v, o=None, lse=None, workspace=None, n_split: int = 0, 
                    scale: float | None = None, stream=None):
     """Split-KV attention (partials + merge): returns (o bf16 [B, H, Nq, d], lse fp32 [B, H, Nq]).
 
-    n_split <= 0 picks the library's default split count for the device.
+    q, k, v, o: bf16 CUDA tensors with contiguous d, dense or any strided view
+    (fa_fwd_splitkv_strided).  n_split <= 0 picks the library's default split count.
     """
     import torch
 
     lib = load_library()
-    B, H, Nq, Nk, d = _check_kv(q, k, v)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    _check_strided("q", q, (B, H, Nq, d), torch.bfloat16)
+    _check_strided("k", k, (B, H, Nk, d), torch.bfloat16)
+    _check_strided("v", v, (B, H, Nk, d), torch.bfloat16)
     n = n_split if n_split > 0 else max(1, fa_splitkv_default_splits(B, H, Nq, Nk, d))
     if o is None:
         o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    _check_bhnd("o", o, (B, H, Nq, d), torch.bfloat16)
+    _check_strided("o", o, (B, H, Nq, d), torch.bfloat16)
     _check_bhnd("lse", lse.view(B, H, Nq, 1), (B, H, Nq, 1), torch.float32)
     if workspace is None:
         workspace = torch.empty(max(fa_splitkv_workspace_size(B, H, Nq, d, n), 1), dtype=torch.uint8,
                                 device=q.device)
     sc = float(scale) if scale is not None else d ** -0.5
     with torch.cuda.device(q.device):
-        st = lib.fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace), _ws_bytes(workspace),
-                                B, H, Nq, Nk, d, n, int(bool(causal)), sc, _stream_handle(stream))
+        if all(t.is_contiguous() for t in (q, k, v, o)):
+            st = lib.fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                                    _ws_bytes(workspace), B, H, Nq, Nk, d, n, int(bool(causal)), sc,
+                                    _stream_handle(stream))
+        else:
+            st = lib.fa_fwd_splitkv_strided(_ptr(q), _strides(q), _ptr(k), _strides(k), _ptr(v), _strides(v), _ptr(o),
+                                            _strides(o), _ptr(lse), _ptr(workspace), _ws_bytes(workspace), B, H, Nq,
+                                            Nk, d, n, int(bool(causal)), sc, _stream_handle(stream))
     _check(st, "fa_fwd_splitkv")
     return o, lse
 

@@ -152,7 +152,8 @@ cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType
 }
 
 cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int cols,
-                         int rows, int heads, int batch, const int64_t strides[3], int box_cols, int box_rows) {
+                         int rows, int heads, int batch, const int64_t strides[3], int box_cols, int box_rows,
+                         CUtensorMapSwizzle swizzle) {
   if (!g_encode) return cudaErrorInitializationError;
   // strides: {row, head, batch} in elements; the column stride is 1.
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
@@ -163,7 +164,7 @@ cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, CUtensorMapDataType
   const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = g_encode(map, dtype, 4, const_cast<void*>(base), dims, gstr, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -315,6 +316,8 @@ int fa_fwd_splitkv_partial(const void* q, const void* k, const void* v, float* o
   a.q = q;
   a.k = k;
   a.v = v;
+  a.sq = fa::dense_strides(H, Nq, d);
+  a.sk = a.sv = fa::dense_strides(H, Nk, d);
   a.o_part = o_part;
   a.lse_part = lse_part;
   a.B = B;
@@ -346,16 +349,20 @@ int fa_merge_partials(const float* o_part, const float* lse_part, void* o, float
   a.o_part = o_part;
   a.lse_part = lse_part;
   a.o = o;
+  a.so = fa::dense_strides(H, Nq, d);
   a.lse = lse;
   a.n_split = n_split;
   a.BH = B * H;
+  a.H = H;
   a.Nq = Nq;
   a.d = d;
   return fa::launch_merge_partials(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace, size_t ws_bytes,
-                   int B, int H, int Nq, int Nk, int d, int n_split, int causal, float scale, fa_stream_t stream) {
+int fa_fwd_splitkv_strided(const void* q, const int64_t* q_strides, const void* k, const int64_t* k_strides,
+                           const void* v, const int64_t* v_strides, void* o, const int64_t* o_strides, float* lse,
+                           void* workspace, size_t ws_bytes, int B, int H, int Nq, int Nk, int d, int n_split,
+                           int causal, float scale, fa_stream_t stream) {
   if (n_split <= 0) {
     const int pre = validate_splitkv(B, H, Nq, Nk, d, 1, causal, scale);
     if (pre < 0) return FA_OK;
@@ -365,15 +372,58 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   const int vs = validate_splitkv(B, H, Nq, Nk, d, n_split, causal, scale);
   if (vs < 0) return FA_OK;
   if (vs != FA_OK) return vs;
-  if (!o || !lse) return FA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa::SplitKvArgs a;
+  fa::MergeArgs m;
+  int st = strides_or_dense(&a.sq, q_strides, H, Nq, d);
+  if (st == FA_OK) st = strides_or_dense(&a.sk, k_strides, H, Nk, d);
+  if (st == FA_OK) st = strides_or_dense(&a.sv, v_strides, H, Nk, d);
+  if (st == FA_OK) st = strides_or_dense(&m.so, o_strides, H, Nq, d);
+  if (st != FA_OK) return st;
   const SplitKvLayout lay = splitkv_layout(B, H, Nq, d, n_split);
   if (!workspace || ws_bytes < lay.total) return FA_ERR_WORKSPACE;
-  if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  if (!aligned(workspace, 256) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  unsigned int* ew = nullptr;
+  st = device_state(&ds, &ew);
+  if (st != FA_OK) return st;
   float* o_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lay.off_o);
   float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lay.off_lse);
-  int st = fa_fwd_splitkv_partial(q, k, v, o_part, lse_part, B, H, Nq, Nk, d, n_split, causal, scale, stream);
-  if (st != FA_OK) return st;
-  return fa_merge_partials(o_part, lse_part, o, lse, n_split, B, H, Nq, d, stream);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.n_split = n_split;
+  a.causal = causal;
+  a.scale = scale;
+  a.err_word = ew;
+  a.dbg = knobs();
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fa::launch_fwd_splitkv_partial(a, s) != cudaSuccess) return FA_ERR_CUDA;
+  m.o_part = o_part;
+  m.lse_part = lse_part;
+  m.o = o;
+  m.lse = lse;
+  m.n_split = n_split;
+  m.BH = B * H;
+  m.H = H;
+  m.Nq = Nq;
+  m.d = d;
+  return fa::launch_merge_partials(m, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace, size_t ws_bytes,
+                   int B, int H, int Nq, int Nk, int d, int n_split, int causal, float scale, fa_stream_t stream) {
+  return fa_fwd_splitkv_strided(q, nullptr, k, nullptr, v, nullptr, o, nullptr, lse, workspace, ws_bytes, B, H, Nq,
+                                Nk, d, n_split, causal, scale, stream);
 }
 
 size_t fa_w4a16_workspace_size(int M, int N, int K, int n_split) {
@@ -623,20 +673,25 @@ int fa_fp8_workspace_offsets(int B, int H, int N, int d, size_t* offsets) {
 
 namespace {
 
-int fp8_prepare_impl(const void* q, const void* k, const void* v, int in_dtype, const int8_t* signs, uint64_t seed,
-                     void* workspace, size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream) {
+int fp8_prepare_impl(const void* q, const int64_t* q_strides, const void* k, const int64_t* k_strides, const void* v,
+                     const int64_t* v_strides, int in_dtype, const int8_t* signs, uint64_t seed, void* workspace,
+                     size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream) {
   const int vs = validate_shape(B, H, N, d, 0, 1.f);
   if (vs < 0) return FA_OK;
   if (vs != FA_OK) return vs;
   if (in_dtype != 0 && in_dtype != 1) return FA_ERR_INVALID_ARG;
   if (!q || !k || !v) return FA_ERR_INVALID_ARG;
+  fa::Fp8PrepArgs a;
+  int sst = strides_or_dense(&a.sq, q_strides, H, N, d);
+  if (sst == FA_OK) sst = strides_or_dense(&a.sk, k_strides, H, N, d);
+  if (sst == FA_OK) sst = strides_or_dense(&a.sv, v_strides, H, N, d);
+  if (sst != FA_OK) return sst;
   if (!workspace) return FA_ERR_WORKSPACE;
   if (ws_bytes < fa::fp8_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(workspace, 256)) return FA_ERR_MISALIGNED;
   DeviceState* ds = nullptr;
   const int st = device_state(&ds);
   if (st != FA_OK) return st;
-  fa::Fp8PrepArgs a;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -658,12 +713,21 @@ extern "C" {
 int fa_fp8_prepare(const void* q, const void* k, const void* v, int in_dtype, const int8_t* signs, void* workspace,
                    size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream) {
   if (!signs && B > 0 && H > 0 && N > 0) return FA_ERR_INVALID_ARG;
-  return fp8_prepare_impl(q, k, v, in_dtype, signs, 0, workspace, ws_bytes, B, H, N, d, stream);
+  return fp8_prepare_impl(q, nullptr, k, nullptr, v, nullptr, in_dtype, signs, 0, workspace, ws_bytes, B, H, N, d,
+                          stream);
 }
 
 int fa_fp8_prepare_seeded(const void* q, const void* k, const void* v, int in_dtype, uint64_t seed, void* workspace,
                           size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream) {
-  return fp8_prepare_impl(q, k, v, in_dtype, nullptr, seed, workspace, ws_bytes, B, H, N, d, stream);
+  return fp8_prepare_impl(q, nullptr, k, nullptr, v, nullptr, in_dtype, nullptr, seed, workspace, ws_bytes, B, H, N,
+                          d, stream);
+}
+
+int fa_fp8_prepare_strided(const void* q, const int64_t* q_strides, const void* k, const int64_t* k_strides,
+                           const void* v, const int64_t* v_strides, int in_dtype, const int8_t* signs, uint64_t seed,
+                           void* workspace, size_t ws_bytes, int B, int H, int N, int d, fa_stream_t stream) {
+  return fp8_prepare_impl(q, q_strides, k, k_strides, v, v_strides, in_dtype, signs, seed, workspace, ws_bytes, B, H,
+                          N, d, stream);
 }
 
 int fa_fp8_rotation_signs(uint64_t seed, int d, int8_t* signs) {
@@ -677,7 +741,6 @@ int fa_fwd_fp8(const void* workspace, size_t ws_bytes, void* o, float* lse, int 
   const int vs = validate_shape(B, H, N, d, causal, scale);
   if (vs < 0) return FA_OK;
   if (vs != FA_OK) return vs;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
   if (!o || !lse) return FA_ERR_INVALID_ARG;
   if (!workspace) return FA_ERR_WORKSPACE;
   if (ws_bytes < fa::fp8_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
@@ -747,7 +810,7 @@ int fa_fp8_dequantize(const void* fp8_ws, size_t fp8_ws_bytes, void* qr, void* k
 }
 
 size_t fa_bwd_fp8_workspace_size(int B, int H, int N, int d) {
-  if (validate_shape(B, H, N, d, 0, 1.f) != FA_OK || d != 128) return 0;
+  if (validate_shape(B, H, N, d, 0, 1.f) != FA_OK) return 0;
   return fp8_bwd_layout(B, H, N, d).total;
 }
 
@@ -759,7 +822,6 @@ int fa_bwd_fp8(const void* fp8_ws, size_t fp8_ws_bytes, const int8_t* signs, con
   const int vs = validate_shape(B, H, N, d, causal, scale);
   if (vs < 0) return FA_OK;
   if (vs != FA_OK) return vs;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
   if (!fp8_ws || fp8_ws_bytes < fa::fp8_layout(B, H, N, d).total) return FA_ERR_WORKSPACE;
   if (!signs) return FA_ERR_INVALID_ARG;
   const Fp8BwdLayout l = fp8_bwd_layout(B, H, N, d);
@@ -788,7 +850,7 @@ int fa_bwd_fp8(const void* fp8_ws, size_t fp8_ws_bytes, const int8_t* signs, con
     if (st != FA_OK) return st;
   }
   cudaError_t e = fa::launch_bwd_bf16(a, s);
-  if (e == cudaSuccess) e = fa::launch_fp8_unrotate(dq, dk, signs, static_cast<long long>(B) * H * N, s);
+  if (e == cudaSuccess) e = fa::launch_fp8_unrotate(dq, dk, signs, static_cast<long long>(B) * H * N, d, s);
   return status_of(e);
 }
 

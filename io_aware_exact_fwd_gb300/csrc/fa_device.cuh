@@ -195,6 +195,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// Shared-memory matrix descriptor with the 64-byte swizzle (layout type 4), for
+// K-major tiles of 64-byte rows (64 e4m3 codes): 8-row groups of 512 bytes (SBO),
+// the 16-byte chunks of each row XOR-permuted by bits 1-2 of the row index, as
+// TMA's 64-byte swizzle writes them.  A K-step of 32 bytes advances the start
+// address inside the row.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset: unused for swizzled K-major
+  d |= static_cast<uint64_t>(512 >> 4) << 32;             // stride byte offset: 8 rows x 64 bytes
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(4) << 61;
+  return d;
+}
+
 // Shared-memory matrix descriptor with the 32-byte swizzle (layout type 6), for
 // K-major tiles whose rows are a single 32-byte K-step (16 bf16): 8-row groups of
 // 256 bytes (SBO); within each group the two 16-byte halves of rows 4-7 swap

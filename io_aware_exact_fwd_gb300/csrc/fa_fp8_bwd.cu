@@ -130,28 +130,30 @@ __global__ void __launch_bounds__(kDeqThreads) fp8_dequant_kernel(const uint8_t*
   }
 }
 
-// x <- bf16((x H_128) * s) per row of 128, for two tensors (blockIdx.y selects).
-// Lane l holds 8 consecutive columns 8 (l % 16) .. +7 of a row (one 16-byte load),
-// so a warp holds two rows per pass; butterfly spans 1, 2, 4 stay in the lane and
-// spans 8 .. 64 pair lane l with lane l ^ (span / 8) of the same half-warp.  Each
-// warp takes kRotPasses passes (2 kRotPasses rows) and issues all their loads
+// x <- bf16((x H_d) * s) per row of d (64 or 128), for two tensors (blockIdx.y
+// selects).  Lane l holds 8 consecutive columns of a row (one 16-byte load): a row
+// spans d / 8 lanes, so a warp holds 32 / (d / 8) rows per pass; butterfly spans
+// 1, 2, 4 stay in the lane and spans 8 .. d / 2 pair lane l with lane l ^ (span / 8)
+// of the same row.  Each warp takes kRotPasses passes and issues all their loads
 // before any arithmetic, to keep enough bytes in flight.
 constexpr int kRotPasses = 4;
-constexpr int kRotRowsPerWarp = 2 * kRotPasses;
 
+template <int D>
 __global__ void __launch_bounds__(kRotThreads) unrotate_kernel(__nv_bfloat16* __restrict__ x0,
                                                                __nv_bfloat16* __restrict__ x1,
                                                                const int8_t* __restrict__ signs, long long rows) {
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerPass = 32 / kLanesPerRow;
   const int lane = threadIdx.x & 31;
-  const int sl = lane & 15;  // the lane's index within its row
+  const int sl = lane & (kLanesPerRow - 1);  // the lane's index within its row
   const long long r0 = (static_cast<long long>(blockIdx.x) * (kRotThreads / 32) + (threadIdx.x >> 5)) *
-                           kRotRowsPerWarp + (lane >> 4);
+                           (kRowsPerPass * kRotPasses) + lane / kLanesPerRow;
   __nv_bfloat16* base = (blockIdx.y == 0 ? x0 : x1) + 8 * sl;
   uint4 raw[kRotPasses];
 #pragma unroll
   for (int p = 0; p < kRotPasses; ++p) {
-    const long long r = r0 + 2 * p;
-    raw[p] = r < rows ? *reinterpret_cast<const uint4*>(base + r * 128) : make_uint4(0u, 0u, 0u, 0u);
+    const long long r = r0 + kRowsPerPass * p;
+    raw[p] = r < rows ? *reinterpret_cast<const uint4*>(base + r * D) : make_uint4(0u, 0u, 0u, 0u);
   }
   float s[8];
 #pragma unroll
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(kRotThreads) unrotate_kernel(__nv_bfloat16* __
       }
     }
 #pragma unroll
-    for (int m = 1; m < 16; m <<= 1) {
+    for (int m = 1; m < kLanesPerRow; m <<= 1) {
       const bool upper = (sl & m) != 0;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -186,14 +188,14 @@ __global__ void __launch_bounds__(kRotThreads) unrotate_kernel(__nv_bfloat16* __
         v[e] = upper ? o - v[e] : v[e] + o;  // (a, b) -> (a + b, a - b), a the lower index
       }
     }
-    const long long r = r0 + 2 * p;
+    const long long r = r0 + kRowsPerPass * p;
     if (r < rows) {
       uint4 out;
       out.x = pack_bf16x2(v[0] * s[0], v[1] * s[1]);
       out.y = pack_bf16x2(v[2] * s[2], v[3] * s[3]);
       out.z = pack_bf16x2(v[4] * s[4], v[5] * s[5]);
       out.w = pack_bf16x2(v[6] * s[6], v[7] * s[7]);
-      *reinterpret_cast<uint4*>(base + r * 128) = out;
+      *reinterpret_cast<uint4*>(base + r * D) = out;
     }
   }
 }
@@ -215,11 +217,16 @@ cudaError_t launch_fp8_dequant(const void* fp8_ws, void* qr, void* kr, void* vr,
   return cudaGetLastError();
 }
 
-cudaError_t launch_fp8_unrotate(void* dq, void* dk, const int8_t* signs, long long rows, cudaStream_t stream) {
-  const int per_block = (kRotThreads / 32) * kRotRowsPerWarp;
+cudaError_t launch_fp8_unrotate(void* dq, void* dk, const int8_t* signs, long long rows, int d,
+                                cudaStream_t stream) {
+  auto* x0 = static_cast<__nv_bfloat16*>(dq);
+  auto* x1 = static_cast<__nv_bfloat16*>(dk);
+  const int per_block = (kRotThreads / 32) * (256 / d) * kRotPasses;  // rows per pass of a warp: 32 / (d / 8)
   const dim3 grid(static_cast<unsigned>((rows + per_block - 1) / per_block), 2);
-  unrotate_kernel<<<grid, kRotThreads, 0, stream>>>(static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
-                                                    signs, rows);
+  if (d == 64)
+    unrotate_kernel<64><<<grid, kRotThreads, 0, stream>>>(x0, x1, signs, rows);
+  else
+    unrotate_kernel<128><<<grid, kRotThreads, 0, stream>>>(x0, x1, signs, rows);
   return cudaGetLastError();
 }
 

@@ -20,6 +20,8 @@
 //    e4m3_rn_satfinite(x * inv), an exact scaling.  e4m3 being floating point, a
 //    power-of-two scale loses no relative precision, and decode(code) * sigma is
 //    exact in fp32 and bf16 (the FP8 backward's operands).
+//  * Inputs may be strided (element (b, h, n, c) at b s[2] + h s[1] + n s[0] + c,
+//    c contiguous); the workspace is always dense.
 //  * Q and K codes are written row-major [BH, N, d]; V codes transposed,
 //    [BH, d, npad] with keys contiguous (npad = N rounded up to 128, a whole
 //    attention key block), so that V is a K-major operand of the P V MMA.
@@ -129,7 +131,8 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
                                                                    const void* __restrict__ k,
                                                                    const void* __restrict__ v, int in_bf16,
                                                                    const int8_t* __restrict__ signs, uint64_t seed,
-                                                                   Fp8Layout lay, uint8_t* __restrict__ ws, int N) {
+                                                                   Fp8Layout lay, uint8_t* __restrict__ ws, int N,
+                                                                   int H, Strides sq, Strides sk, Strides sv) {
   constexpr int E = D / 32;
   constexpr int kRowsPerWarp = kTileRows / 8;
   constexpr int kVtPitch = kTileRows + 4;  // 17 words per d-row: byte stores of 32 lanes hit 32 banks
@@ -142,6 +145,9 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
   __shared__ float s_amax[8];
   __shared__ __align__(16) uint8_t s_vt[D * kVtPitch];  // V codes of this tile, transposed [d][64 (+4)]
 
+  // Element (b, h, row, c) of an input at b s[2] + h s[1] + row s[0] + c.
+  const Strides& sin = which == 0 ? sq : (which == 1 ? sk : sv);
+  const size_t head_off = static_cast<size_t>(bh / H) * sin.s[2] + static_cast<size_t>(bh % H) * sin.s[1];
   float x[kRowsPerWarp][E];
   if (which == 2) {
     // ------------------------------------------------ V: no rotation, transposed out
@@ -154,7 +160,7 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
       for (int m = 0; m < E; ++m) {
         float val = 0.f;
         if (row < N) {
-          const size_t e = (static_cast<size_t>(bh) * N + row) * D + lane + 32 * m;
+          const size_t e = head_off + static_cast<size_t>(row) * sin.s[0] + lane + 32 * m;
           val = in_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(v)[e]) : static_cast<const float*>(v)[e];
         }
         x[r][m] = val;
@@ -209,7 +215,7 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
   for (int p = 0; p < kPasses; ++p) {
     const int row = tile * kTileRows + warp * kRowsPerWarp + p * kRowsPerPass + rg;
     if (row < N) {
-      load16(src, (static_cast<size_t>(bh) * N + row) * D + kE * sl, in_bf16, xr[p]);
+      load16(src, head_off + static_cast<size_t>(row) * sin.s[0] + kE * sl, in_bf16, xr[p]);
     } else {
 #pragma unroll
       for (int i = 0; i < kE; ++i) xr[p][i] = 0.f;
@@ -270,10 +276,10 @@ cudaError_t launch_fp8_prepare(const Fp8PrepArgs& a, cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   if (a.d == 64)
     fp8_prepare_kernel<64><<<grid, kPrepThreads, 0, stream>>>(a.q, a.k, a.v, a.in_bf16, a.signs, a.seed, lay, ws,
-                                                              a.N);
+                                                              a.N, a.H, a.sq, a.sk, a.sv);
   else
     fp8_prepare_kernel<128><<<grid, kPrepThreads, 0, stream>>>(a.q, a.k, a.v, a.in_bf16, a.signs, a.seed, lay, ws,
-                                                               a.N);
+                                                               a.N, a.H, a.sq, a.sk, a.sv);
   return cudaGetLastError();
 }
 

@@ -85,8 +85,10 @@ enum : uint32_t {
 template <int D, bool FP8>
 struct FwdCfg {
   static constexpr int kRowBytes = D * (FP8 ? 1 : 2);       // one row of a Q, K or V tile
-  static constexpr int kBoxes = kRowBytes / 128;            // 128-byte-wide TMA boxes per row
+  static constexpr int kBoxes = (kRowBytes + 127) / 128;    // TMA boxes per row, 128 bytes wide (64 for FP8 d = 64)
   static constexpr int kBoxBytes = kBlockK * 128;           // 16 KB: 128 rows x 128 bytes
+  // FP8 at d = 64: Q and K rows are 64 bytes, staged with the 64-byte swizzle.
+  static constexpr bool kSw64 = kRowBytes == 64;
   static constexpr int kTileBytes = kBlockK * kRowBytes;    // one Q, K or V tile
   static constexpr int kKSteps = kRowBytes / 32;            // MMA K-steps of 32 bytes over d
   static constexpr int kOBytes = kBlockQ * D * 2;           // bf16 O staging of one query tile
@@ -264,8 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // Base descriptors; every MMA operand below is one of these advanced by a
       // compile-time byte offset (a single 32-bit add on the issuing thread).
-      const uint64_t qdesc = sdesc_sw128(q_addr, 16, 1024);          // K-major, SBO = 8 rows x 128 B
-      const uint64_t kdesc = sdesc_sw128(ring_addr, 16, 1024);       // K-major view of a ring slot
+      // K-major, SBO = 8 rows x the row (128 B, or 64 B for FP8 at d = 64).
+      const uint64_t qdesc = C::kSw64 ? sdesc_sw64(q_addr) : sdesc_sw128(q_addr, 16, 1024);
+      const uint64_t kdesc = C::kSw64 ? sdesc_sw64(ring_addr) : sdesc_sw128(ring_addr, 16, 1024);  // a ring slot
       // bf16: V is MN-major (LBO = one box); FP8: V^T is K-major like K.
       const uint64_t vdesc = sdesc_sw128(ring_addr, FP8 ? 16 : C::kBoxBytes, 1024);
 
@@ -792,19 +795,17 @@ cudaError_t launch_splitkv_impl(const SplitKvArgs& a, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
   cudaError_t e;
   constexpr auto kBf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const Strides sq = dense_strides(a.H, a.Nq, D), skv = dense_strides(a.H, a.Nk, D);
-  if ((e = make_tmap_4d(&tq, a.q, kBf16, 2, D, a.Nq, a.H, a.B, sq.s, kBoxCols, kBlockQ))) return e;
-  if ((e = make_tmap_4d(&tk, a.k, kBf16, 2, D, a.Nk, a.H, a.B, skv.s, kBoxCols, kBlockK))) return e;
-  if ((e = make_tmap_4d(&tv, a.v, kBf16, 2, D, a.Nk, a.H, a.B, skv.s, kBoxCols, kBlockK))) return e;
+  if ((e = make_tmap_4d(&tq, a.q, kBf16, 2, D, a.Nq, a.H, a.B, a.sq.s, kBoxCols, kBlockQ))) return e;
+  if ((e = make_tmap_4d(&tk, a.k, kBf16, 2, D, a.Nk, a.H, a.B, a.sk.s, kBoxCols, kBlockK))) return e;
+  if ((e = make_tmap_4d(&tv, a.v, kBf16, 2, D, a.Nk, a.H, a.B, a.sv.s, kBoxCols, kBlockK))) return e;
   const KeySplit ks{a.Nk, a.n_split, splitkv_kbps(a.Nk, a.n_split), a.Nk - a.Nq, a.o_part, a.lse_part};
   // The partial epilogue stores fp32 rows itself; the O tensor map is never used.
   return launch_kernel<D, CAUSAL, false, true>(tq, tk, tv, tq, nullptr, a.Nq, a.H, BH, a.scale * 1.4426950408889634f,
                                                a.err_word, a.dbg, Fp8Scales{nullptr, nullptr, nullptr, 0}, ks, stream);
 }
 
-template <bool CAUSAL>
+template <int D, bool CAUSAL>
 cudaError_t launch_fwd_fp8_impl(const FwdArgs& a, const void* workspace, cudaStream_t stream) {
-  constexpr int D = 128;
   const int BH = a.B * a.H;
   const Fp8Layout lay = fp8_layout(a.B, a.H, a.N, D);
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
@@ -812,8 +813,10 @@ cudaError_t launch_fwd_fp8_impl(const FwdArgs& a, const void* workspace, cudaStr
   cudaError_t e;
   constexpr auto kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const Strides s8 = dense_strides(a.H, a.N, D), svt = dense_strides(a.H, D, lay.npad);
-  if ((e = make_tmap_4d(&tq, ws + lay.off_q8, kU8, 1, D, a.N, a.H, a.B, s8.s, 128, kBlockQ))) return e;
-  if ((e = make_tmap_4d(&tk, ws + lay.off_k8, kU8, 1, D, a.N, a.H, a.B, s8.s, 128, kBlockK))) return e;
+  // Q and K code rows: one box of the whole row (128 bytes at d = 128, 64 at d = 64).
+  constexpr auto kSwQK = D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  if ((e = make_tmap_4d(&tq, ws + lay.off_q8, kU8, 1, D, a.N, a.H, a.B, s8.s, D, kBlockQ, kSwQK))) return e;
+  if ((e = make_tmap_4d(&tk, ws + lay.off_k8, kU8, 1, D, a.N, a.H, a.B, s8.s, D, kBlockK, kSwQK))) return e;
   if ((e = make_tmap_4d(&tv, ws + lay.off_v8t, kU8, 1, lay.npad, D, a.H, a.B, svt.s, kBlockK, D))) return e;
   if ((e = make_tmap_4d(&to, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.H, a.B, a.so.s, kBoxCols, kBlockQ)))
     return e;
@@ -833,7 +836,11 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_fwd_fp8(const FwdArgs& a, const void* workspace, cudaStream_t stream) {
-  return a.causal ? launch_fwd_fp8_impl<true>(a, workspace, stream) : launch_fwd_fp8_impl<false>(a, workspace, stream);
+  if (a.d == 64)
+    return a.causal ? launch_fwd_fp8_impl<64, true>(a, workspace, stream)
+                    : launch_fwd_fp8_impl<64, false>(a, workspace, stream);
+  return a.causal ? launch_fwd_fp8_impl<128, true>(a, workspace, stream)
+                  : launch_fwd_fp8_impl<128, false>(a, workspace, stream);
 }
 
 int splitkv_kbps(int Nk, int n_split) {

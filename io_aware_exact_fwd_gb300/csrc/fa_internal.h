@@ -57,6 +57,7 @@ struct SplitKvArgs {
   const void* q;
   const void* k;
   const void* v;
+  Strides sq, sk, sv;  // element strides (row, head, batch) of q, k, v
   float* o_part;
   float* lse_part;
   int B, H, Nq, Nk, d, n_split;
@@ -74,8 +75,9 @@ struct MergeArgs {
   const float* o_part;
   const float* lse_part;
   void* o;
+  Strides so;  // element strides (row, head, batch) of o
   float* lse;
-  int n_split, BH, Nq, d;
+  int n_split, BH, H, Nq, d;
 };
 cudaError_t launch_merge_partials(const MergeArgs& a, cudaStream_t stream);
 
@@ -137,21 +139,23 @@ struct Fp8Layout {
 Fp8Layout fp8_layout(int B, int H, int N, int d);
 
 // FP8 forward launcher (fa_fwd.cu): reads the prepared workspace (q, k, v of
-// FwdArgs unused), writes bf16 O and fp32 LSE; d = 128.
+// FwdArgs unused), writes bf16 O and fp32 LSE; d = 64 or 128.
 cudaError_t launch_fwd_fp8(const FwdArgs& a, const void* workspace, cudaStream_t stream);
 
 // FP8 backward helpers (fa_fp8_bwd.cu).  launch_fp8_dequant: bf16 operands
 // bf16_rn(decode(code) * tile scale) of the rotated Q, K and of V, dense [BH, N, d],
-// from a prepared FP8 workspace.  launch_fp8_unrotate: rows of 128 of dq and dk
-// (dense, `rows` each) replaced in place by bf16((x H_128) * s).
+// from a prepared FP8 workspace.  launch_fp8_unrotate: rows of d (64 or 128) of dq
+// and dk (dense, `rows` each) replaced in place by bf16((x H_d) * s).
 cudaError_t launch_fp8_dequant(const void* fp8_ws, void* qr, void* kr, void* vr, int B, int H, int N, int d,
                                cudaStream_t stream);
-cudaError_t launch_fp8_unrotate(void* dq, void* dk, const int8_t* signs, long long rows, cudaStream_t stream);
+cudaError_t launch_fp8_unrotate(void* dq, void* dk, const int8_t* signs, long long rows, int d,
+                                cudaStream_t stream);
 
 struct Fp8PrepArgs {
   const void* q;
   const void* k;
   const void* v;
+  Strides sq, sk, sv;      // element strides (row, head, batch) of q, k, v
   int in_bf16;             // 0: fp32 inputs, 1: bf16 inputs
   const int8_t* signs;     // [d], the sign of each entry is used; NULL: signs from `seed`
   uint64_t seed;           // used when signs is NULL (see seeded_sign)
@@ -204,7 +208,8 @@ bool w4a16_uses_gemv(int M, int K);
 cudaError_t launch_w4a16(const W4a16Args& a, cudaStream_t stream);
 
 cudaError_t make_tmap_4d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int cols,
-                         int rows, int heads, int batch, const int64_t strides[3], int box_cols, int box_rows);
+                         int rows, int heads, int batch, const int64_t strides[3], int box_cols, int box_rows,
+                         CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes,
                          int cols, int rows, int depth, int box_cols, int box_rows);
 

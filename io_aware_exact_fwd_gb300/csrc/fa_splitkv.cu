@@ -16,6 +16,7 @@
 // Bound: HBM.  One warp per query row: the lanes first reduce the row's LSE_s
 // (max, then the sum of exp(LSE_s - max)), then walk the splits once, each lane
 // accumulating d/32 consecutive elements of O (coalesced 128- or 256-byte rows).
+// O may be strided (element (b, h, i, c) at b so[2] + h so[1] + i so[0] + c).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -30,8 +31,9 @@ constexpr int kMergeThreads = 256;  // 8 rows per block
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __restrict__ o_part,
                                                               const float* __restrict__ lse_part,
-                                                              __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-                                                              int n_split, long long rows) {
+                                                              __nv_bfloat16* __restrict__ o, Strides so,
+                                                              float* __restrict__ lse, int n_split, long long rows,
+                                                              int H, int Nq) {
   constexpr int kPer = D / 32;  // elements of O per lane
   const long long r = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -71,7 +73,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
     for (int i = 0; i < kPer; ++i) acc[i] *= inv;
     if (lane == 0) lse[r] = m + logf(tot);
   }
-  __nv_bfloat16* dst = o + r * D + lane * kPer;
+  // Row r = (b H + h) Nq + i of the partials; O element (b, h, i, c) at the strides.
+  const long long bh = r / Nq, i = r % Nq;
+  __nv_bfloat16* dst = o + (bh / H) * so.s[2] + (bh % H) * so.s[1] + i * so.s[0] + lane * kPer;
   if constexpr (kPer == 4) {
     uint2 pk;
     pk.x = pack_bf16x2(acc[0], acc[1]);
@@ -90,9 +94,11 @@ cudaError_t launch_merge_partials(const MergeArgs& a, cudaStream_t stream) {
   const unsigned blocks = static_cast<unsigned>((rows + per_block - 1) / per_block);
   auto* o = static_cast<__nv_bfloat16*>(a.o);
   if (a.d == 64)
-    merge_kernel<64><<<blocks, kMergeThreads, 0, stream>>>(a.o_part, a.lse_part, o, a.lse, a.n_split, rows);
+    merge_kernel<64><<<blocks, kMergeThreads, 0, stream>>>(a.o_part, a.lse_part, o, a.so, a.lse, a.n_split, rows,
+                                                          a.H, a.Nq);
   else
-    merge_kernel<128><<<blocks, kMergeThreads, 0, stream>>>(a.o_part, a.lse_part, o, a.lse, a.n_split, rows);
+    merge_kernel<128><<<blocks, kMergeThreads, 0, stream>>>(a.o_part, a.lse_part, o, a.so, a.lse, a.n_split, rows,
+                                                           a.H, a.Nq);
   return cudaGetLastError();
 }
 

@@ -164,14 +164,16 @@ def test_fp8_backward_validation_statuses(lib):
     f8 = lib.fa_fp8_workspace_size(B, H, N, d)
     need = lib.fa_bwd_fp8_workspace_size(B, H, N, d)
     assert need >= lib.fa_bwd_workspace_size(B, H, N, d) + 4 * B * H * N * d * 2 + B * H * N * 4
-    assert lib.fa_bwd_fp8_workspace_size(B, H, N, 64) == 0
+    # d = 64 is supported; other head dims are not.
+    assert lib.fa_bwd_fp8_workspace_size(B, H, N, 64) >= lib.fa_bwd_workspace_size(B, H, N, 64)
+    assert lib.fa_bwd_fp8_workspace_size(B, H, N, 96) == 0
 
     def g(det=0, rec=0, dd=d, ws8=FAKE, f8b=f8, signs=FAKE, ws=FAKE, wsb=need, n=N):
         return lib.fa_bwd_fp8(vp(ws8), f8b, vp(signs), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
                               vp(ws), wsb, B, H, n, dd, 0, 0.1, det, rec, vp(0))
     assert g(det=2) == 1
     assert g(rec=-1) == 1
-    assert g(dd=64) == 2
+    assert g(dd=96) == 2
     assert g(ws8=0) == 6
     assert g(f8b=f8 - 1) == 6
     assert g(signs=0) == 1

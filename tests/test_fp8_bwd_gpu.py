@@ -73,10 +73,11 @@ def test_dequantize_bit_exact(N, d):
         np.testing.assert_array_equal(g.float().cpu().numpy().astype(np.float64), w)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 63, 65, 128, 200, 1000])
-def test_backward_given_oracle_forward(N, causal):
-    B, H, d = 1, 2, 128
+def test_backward_given_oracle_forward(N, causal, d):
+    B, H = 1, 2
     scale = d ** -0.5
     x, do, s, ws = _setup(B, H, N, d, 800 + N)
     prep = fp8_prepare(x["q"], x["k"], x["v"], s.numpy())
@@ -89,10 +90,11 @@ def test_backward_given_oracle_forward(N, causal):
     assert max(errs) <= BWD_REL, errs
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 65, 200, 1000])
-def test_end_to_end_recompute(N, causal):
-    B, H, d = 1, 2, 128
+def test_end_to_end_recompute(N, causal, d):
+    B, H = 1, 2
     scale = d ** -0.5
     x, do, s, ws = _setup(B, H, N, d, 900 + N)
     dq, dk, dv = fa.fa_bwd_fp8(ws, s.cuda(), None, do.cuda(), None, causal=causal, scale=scale,
@@ -112,10 +114,11 @@ def test_end_to_end_recompute(N, causal):
         assert max(errs_x) <= 0.5, errs_x
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [200, 1000])
-def test_end_to_end_with_fp8_forward_output(N, causal):
-    B, H, d = 1, 2, 128
+def test_end_to_end_with_fp8_forward_output(N, causal, d):
+    B, H = 1, 2
     scale = d ** -0.5
     x, do, s, ws = _setup(B, H, N, d, 900 + N)
     o, lse = fa.fa_fwd_fp8(ws, (B, H, N, d), causal=causal, scale=scale)

@@ -98,10 +98,11 @@ def _dequantised(ref):
     return qd, kd, vd
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 65, 128, 200, 1000])
-def test_fp8_forward_small(N, causal):
-    B, H, d = 1, 2, 128
+def test_fp8_forward_small(N, causal, d):
+    B, H = 1, 2
     x = outlier_qkv(B, H, N, d, seed=600 + N)
     s = rotation_signs(d, seed=600 + N)
     ws = fa.fa_fp8_prepare(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), s.cuda())
@@ -114,7 +115,7 @@ def test_fp8_forward_small(N, causal):
     assert _rel_rmse(o, o_deq) <= FP8_RMSE_REL
     assert float(np.abs(lse.cpu().numpy() - lse_deq).max()) <= 1e-2
     o_exact, _ = attention_forward(x["q"], x["k"], x["v"], scale, causal)
-    report(f"fp8 fwd B=1 H=2 N={N} d=128 causal={int(causal)}", rmse_vs_dequantised=_rel_rmse(o, o_deq),
+    report(f"fp8 fwd B=1 H=2 N={N} d={d} causal={int(causal)}", rmse_vs_dequantised=_rel_rmse(o, o_deq),
            rmse_vs_unquantised=_rel_rmse(o, o_exact))
     assert _rel_rmse(o, o_exact) <= 1e-1
 
@@ -150,6 +151,39 @@ def test_fp8_forward_config_whole_heads(causal):
     rmse_exact = np.sqrt(sum(e[2] for e in r) / sum(e[3] for e in r))
     lse_err = max(e[4] for e in r)
     report(f"fp8 fwd B=2 H=16 N=8192 d=128 causal={int(causal)}", heads=len(heads), rmse_vs_dequantised=rmse_deq,
+           rmse_vs_unquantised=rmse_exact, lse_vs_dequantised=lse_err)
+    assert rmse_deq <= FP8_RMSE_REL, rmse_deq
+    assert lse_err <= 1e-2, lse_err
+    assert rmse_exact <= 1e-1, rmse_exact
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_d64_all_heads(causal):
+    # d = 64 (Q and K code rows of 64 bytes, staged with the 64-byte swizzle):
+    # B=2, H=4, N=4096, every row of every head against the dequantised reference.
+    B, H, N, d = 2, 4, 4096, 64
+    x = outlier_qkv(B, H, N, d, seed=7)
+    s = rotation_signs(d, seed=7)
+    ws = fa.fa_fp8_prepare(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), s.cuda())
+    o, lse = fa.fa_fwd_fp8(ws, (B, H, N, d), causal=causal)
+    fa.fa_sync_check()
+    scale = d ** -0.5
+    oh, lh = host_f64(o), host_f64(lse)
+
+    def one(b, h):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = fp8_prepare(x["q"][sl], x["k"][sl], x["v"][sl], s.numpy())
+        qd, kd, vd = _dequantised(ref)
+        od, ld = attention_forward(qd, kd, vd, scale / d, causal)
+        oe, _ = attention_forward(x["q"][sl], x["k"][sl], x["v"][sl], scale, causal)
+        return (float(((oh[sl] - od) ** 2).sum()), float((od ** 2).sum()), float(((oh[sl] - oe) ** 2).sum()),
+                float((oe ** 2).sum()), float(np.abs(lh[sl] - ld).max()))
+
+    r = map_heads(one, [(b, h) for b in range(B) for h in range(H)])
+    rmse_deq = np.sqrt(sum(e[0] for e in r) / sum(e[1] for e in r))
+    rmse_exact = np.sqrt(sum(e[2] for e in r) / sum(e[3] for e in r))
+    lse_err = max(e[4] for e in r)
+    report(f"fp8 fwd B=2 H=4 N=4096 d=64 causal={int(causal)}", heads=len(r), rmse_vs_dequantised=rmse_deq,
            rmse_vs_unquantised=rmse_exact, lse_vs_dequantised=lse_err)
     assert rmse_deq <= FP8_RMSE_REL, rmse_deq
     assert lse_err <= 1e-2, lse_err

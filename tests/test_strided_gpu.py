@@ -98,3 +98,79 @@ def test_bad_strides_are_refused():
     with pytest.raises(fa.FAError) as e:
         fa.fa_fwd(bad, k, v)
     assert e.value.status == 3
+
+
+# ------------------------------------------------------------ FP8 prepare, split-KV
+#
+# fa_fp8_prepare_strided reads its inputs at the strides and writes the dense
+# workspace: the whole workspace (codes and scales) must be bitwise that of the
+# dense call.  fa_fwd_splitkv_strided addresses q, k, v through the same TMA maps
+# and o through the merge kernel's strides: O and LSE bitwise those of dense.
+
+from oracle import attention_general  # noqa: E402
+from synth import outlier_qkv, rotation_signs  # noqa: E402
+
+
+def _padded_f32(t, pad=32):
+    B, H, N, d = t.shape
+    buf = torch.zeros((B, H, N, d + pad), dtype=t.dtype, device=t.device)
+    buf[..., :d] = t
+    return buf[..., :d]
+
+
+@pytest.mark.parametrize("layout", ["bnhd", "padded"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_prepare_strided_equals_dense(layout, dtype, d):
+    B, H, N = 2, 3, 333
+    x = outlier_qkv(B, H, N, d, seed=40 + d)
+    dense = [x[n].to(dtype).cuda() for n in ("q", "k", "v")]
+    view = [_bnhd(t) if layout == "bnhd" else _padded_f32(t) for t in dense]
+    assert not any(t.is_contiguous() for t in view)
+    s = rotation_signs(d, seed=41).cuda()
+    # Zeroed workspaces: the alignment gaps between regions are never written.
+    zws = lambda: torch.zeros(fa.fa_fp8_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    ws_dense = fa.fa_fp8_prepare(*dense, s, workspace=zws())
+    ws_view = fa.fa_fp8_prepare(*view, s, workspace=zws())
+    ws_seed_dense = fa.fa_fp8_prepare_seeded(*dense, 1234567, workspace=zws())
+    ws_seed_view = fa.fa_fp8_prepare_seeded(*view, 1234567, workspace=zws())
+    fa.fa_sync_check()
+    assert torch.equal(ws_dense, ws_view)
+    assert torch.equal(ws_seed_dense, ws_seed_view)
+
+
+@pytest.mark.parametrize("layout", ["bnhd", "padded"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_splitkv_strided_equals_dense(layout, causal, d):
+    B, H, Nq, Nk = 2, 3, 5, 1500
+    kv = normal_qkv(B, H, Nk, d, 50)
+    k, v = (kv[n].to(torch.bfloat16).cuda() for n in ("k", "v"))
+    q = normal_qkv(B, H, Nq, d, 51)["q"].to(torch.bfloat16).cuda()
+    conv = _bnhd if layout == "bnhd" else _padded
+    qv, kvv, vv = conv(q), conv(k), conv(v)
+    o_view = conv(torch.zeros_like(q))
+    o, lse = fa.fa_fwd_splitkv(q, k, v, n_split=4, causal=causal)
+    o2, lse2 = fa.fa_fwd_splitkv(qv, kvv, vv, o=o_view, n_split=4, causal=causal)
+    fa.fa_sync_check()
+    assert not o_view.is_contiguous()
+    assert torch.equal(o, o2.contiguous())
+    assert torch.equal(lse, lse2)
+    # Sanity against the oracle on one head (queries are the last Nq positions).
+    ref_o, ref_l = attention_general(q[:1, :1], k[:1, :1], v[:1, :1], d ** -0.5, causal)
+    assert o_excess(o2[:1, :1], ref_o) <= FWD_O_ATOL
+    assert max_abs(lse2[:1, :1], ref_l) <= FWD_LSE_ATOL
+
+
+def test_fp8_prepare_and_splitkv_bad_strides_are_refused():
+    q = torch.zeros((1, 2, 64, 136), dtype=torch.bfloat16, device="cuda")[..., :128]  # rows of 136: 16-byte multiples
+    bad = torch.zeros((1, 2, 64, 132), dtype=torch.bfloat16, device="cuda")[..., :128]  # rows of 132: not
+    s = rotation_signs(128, seed=1).cuda()
+    fa.fa_fp8_prepare(q, q, q, s)
+    with pytest.raises(fa.FAError) as e:
+        fa.fa_fp8_prepare(bad, q, q, s)
+    assert e.value.status == 3
+    with pytest.raises(fa.FAError) as e:
+        fa.fa_fwd_splitkv(q[:, :, :1], bad, q, n_split=2)
+    assert e.value.status == 3
+    fa.fa_sync_check()
