@@ -36,6 +36,7 @@
 //
 // Every mbarrier wait is bounded (see fa_device.cuh); on expiry the CTA sets a
 // device error word, drains its own in-flight copies, frees TMEM and exits.
+#include <limits.h>
 #include <math.h>
 
 #include "fa_device.cuh"
@@ -98,8 +99,9 @@ struct FwdCfg {
   static constexpr int kOOff = kTiles * kTileBytes;         // O staging, shared by both tiles in turn
   static constexpr int kRingOff = kOOff + kOBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
-  // q_full[2], q_empty[2], full[kSlots], empty[kSlots], s_full[2], p_full[2], o_done[2], epi[2], stg, drain
-  static constexpr int kNumBars = 2 + 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1;
+  // q_full[2], q_empty[2], full[kSlots], empty[kSlots], s_full[2], p_full[2], o_done[2], epi[2], stg, drain,
+  // shared-tile swap
+  static constexpr int kNumBars = 2 + 2 + 2 * kSlots + 2 + 2 + 2 + 2 + 1 + 1 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -112,13 +114,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, bool CAUSAL, bool FP8, bool SPLIT>
+// TAIL: the build for launches whose last pass is dealt out as shared tiles
+// (item_at); only the non-causal, whole-key forward has one.  Every other launch
+// uses the build without that code.
+template <int D, bool CAUSAL, bool FP8, bool SPLIT, bool TAIL = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                float* __restrict__ lse, int N, int H, int BH, int nunits, float scale_log2,
                unsigned int* err_word, unsigned long long wait_ns, int fault, Fp8Scales f8, KeySplit ks) {
   static_assert(!(SPLIT && FP8), "the split-KV variant is bf16 only");
+  static_assert(!(TAIL && (CAUSAL || SPLIT)), "shared tiles only for the non-causal, whole-key forward");
   using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -136,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_epi = bar_o + 2;             // [2] per tile: O staged in shared memory
   uint64_t* bar_stg = bar_epi + 2;           // O staging buffer read out by the previous store
   uint64_t* bar_drain = bar_stg + 1;
+  uint64_t* bar_xm = bar_drain + 1;          // shared tile: both warpgroups stored their (m, l)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
@@ -161,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_stg, 1);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_xm, 8);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -205,15 +213,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       for (int k = 0; ok; ++k) {
-        const int w = unit_of(k, cta, G);
-        if (w >= total) break;
-        int u, bh, sp;
-        decode_unit<CAUSAL>(w, nunits, BH, ks.nsplit, u, bh, sp);
-        const KvSpan a = kv_span<CAUSAL>(u, 0, sp, N, ks), b = kv_span<CAUSAL>(u, 1, sp, N, ks);
-        const int n_max = max(a.count, b.count);  // both tiles start at the split's first block
-        for (int j = 0; ok && j < n_max; ++j) {
-          ok = push(&tm_k, a.begin + j, bh);
-          if (ok) ok = push(&tm_v, a.begin + j, bh);
+        Item it;
+        if (!item_at<CAUSAL, TAIL>(unit_of(k, cta, G), total, nunits, BH, ks, it)) break;
+        // Every block of the item once, in order: for a whole unit the blocks of its
+        // longer tile (both tiles start at the split's first block), for a shared
+        // tile all of the tile's blocks.
+        const KvSpan a = kv_span<CAUSAL>(it.u, it.ts < 0 ? 0 : it.ts, it.sp, N, ks);
+        const int n_blocks = it.ts < 0 ? max(a.count, kv_span<CAUSAL>(it.u, 1, it.sp, N, ks).count) : a.count;
+        for (int j = 0; ok && j < n_blocks; ++j) {
+          ok = push(&tm_k, a.begin + j, it.bh);
+          if (ok) ok = push(&tm_v, a.begin + j, it.bh);
         }
       }
       if (!ok) {  // drain: the last (up to kSlots) issued copies may still be landing
@@ -230,18 +239,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nload[kTiles] = {0, 0};
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int w = unit_of(k, cta, G);
-        if (w >= total) break;
-        int u, bh, sp;
-        decode_unit<CAUSAL>(w, nunits, BH, ks.nsplit, u, bh, sp);
+        Item it;
+        if (!item_at<CAUSAL, TAIL>(unit_of(k, cta, G), total, nunits, BH, ks, it)) break;
         for (int t = 0; ok && t < kTiles; ++t) {
-          if (kv_span<CAUSAL>(u, t, sp, N, ks).count == 0) continue;
+          const SlotWork sw = slot_work<CAUSAL>(it, t, N, ks);  // a shared tile loads into both slots
+          if (sw.count == 0) continue;
           if (nload[t] > 0 && !(ok = mbar_wait(&bar_qe[t], (nload[t] - 1) & 1, wc, kSiteLoadQ))) break;
           mbar_arrive_expect_tx(&bar_q[t], C::kTileBytes);
 #pragma unroll
           for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_4d(sQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, &bar_q[t], b * kBoxCols,
-                        u * kRowsPerCta + t * kBlockQ, bh % H, bh / H);
+            tma_load_4d(sQ + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, &bar_q[t], b * kBoxCols, sw.row0,
+                        it.bh % H, it.bh / H);
           ++nload[t];
         }
       }
@@ -263,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nq_seen[kTiles] = {0, 0};  // Q tiles consumed so far (bar_q phase)
       int np[kTiles] = {0, 0};       // P blocks consumed so far (bar_p phase)
       bool ok = true;
+      Item shared_item{0, 0, 0, -1};
 
       // Base descriptors; every MMA operand below is one of these advanced by a
       // compile-time byte offset (a single 32-bit add on the issuing thread).
@@ -306,11 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 
       for (int k = 0; ok; ++k) {
-        const int w = unit_of(k, cta, G);
-        if (w >= total) break;
-        int u, bh, sp;
-        decode_unit<CAUSAL>(w, nunits, BH, ks.nsplit, u, bh, sp);
-        const int nq[kTiles] = {kv_span<CAUSAL>(u, 0, sp, N, ks).count, kv_span<CAUSAL>(u, 1, sp, N, ks).count};
+        Item itm;
+        if (!item_at<CAUSAL, TAIL>(unit_of(k, cta, G), total, nunits, BH, ks, itm)) break;
+        if (TAIL && itm.ts >= 0) {  // a shared tile: always the CTA's last item (below)
+          shared_item = itm;
+          break;
+        }
+        const int u = itm.u;
+        const int nq[kTiles] = {kv_span<CAUSAL>(u, 0, itm.sp, N, ks).count, kv_span<CAUSAL>(u, 1, itm.sp, N, ks).count};
         const int n_max = max(nq[0], nq[1]);
         if (n_max == 0) continue;  // an empty key split: nothing was loaded for it
         // Prologue: S_a = Q_a K_0^T, S_b = Q_b K_0^T.  S_t is free: the previous
@@ -373,6 +385,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (TAIL && ok && shared_item.ts >= 0) {
+        // A shared tile: slot t takes key blocks t, t + 2, ... of the tile (Q loaded
+        // into both slots).  K_j is ring item i0 + 2j and V_j item i0 + 2j + 1;
+        // they are consumed slightly out of order (K_{j+2} before V_{j+1}), which
+        // the ring of at least 4 slots, filled in order, always allows.
+        const Item& itm = shared_item;
+        const int n = kv_span<CAUSAL>(itm.u, itm.ts, itm.sp, N, ks).count;  // 0: past the last query row
+        const int i0 = item;
+        auto wait_item = [&](int i, uint32_t site) {
+          return mbar_wait(&bar_full[i % C::kSlots], (i / C::kSlots) & 1, wc, site);
+        };
+        for (int t = 0; ok && t < kTiles && t < n; ++t) {  // S_t = Q K_t^T
+          if (!(ok = wait_item(i0 + 2 * t, kSiteMmaK))) break;
+          if (!(ok = mbar_wait(&bar_q[t], nq_seen[t] & 1, wc, kSiteMmaQ))) break;
+          tc_fence_after();
+          qk(t, (i0 + 2 * t) % C::kSlots);
+          if (t + 2 >= n) mma_commit(&bar_qe[t]);
+          mma_commit(&bar_empty[(i0 + 2 * t) % C::kSlots]);
+        }
+        for (int j = 0; ok && j < n; ++j) {
+          const int t = j & 1;
+          if (!(ok = wait_item(i0 + 2 * j + 1, kSiteMmaV))) break;
+          // (np indexed by constants only: a runtime index would put it in local memory)
+          if (!(ok = mbar_wait(&bar_p[t], (t ? np[1] : np[0]) & 1, wc, kSiteMmaP))) break;
+          if (t) ++np[1]; else ++np[0];
+          tc_fence_after();
+          pv(t, (i0 + 2 * j + 1) % C::kSlots, j >= 2);  // slot t's first block (j = t) overwrites O_t
+          mma_commit(&bar_empty[(i0 + 2 * j + 1) % C::kSlots]);
+          if (j + 2 >= n) {
+            mma_commit(&bar_o[t]);
+          } else {  // S_t = Q K_{j+2}^T, the slot's next block
+            if (!(ok = wait_item(i0 + 2 * j + 4, kSiteMmaK))) break;
+            tc_fence_after();
+            qk(t, (i0 + 2 * j + 4) % C::kSlots);
+            if (j + 4 >= n) mma_commit(&bar_qe[t]);
+            mma_commit(&bar_empty[(i0 + 2 * j + 4) % C::kSlots]);
+          }
+        }
+      }
       // Every issued MMA must finish before TMEM is released.
       mma_commit(bar_drain);
       mbar_wait_drain(bar_drain, 0, wait_ns);
@@ -387,23 +438,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t col_s = C::col_s(t);
     const uint32_t col_o = C::col_o(t);
-    uint32_t scnt = 0;  // S blocks consumed so far (bar_s phase)
-    uint32_t ocnt = 0;  // units finished by this tile (bar_o, bar_epi phase)
-    uint32_t nepi = 0;  // epilogues of both tiles before this unit's (bar_stg phase)
+    uint32_t scnt = 0;             // S blocks consumed so far (bar_s phase)
+    uint32_t oc0 = 0, oc1 = 0;     // items in which slot 0 / slot 1 had keys (bar_o, bar_epi phases)
+    uint32_t nepi = 0;             // epilogues before this item's (bar_stg phase)
     bool ok = true;
+    // What the merge epilogue of a shared tile needs once the item loop is left.
+    struct {
+      bool pending = false;
+      float m = 0.f, l = 0.f, svmax = 1.f;
+      int bh = 0, qrow0 = 0;
+      uint32_t ph0 = 0, ph1 = 0, epi_index = 0;
+    } sh;
     for (int k = 0; ok; ++k) {
-      const int w = unit_of(k, cta, G);
-      if (w >= total) break;
-      int u, bh, sp;
-      decode_unit<CAUSAL>(w, nunits, BH, ks.nsplit, u, bh, sp);
-      const KvSpan span = kv_span<CAUSAL>(u, t, sp, N, ks);
-      const int n_a = kv_span<CAUSAL>(u, 0, sp, N, ks).count;
-      const int n_b = kv_span<CAUSAL>(u, 1, sp, N, ks).count;
-      const int nkt = span.count;
-      // Epilogues run in (unit, tile) order through one staging buffer.
-      const uint32_t epi_index = nepi + ((t == 1 && n_a > 0) ? 1u : 0u);
-      nepi += (n_a > 0 ? 1u : 0u) + (n_b > 0 ? 1u : 0u);
-      const int qrow0 = u * kRowsPerCta + t * kBlockQ;
+      Item itm;
+      if (!item_at<CAUSAL, TAIL>(unit_of(k, cta, G), total, nunits, BH, ks, itm)) break;
+      const int bh = itm.bh, sp = itm.sp;
+      const bool shared = itm.ts >= 0;  // both warpgroups on one tile (see item_at)
+      const SlotWork sw = slot_work<CAUSAL>(itm, t, N, ks);
+      const bool has0 = slot_work<CAUSAL>(itm, 0, N, ks).count > 0;
+      const bool has1 = slot_work<CAUSAL>(itm, 1, N, ks).count > 0;
+      const int nkt = sw.count;
+      const uint32_t ph0 = oc0, ph1 = oc1;          // this item's phases of slot 0 and slot 1
+      const uint32_t ph_t = t == 0 ? ph0 : ph1;     // own slot
+      oc0 += has0 ? 1u : 0u;
+      oc1 += has1 ? 1u : 0u;
+      // Epilogues run in (item, tile) order through one staging buffer; a shared
+      // tile has one.
+      const uint32_t epi_index = nepi + ((!shared && t == 1 && has0) ? 1u : 0u);
+      nepi += shared ? (has0 ? 1u : 0u) : (has0 ? 1u : 0u) + (has1 ? 1u : 0u);
+      const int qrow0 = sw.row0;
       const int qrow = qrow0 + row;
       if (nkt == 0) {
         // No key of this split is visible to the tile: an empty partial.
@@ -438,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (FP8) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int kt = 2 * (span.begin + jj) + h;
+            const int kt = 2 * (sw.begin + sw.step * jj) + h;
             const bool in = jj < nkt && kt < f8.ntiles;
             nsk[h] = in ? skh[kt] : 1.f;
             nsv[h] = in ? svh[kt] : svmax;
@@ -453,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const int kbase = (span.begin + j) * kBlockK;
+        const int kbase = (sw.begin + sw.step * j) * kBlockK;
         // Some key of the block is past Nk, or beyond what the tile's first row sees.
         const bool need_mask = (kbase + kBlockK > ks.Nk) || (CAUSAL && kbase + kBlockK - 1 > qrow0 + ks.coff);
         // Per 64-key half h: multiplier c[h] of the raw score (FP8: times that key
@@ -663,8 +726,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
 
+      if (TAIL && shared) {  // the merge epilogue follows the loop (always the last item)
+        sh.pending = true;
+        sh.m = m_used;
+        sh.l = l;
+        sh.svmax = svmax;
+        sh.bh = bh;
+        sh.qrow0 = qrow0;
+        sh.ph0 = ph0;
+        sh.ph1 = ph1;
+        sh.epi_index = epi_index;
+        break;
+      }
       // ---------------------------------------------------------- epilogue
-      if (!(ok = warp_wait(&bar_o[t], ocnt & 1, wc, kSiteSoftO))) break;
+      if (!(ok = warp_wait(&bar_o[t], ph_t & 1, wc, kSiteSoftO))) break;
       tc_fence_after();
       if constexpr (SPLIT) {
         // Partial of this split: O / l in fp32 straight from TMEM, LSE in natural
@@ -687,7 +762,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         if (qrow < N)
           ks.lse_part[(static_cast<size_t>(sp) * BH + bh) * N + qrow] = seen ? (m_used + log2f(l)) * kLn2 : -INFINITY;
-        ++ocnt;
         continue;
       }
       // The staging buffer is free once the previous epilogue's store has read it.
@@ -722,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bar_epi[t]);
       if (qrow < N) lse[static_cast<size_t>(bh) * N + qrow] = (m_used + log2f(l)) * kLn2;
       if (row == 0) {
-        if ((ok = mbar_wait(&bar_epi[t], ocnt & 1, wc, kSiteEpi))) {
+        if ((ok = mbar_wait(&bar_epi[t], ph_t & 1, wc, kSiteEpi))) {
 #pragma unroll
           for (int b = 0; b < C::kOBoxes; ++b)
             tma_store_4d(&tm_o, sO + b * C::kBoxBytes, b * kBoxCols, qrow0, bh % H, bh / H);
@@ -731,8 +805,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      ++ocnt;
     }
+    if (TAIL && ok && sh.pending) do {
+      // Shared tile: slot t holds the softmax of the tile over key blocks t, t+2,
+      // ... (running maximum m_t, sum l_t, O_t).  Once the other slot's last P V
+      // is done too, the two warpgroups swap (m, l) through the Q buffer (every
+      // Q K^T of the item has completed) and each writes half of O's columns:
+      //   O = (a_0 O_0 + a_1 O_1) / (a_0 l_0 + a_1 l_1),  a_t = 2^(m_t - max(m_0, m_1)).
+      // (At most one shared tile per CTA, its last item: the barrier is used once.)
+      if (!(ok = warp_wait(&bar_o[t], (t == 0 ? sh.ph0 : sh.ph1) & 1, wc, kSiteSoftO))) break;
+      if (!(ok = warp_wait(&bar_o[t ^ 1], (t == 0 ? sh.ph1 : sh.ph0) & 1, wc, kSiteSoftO))) break;
+      tc_fence_after();
+      float2* xch = reinterpret_cast<float2*>(sQ);
+      xch[t * kBlockQ + row] = make_float2(sh.m, sh.l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_xm);
+      if (!(ok = warp_wait(bar_xm, 0, wc, kSiteSoftO))) break;
+      const float2 other = xch[(t ^ 1) * kBlockQ + row];
+      const float m0 = t == 0 ? sh.m : other.x, l0 = t == 0 ? sh.l : other.y;
+      const float m1 = t == 0 ? other.x : sh.m, l1 = t == 0 ? other.y : sh.l;
+      const float mm = fmaxf(m0, m1);
+      const float a0 = ex2_approx(m0 - mm), a1 = ex2_approx(m1 - mm);
+      const float lsum = l0 * a0 + l1 * a1;
+      const float inv_l = sh.svmax / lsum;  // svmax = 1 for bf16
+      if (sh.epi_index > 0 && !(ok = warp_wait(bar_stg, (sh.epi_index - 1) & 1, wc, kSiteEpi))) break;
+      const float2 w0 = make_float2(a0 * inv_l, a0 * inv_l), w1 = make_float2(a1 * inv_l, a1 * inv_l);
+#pragma unroll 1
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = t * (D / 64) + cc;  // 32-column chunk of O written by this warpgroup
+        uint32_t o0[32], o1[32];
+        tmem_ld32(trow + C::col_o(0) + c * 32, o0);
+        tmem_ld32(trow + C::col_o(1) + c * 32, o1);
+        tmem_ld_wait32(o0);
+        tmem_ld_wait32(o1);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 v = __ffma2_rn(make_float2(__uint_as_float(o0[2 * i]), __uint_as_float(o0[2 * i + 1])), w0,
+                                      __fmul2_rn(make_float2(__uint_as_float(o1[2 * i]),
+                                                             __uint_as_float(o1[2 * i + 1])), w1));
+          pk[i] = pack_bf16x2(v.x, v.y);
+        }
+        uint8_t* box = sO + (c / 2) * C::kBoxBytes + row * 128;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chunk = (c % 2) * 4 + q4;
+          const uint4 val = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          *reinterpret_cast<uint4*>(box + ((chunk ^ (row & 7)) * 16)) = val;
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_epi[t]);
+      const int qrow = sh.qrow0 + row;
+      if (t == 0 && qrow < N) lse[static_cast<size_t>(sh.bh) * N + qrow] = (mm + log2f(lsum)) * kLn2;
+      if (t == 0 && row == 0) {
+        if ((ok = mbar_wait(&bar_epi[0], sh.ph0 & 1, wc, kSiteEpi) &&
+                  mbar_wait(&bar_epi[1], sh.ph1 & 1, wc, kSiteEpi))) {
+#pragma unroll
+          for (int b = 0; b < C::kOBoxes; ++b)
+            tma_store_4d(&tm_o, sO + b * C::kBoxBytes, b * kBoxCols, sh.qrow0, sh.bh % H, sh.bh / H);
+          tma_store_commit_and_wait_read();
+          mbar_arrive(bar_stg);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    } while (false);
     __syncwarp();
   }
 
@@ -751,13 +890,6 @@ cudaError_t launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   using C = FwdCfg<D, FP8>;
   cudaError_t e;
   auto kern = fwd_kernel<D, CAUSAL, FP8, SPLIT>;
-  // Per device and idempotent; cheap enough to repeat on every launch.
-  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes))) return e;
-  // setmaxnreg.inc can only draw on the registers the block was launched with; a
-  // build that allocated fewer per thread than the split assumes would stall.
-  cudaFuncAttributes fattr;
-  if ((e = cudaFuncGetAttributes(&fattr, kern))) return e;
-  if (static_cast<uint32_t>(fattr.numRegs) * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
   const int nunits = (N + kRowsPerCta - 1) / kRowsPerCta;
   // Persistent: one CTA per SM (shared memory and TMEM admit no second), each
   // walking its share of the units.
@@ -765,14 +897,38 @@ cudaError_t launch_kernel(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   if ((e = cudaGetDevice(&dev))) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
   const long long units = static_cast<long long>(nunits) * BH * ks.nsplit;
-  dim3 grid(static_cast<unsigned>(min(units, static_cast<long long>(sms))));
+  // Non-causal, unsplit keys, at least two key blocks: if the units leave a partial
+  // last pass of R <= sms / 2 units, its units are dealt out as 2R shared tiles
+  // (item_at), so that pass takes about half a unit's time.  The build with shared
+  // tiles runs whole units about 3 % slower (measured), so it is used only when
+  // the saving, half a pass of P + 1, is large: P <= 4 full passes.
+  KeySplit kse = ks;
+  long long items = units;
+  if constexpr (!CAUSAL && !SPLIT) {
+    if (ks.nsplit == 1 && (ks.Nk + kBlockK - 1) / kBlockK >= 2) {
+      const long long full = units / sms * sms, rem = units - full;
+      if (rem > 0 && 2 * rem <= sms && full / sms <= 4) {
+        kse.tail_from = static_cast<int>(full);
+        items = full + 2 * rem;
+        kern = fwd_kernel<D, CAUSAL, FP8, SPLIT, true>;
+      }
+    }
+  }
+  // Per device and idempotent; cheap enough to repeat on every launch.
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes))) return e;
+  // setmaxnreg.inc can only draw on the registers the block was launched with; a
+  // build that allocated fewer per thread than the split assumes would stall.
+  cudaFuncAttributes fattr;
+  if ((e = cudaFuncGetAttributes(&fattr, kern))) return e;
+  if (static_cast<uint32_t>(fattr.numRegs) * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+  dim3 grid(static_cast<unsigned>(min(items, static_cast<long long>(sms))));
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, lse, N, H, BH, nunits, scale_log2, err_word,
-                                                   dbg.wait_limit_ns, dbg.fault, f8, ks);
+                                                   dbg.wait_limit_ns, dbg.fault, f8, kse);
   return cudaGetLastError();
 }
 
 // The plain forward: one split over all N keys, queries aligned with keys.
-KeySplit whole_keys(int N) { return KeySplit{N, 1, (N + kBlockK - 1) / kBlockK, 0, nullptr, nullptr}; }
+KeySplit whole_keys(int N) { return KeySplit{N, 1, (N + kBlockK - 1) / kBlockK, 0, nullptr, nullptr, INT_MAX}; }
 
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
@@ -798,7 +954,7 @@ cudaError_t launch_splitkv_impl(const SplitKvArgs& a, cudaStream_t stream) {
   if ((e = make_tmap_4d(&tq, a.q, kBf16, 2, D, a.Nq, a.H, a.B, a.sq.s, kBoxCols, kBlockQ))) return e;
   if ((e = make_tmap_4d(&tk, a.k, kBf16, 2, D, a.Nk, a.H, a.B, a.sk.s, kBoxCols, kBlockK))) return e;
   if ((e = make_tmap_4d(&tv, a.v, kBf16, 2, D, a.Nk, a.H, a.B, a.sv.s, kBoxCols, kBlockK))) return e;
-  const KeySplit ks{a.Nk, a.n_split, splitkv_kbps(a.Nk, a.n_split), a.Nk - a.Nq, a.o_part, a.lse_part};
+  const KeySplit ks{a.Nk, a.n_split, splitkv_kbps(a.Nk, a.n_split), a.Nk - a.Nq, a.o_part, a.lse_part, INT_MAX};
   // The partial epilogue stores fp32 rows itself; the O tensor map is never used.
   return launch_kernel<D, CAUSAL, false, true>(tq, tk, tv, tq, nullptr, a.Nq, a.H, BH, a.scale * 1.4426950408889634f,
                                                a.err_word, a.dbg, Fp8Scales{nullptr, nullptr, nullptr, 0}, ks, stream);

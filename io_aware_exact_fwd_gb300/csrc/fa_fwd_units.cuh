@@ -1,4 +1,4 @@
-// Work units of the persistent forward kernels (fa_fwd.cu, fa_fwd_fp8.cu): a unit
+// Work units of the persistent forward kernel (fa_fwd.cu): a unit
 // is 256 query rows (two 128-row tiles) of one head and, for the split-KV
 // forward, one range of its keys.  Each persistent CTA walks a fixed list of
 // units; causal units are numbered heaviest first and dealt out in zigzag passes
@@ -25,6 +25,7 @@ struct KeySplit {
   int coff;
   float* o_part;
   float* lse_part;
+  int tail_from;  // work items >= tail_from are shared tiles (see item_at); INT_MAX: none
 };
 
 // K/V blocks [begin, begin + count) that query tile t of unit (u, split s) attends
@@ -72,9 +73,47 @@ __device__ __forceinline__ void decode_unit(int w, int nunits, int BH, int nspli
   }
 }
 
-// k-th unit of CTA c out of G persistent CTAs: pass k covers units kG .. kG+G-1,
+// k-th work item of CTA c out of G persistent CTAs: pass k covers items kG .. kG+G-1,
 // in increasing CTA order on even passes and decreasing on odd ones.
 __device__ __forceinline__ int unit_of(int k, int c, int G) { return k * G + ((k & 1) ? (G - 1 - c) : c); }
+
+// A work item: a whole unit (ts = -1: query tile t of the unit goes to warpgroup /
+// Q slot / TMEM buffer t, each with all its keys), or one query tile ts of a unit
+// shared by both warpgroups, slot t taking the tile's key blocks t, t+2, t+4, ...
+// and the two partial softmaxes merged at the end.  Shared tiles fill the last
+// pass when the units do not divide evenly over the CTAs (non-causal only): the
+// R leftover units become 2R shared tiles on 2R <= G CTAs, so that pass takes
+// about half a unit's time instead of a whole one.
+struct Item {
+  int u, bh, sp, ts;
+};
+template <bool CAUSAL, bool TAIL>
+__device__ __forceinline__ bool item_at(int w, int total, int nunits, int BH, const KeySplit& ks, Item& it) {
+  int wu = w;
+  it.ts = -1;
+  if (TAIL && w >= ks.tail_from) {  // only the kernel built for shared tiles has them
+    wu = ks.tail_from + (w - ks.tail_from) / 2;
+    it.ts = (w - ks.tail_from) & 1;
+  }
+  if (wu >= total) return false;
+  decode_unit<CAUSAL>(wu, nunits, BH, ks.nsplit, it.u, it.bh, it.sp);
+  return true;
+}
+
+// Query rows and key blocks of slot t for an item: rows row0 .. row0 + 127, key
+// blocks begin, begin + step, ... (count of them).
+struct SlotWork {
+  int row0, begin, count, step;
+};
+template <bool CAUSAL>
+__device__ __forceinline__ SlotWork slot_work(const Item& it, int t, int N, const KeySplit& ks) {
+  if (it.ts < 0) {
+    const KvSpan s = kv_span<CAUSAL>(it.u, t, it.sp, N, ks);
+    return {it.u * kRowsPerCta + t * kBlockQ, s.begin, s.count, 1};
+  }
+  const KvSpan s = kv_span<CAUSAL>(it.u, it.ts, it.sp, N, ks);
+  return {it.u * kRowsPerCta + it.ts * kBlockQ, s.begin + t, (s.count + 1 - t) / 2, 2};
+}
 
 
 }  // namespace fa

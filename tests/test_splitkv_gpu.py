@@ -107,18 +107,38 @@ def test_all_splits_empty_row():
     assert torch.all(o[0, 0, 1] == 2.0) and abs(float(lse[0, 0, 1]) - 0.5) < 1e-6
 
 
+def _fwd_takes_whole_units(B, H, N, causal):
+    # fa_fwd deals a partial last pass of R <= SMs / 2 non-causal units (after at
+    # most 4 full passes) out as 2R shared tiles (two warpgroups on one tile,
+    # partial softmaxes merged): the same values up to rounding, but not bitwise
+    # those of one whole-key split.
+    units = B * H * ((N + 255) // 256)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rem = units % sms
+    return causal or N <= 128 or rem == 0 or 2 * rem > sms or units // sms > 4
+
+
+@pytest.mark.parametrize("B, N", [(2, 700), (40, 700)])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("d", [64, 128])
-def test_one_split_equals_fa_fwd_bitwise(causal, d):
+def test_one_split_equals_fa_fwd(B, N, causal, d):
     # With one split and Nq == Nk the partial is the forward's O and LSE before
-    # the bf16 rounding; the merge of one split multiplies by exactly 1.
-    B, H, N = 2, 2, 700
+    # the bf16 rounding; the merge of one split multiplies by exactly 1.  Bitwise
+    # when fa_fwd takes whole units; otherwise within one bf16 rounding of O.
+    H = 2
     q, k, v = _inputs(B, H, N, N, d, 9)
     o1, l1 = fa.fa_fwd(q, k, v, causal=causal)
     o2, l2 = fa.fa_fwd_splitkv(q, k, v, n_split=1, causal=causal)
     fa.fa_sync_check()
-    assert torch.equal(o1, o2)
-    assert torch.equal(l1, l2)
+    if _fwd_takes_whole_units(B, H, N, causal):
+        assert torch.equal(o1, o2)
+        assert torch.equal(l1, l2)
+    else:
+        # Both round the same exact values to bf16: at most one bf16 step apart
+        # (2^-7 relative), plus a small absolute slack where |O| is tiny.
+        a, b = o1.float(), o2.float()
+        assert bool(((a - b).abs() <= 2.0 ** -7 * torch.maximum(a.abs(), b.abs()) + 1e-3).all())
+        assert float((l1 - l2).abs().max()) <= 1e-5
 
 
 @pytest.mark.parametrize("causal", [False, True])
