@@ -208,7 +208,8 @@ FA_API int fa_bwd_dq(const void* workspace, size_t ws_bytes, void* dq, int B, in
  *  - Arguments are validated exactly as fa_bwd validates them (same statuses)
  *    before the buffer is touched; then sizes whose fa_bwd_workspace_size()
  *    exceeds the buffer are rejected with FA_ERR_WORKSPACE before anything is
- *    launched (at d = 128 this admits about B*H*N <= 127,000 rows).
+ *    launched (this admits B*H*N up to about 116,000 rows at d = 128 and
+ *    209,000 at d = 64).
  *  - It calls no cudaMalloc, cudaFree or other allocating routine.
  *  - Every call looks up the buffer's device address in the context current on
  *    the calling thread (a table lookup; a context replaced since, e.g. by

@@ -126,7 +126,10 @@ __device__ __forceinline__ void pow2_scale(float amax, float& sigma, float& inv)
   inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
 }
 
-template <int D>
+// STRIDED: inputs at the caller's strides; otherwise dense [B, H, N, d] (the
+// index arithmetic of the dense build is cheaper, and this kernel is partly
+// issue-bound).
+template <int D, bool STRIDED>
 __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* __restrict__ q,
                                                                    const void* __restrict__ k,
                                                                    const void* __restrict__ v, int in_bf16,
@@ -145,9 +148,15 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
   __shared__ float s_amax[8];
   __shared__ __align__(16) uint8_t s_vt[D * kVtPitch];  // V codes of this tile, transposed [d][64 (+4)]
 
-  // Element (b, h, row, c) of an input at b s[2] + h s[1] + row s[0] + c.
-  const Strides& sin = which == 0 ? sq : (which == 1 ? sk : sv);
-  const size_t head_off = static_cast<size_t>(bh / H) * sin.s[2] + static_cast<size_t>(bh % H) * sin.s[1];
+  // Element (b, h, row, c) of an input at b s[2] + h s[1] + row s[0] + c (dense:
+  // (bh N + row) d + c).
+  size_t head_off = static_cast<size_t>(bh) * N * D;
+  int64_t row_stride = D;
+  if constexpr (STRIDED) {
+    const Strides& sin = which == 0 ? sq : (which == 1 ? sk : sv);
+    head_off = static_cast<size_t>(bh / H) * sin.s[2] + static_cast<size_t>(bh % H) * sin.s[1];
+    row_stride = sin.s[0];
+  }
   float x[kRowsPerWarp][E];
   if (which == 2) {
     // ------------------------------------------------ V: no rotation, transposed out
@@ -160,7 +169,7 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
       for (int m = 0; m < E; ++m) {
         float val = 0.f;
         if (row < N) {
-          const size_t e = head_off + static_cast<size_t>(row) * sin.s[0] + lane + 32 * m;
+          const size_t e = head_off + static_cast<size_t>(row) * row_stride + lane + 32 * m;
           val = in_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(v)[e]) : static_cast<const float*>(v)[e];
         }
         x[r][m] = val;
@@ -215,7 +224,7 @@ __global__ void __launch_bounds__(kPrepThreads) fp8_prepare_kernel(const void* _
   for (int p = 0; p < kPasses; ++p) {
     const int row = tile * kTileRows + warp * kRowsPerWarp + p * kRowsPerPass + rg;
     if (row < N) {
-      load16(src, head_off + static_cast<size_t>(row) * sin.s[0] + kE * sl, in_bf16, xr[p]);
+      load16(src, head_off + static_cast<size_t>(row) * row_stride + kE * sl, in_bf16, xr[p]);
     } else {
 #pragma unroll
       for (int i = 0; i < kE; ++i) xr[p][i] = 0.f;
@@ -274,12 +283,17 @@ cudaError_t launch_fp8_prepare(const Fp8PrepArgs& a, cudaStream_t stream) {
   const Fp8Layout lay = fp8_layout(a.B, a.H, a.N, a.d);
   dim3 grid(static_cast<unsigned>(lay.npad / kTileRows), static_cast<unsigned>(a.B * a.H), 3);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  const Strides dense = dense_strides(a.H, a.N, a.d);
+  auto same = [&](const Strides& x) { return x.s[0] == dense.s[0] && x.s[1] == dense.s[1] && x.s[2] == dense.s[2]; };
+  const bool strided = !(same(a.sq) && same(a.sk) && same(a.sv));
+  auto go = [&](auto kern) {
+    kern<<<grid, kPrepThreads, 0, stream>>>(a.q, a.k, a.v, a.in_bf16, a.signs, a.seed, lay, ws, a.N, a.H, a.sq, a.sk,
+                                            a.sv);
+  };
   if (a.d == 64)
-    fp8_prepare_kernel<64><<<grid, kPrepThreads, 0, stream>>>(a.q, a.k, a.v, a.in_bf16, a.signs, a.seed, lay, ws,
-                                                              a.N, a.H, a.sq, a.sk, a.sv);
+    strided ? go(fp8_prepare_kernel<64, true>) : go(fp8_prepare_kernel<64, false>);
   else
-    fp8_prepare_kernel<128><<<grid, kPrepThreads, 0, stream>>>(a.q, a.k, a.v, a.in_bf16, a.signs, a.seed, lay, ws,
-                                                               a.N, a.H, a.sq, a.sk, a.sv);
+    strided ? go(fp8_prepare_kernel<128, true>) : go(fp8_prepare_kernel<128, false>);
   return cudaGetLastError();
 }
 
