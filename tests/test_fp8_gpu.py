@@ -190,6 +190,35 @@ def test_fp8_forward_d64_all_heads(causal):
     assert rmse_exact <= 1e-1, rmse_exact
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_forward_shared_tail_all_heads(d):
+    # B=1, H=160, N=512: 320 units, two full passes and 16 leftover units run as 32
+    # shared tiles (two warpgroups on one tile's even and odd key blocks, merged).
+    # Every head against the dequantised reference.
+    B, H, N = 1, 160, 512
+    x = outlier_qkv(B, H, N, d, seed=70 + d)
+    s = rotation_signs(d, seed=70)
+    ws = fa.fa_fp8_prepare(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), s.cuda())
+    o, lse = fa.fa_fwd_fp8(ws, (B, H, N, d))
+    fa.fa_sync_check()
+    scale = d ** -0.5
+    oh, lh = host_f64(o), host_f64(lse)
+
+    def one(b, h):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = fp8_prepare(x["q"][sl], x["k"][sl], x["v"][sl], s.numpy())
+        qd, kd, vd = _dequantised(ref)
+        od, ld = attention_forward(qd, kd, vd, scale / d, False)
+        return float(((oh[sl] - od) ** 2).sum()), float((od ** 2).sum()), float(np.abs(lh[sl] - ld).max())
+
+    r = map_heads(one, [(0, h) for h in range(H)])
+    rmse = np.sqrt(sum(e[0] for e in r) / sum(e[1] for e in r))
+    lse_err = max(e[2] for e in r)
+    report(f"fp8 fwd shared tail B=1 H=160 N=512 d={d}", heads=H, rmse_vs_dequantised=rmse, lse_vs_dequantised=lse_err)
+    assert rmse <= FP8_RMSE_REL, rmse
+    assert lse_err <= 1e-2, lse_err
+
+
 def test_prepare_extreme_tiles_bit_exact():
     # Tile scales at the ends of the power-of-two rule: an all-zero tile (scale 1), a
     # tile near the fp32 maximum (V: amax 3e38, exponent 120), a tile whose amax is an

@@ -152,6 +152,33 @@ def test_dominant_score_selects_value_row():
     assert o_excess(o[0, 0, :d], vd[0, 0, target]) <= FWD_O_ATOL
 
 
+def _shared_tail(B, H, N):
+    # Whether fa_fwd deals its partial last pass out as shared tiles on this device
+    # (non-causal; 0 < R = units mod SMs, 2R <= SMs, at most 4 full passes, N > 128).
+    units = B * H * ((N + 255) // 256)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rem = units % sms
+    return N > 128 and rem > 0 and 2 * rem <= sms and units // sms <= 4
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("B,H,N", [(1, 160, 512), (2, 44, 1536), (3, 20, 700)])
+def test_shared_tail_tiles_all_heads(B, H, N, d):
+    # Launches whose last pass runs as shared tiles after one to four full passes of
+    # whole units (and a ragged N = 700): every head against the oracle, the
+    # softmax of each shared tile being split over two warpgroups (even and odd key
+    # blocks) and merged; then bitwise reproducible.
+    if not _shared_tail(B, H, N):
+        pytest.skip("this device's SM count gives no shared last pass for the shape")
+    o, lse = _run_and_compare(B, H, N, d, False, seed=46 + d,
+                              name=f"fwd shared tail B={B} H={H} N={N} d={d}")
+    x = normal_qkv(B, H, N, d, 46 + d)
+    q, k, v = to_dev_bf16(x)
+    o2, l2 = fa.fa_fwd(q, k, v)
+    fa.fa_sync_check()
+    assert torch.equal(o, o2) and torch.equal(lse, l2)
+
+
 def test_forward_is_bitwise_deterministic():
     x = normal_qkv(2, 4, 1500, 128, 44)
     q, k, v = to_dev_bf16(x)
