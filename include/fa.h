@@ -399,8 +399,9 @@ FA_API size_t fa_splitkv_workspace_size(int B, int H, int Nq, int d, int n_split
 
 /* A split count for these sizes on the current device: the fewest splits (1..64,
  * each of at least 4 key blocks) within 2 % of the best balance of work units over
- * the SMs; 1 when Nq > 128 and the unsplit units already cover every SM.  Returns
- * >= 1, or 0 for invalid sizes. */
+ * the SMs (for Nq == 1 at d == 64, over the SMs times the CTAs of the one-row
+ * kernel resident on each); 1 when Nq > 128 and the unsplit units already cover
+ * every SM.  Returns >= 1, or 0 for invalid sizes. */
 FA_API int fa_splitkv_default_splits(int B, int H, int Nq, int Nk, int d);
 
 /*
@@ -409,7 +410,8 @@ FA_API int fa_splitkv_default_splits(int B, int H, int Nq, int Nk, int d);
  *   o_part   : float [n_split, B, H, Nq, d]  (output; rows of empty splits unwritten)
  *   lse_part : float [n_split, B, H, Nq]     (output, every element written)
  * Numerics: as fa_fwd (fp32 scores on the tensor cores, bf16 P for P V), but O_s
- * stays fp32.  Errors: as fa_fwd; FA_ERR_INVALID_ARG also for n_split outside
+ * stays fp32; for Nq == 1 at d == 64 every step is fp32 on the CUDA cores (P is
+ * not rounded to bf16).  Errors: as fa_fwd; FA_ERR_INVALID_ARG also for n_split outside
  * [1, 1024], Nk < 1, or causal with Nq > Nk.  B * H * Nq == 0 is a no-op.
  */
 FA_API int fa_fwd_splitkv_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part,

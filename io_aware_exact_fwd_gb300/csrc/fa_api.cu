@@ -264,13 +264,16 @@ int validate_splitkv(int B, int H, int Nq, int Nk, int d, int n_split, int causa
   return FA_OK;
 }
 
-int default_splits(int B, int H, int Nq, int Nk) {
+int default_splits(int B, int H, int Nq, int Nk, int d) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                  cudaSuccess || sms < 1)
     sms = 148;
   const long long units = static_cast<long long>(B) * H * ((Nq + 2 * fa::kBlockQ - 1) / (2 * fa::kBlockQ));
   const int nkb = (Nk + fa::kBlockK - 1) / fa::kBlockK;
+  // One query row runs one small CTA per (head, split), several resident per SM:
+  // balance over those slots rather than over SMs.
+  if (fa::decode_takes(Nq, d)) sms *= fa::decode_ctas_per_sm(d);
   // Many query rows and a full GPU: splitting would only add partials to merge.
   if (Nq > fa::kBlockQ && units >= sms) return 1;
   // Splits of at least 4 key blocks keep the per-unit Q load and epilogue small
@@ -297,7 +300,7 @@ size_t fa_splitkv_workspace_size(int B, int H, int Nq, int d, int n_split) {
 
 int fa_splitkv_default_splits(int B, int H, int Nq, int Nk, int d) {
   if (validate_splitkv(B, H, Nq, Nk, d, 1, 0, 1.f) != FA_OK) return 0;
-  return default_splits(B, H, Nq, Nk);
+  return default_splits(B, H, Nq, Nk, d);
 }
 
 int fa_fwd_splitkv_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int B, int H,
@@ -367,7 +370,7 @@ int fa_fwd_splitkv_strided(const void* q, const int64_t* q_strides, const void* 
     const int pre = validate_splitkv(B, H, Nq, Nk, d, 1, causal, scale);
     if (pre < 0) return FA_OK;
     if (pre != FA_OK) return pre;
-    n_split = default_splits(B, H, Nq, Nk);
+    n_split = default_splits(B, H, Nq, Nk, d);
   }
   const int vs = validate_splitkv(B, H, Nq, Nk, d, n_split, causal, scale);
   if (vs < 0) return FA_OK;

@@ -68,6 +68,12 @@ struct SplitKvArgs {
 };
 int splitkv_kbps(int Nk, int n_split);
 cudaError_t launch_fwd_splitkv_partial(const SplitKvArgs& a, cudaStream_t stream);
+// The same partials for one query row on the CUDA cores (fa_splitkv.cu), taken
+// where it streams K and V faster than the tensor-core kernel: Nq = 1 at d = 64.
+inline bool decode_takes(int Nq, int d) { return Nq == 1 && d == 64; }
+cudaError_t launch_decode_partial(const SplitKvArgs& a, cudaStream_t stream);
+// CTAs of the one-row kernel (one per split and head) resident on one SM at head dim d.
+int decode_ctas_per_sm(int d);
 
 // Exact merge of split-KV partials into bf16 O [B*H, Nq, d] and fp32 LSE
 // [B*H, Nq] (fa_splitkv.cu).

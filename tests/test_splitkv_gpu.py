@@ -54,6 +54,13 @@ CASES = [
     (1, 1, 129, 900, 64, 2, False),
     (1, 2, 5, 300, 128, 40, False),   # 3 key blocks: 37 trailing splits are empty
     (1, 1, 600, 600, 128, 1, False),  # several 256-row query units, one split
+    # One query row: at d = 64 the CUDA-core partials (32-key chunks over four warps).
+    (2, 3, 1, 777, 64, 4, False),     # a ragged last chunk
+    (1, 2, 1, 300, 64, 40, True),     # 37 trailing splits empty
+    (1, 1, 1, 33, 64, 1, False),      # one full chunk and one key
+    (1, 1, 1, 5, 64, 1, False),       # fewer keys than lanes, three warps idle
+    (3, 2, 1, 4500, 64, 2, True),     # many chunks per warp
+    (1, 2, 1, 300, 128, 40, True),    # d = 128: the tensor-core kernel with one row
 ]
 
 
