@@ -78,6 +78,7 @@ enum : uint32_t {
   kSiteSoftS = 0x301,
   kSiteSoftO = 0x302,
   kSiteEpi = 0x303,
+  kSiteSoftKV = 0x304,
 };
 
 // FP8 selects the e4m3 variant: Q, K and V tiles of e4m3 codes (V transposed,
@@ -105,6 +106,14 @@ struct FwdCfg {
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  // Who waits for the K/V ring inside a whole unit.  The single MMA-issuing thread
+  // paces the tensor pipe: each instruction it runs between two MMA bursts leaves
+  // the pipe idle, while the softmax warpgroups wait for S more than half the time.
+  // For bf16 at d = 128 the softmax warpgroups therefore check that V_j and K_{j+1}
+  // have landed before signalling P, and the MMA thread waits on P alone.  With
+  // FP8 or d = 64 the MMA bursts are shorter and the softmax chain is the longer
+  // one, so there the MMA thread keeps those waits (measured both ways).
+  static constexpr bool kRingWaitsInSoftmax = !FP8 && D == 128;
   static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * static_cast<uint32_t>(t); }
   static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + D * static_cast<uint32_t>(t); }
 };
@@ -343,16 +352,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&bar_empty[slot]);
           ++item;
         }
+        // With kRingWaitsInSoftmax, V_j and K_{j+1} are not waited for here: a
+        // softmax warpgroup signals P_t only once both have landed, so the wait on
+        // P_t covers them and this thread does one wait per tile and block.
         for (int j = 0; ok && j < n_max; ++j) {
           const int slot_v = item % C::kSlots;
-          ok = mbar_wait(&bar_full[slot_v], (item / C::kSlots) & 1, wc, kSiteMmaV);
+          if constexpr (!C::kRingWaitsInSoftmax) {
+            ok = mbar_wait(&bar_full[slot_v], (item / C::kSlots) & 1, wc, kSiteMmaV);
+            if (!ok) break;
+          }
           ++item;
-          if (!ok) break;
           const bool has_next = j + 1 < n_max;
           const int slot_k = item % C::kSlots;
           const uint32_t par_k = (item / C::kSlots) & 1;
           if (has_next) ++item;
-          bool k_ready = false;
+          bool k_ready = C::kRingWaitsInSoftmax;
           for (int t = 0; ok && t < kTiles; ++t) {
             if (j >= nq[t]) continue;
             ok = mbar_wait(&bar_p[t], np[t] & 1, wc, kSiteMmaP);
@@ -441,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t scnt = 0;             // S blocks consumed so far (bar_s phase)
     uint32_t oc0 = 0, oc1 = 0;     // items in which slot 0 / slot 1 had keys (bar_o, bar_epi phases)
     uint32_t nepi = 0;             // epilogues before this item's (bar_stg phase)
+    int ring0 = 0;                 // K/V ring items of the whole units before this one
     bool ok = true;
     // What the merge epilogue of a shared tile needs once the item loop is left.
     struct {
@@ -458,6 +473,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool has0 = slot_work<CAUSAL>(itm, 0, N, ks).count > 0;
       const bool has1 = slot_work<CAUSAL>(itm, 1, N, ks).count > 0;
       const int nkt = sw.count;
+      // A whole unit takes 2 n_max ring items: K_0, then V_j and K_{j+1} per block j.
+      int n_max = 0, ring_unit = 0;
+      if constexpr (C::kRingWaitsInSoftmax) {
+        n_max = shared ? 0 : max(slot_work<CAUSAL>(itm, 0, N, ks).count, slot_work<CAUSAL>(itm, 1, N, ks).count);
+        ring_unit = ring0;
+        ring0 += 2 * n_max;
+      }
       const uint32_t ph0 = oc0, ph1 = oc1;          // this item's phases of slot 0 and slot 1
       const uint32_t ph_t = t == 0 ? ph0 : ph1;     // own slot
       oc0 += has0 ? 1u : 0u;
@@ -722,7 +744,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_p[t]);
+        if (lane == 0) {
+          // With kRingWaitsInSoftmax, P_t of a whole unit signals more than P: V_j
+          // (ring item ring_unit + 1 + 2j), and K_{j+1} after it when there is one,
+          // have landed, so the MMA thread waits on P_t alone before P_t V_j and
+          // S_t = Q_t K_{j+1}^T.
+          bool landed = true;
+          if (C::kRingWaitsInSoftmax && !shared) {
+            const int iv = ring_unit + 1 + 2 * j;
+            landed = mbar_wait(&bar_full[iv % C::kSlots], (iv / C::kSlots) & 1, wc, kSiteSoftKV);
+            if (landed && j + 1 < n_max)
+              landed = mbar_wait(&bar_full[(iv + 1) % C::kSlots], ((iv + 1) / C::kSlots) & 1, wc, kSiteSoftKV);
+          }
+          if (landed) mbar_arrive(&bar_p[t]);
+        }
+        if (C::kRingWaitsInSoftmax && !__shfl_sync(0xffffffffu, static_cast<int>(*abort_flag == 0), 0)) {
+          ok = false;  // lane 0 gave up on the ring (the CTA is aborting)
+          break;
+        }
       }
       if (!ok) break;
 
