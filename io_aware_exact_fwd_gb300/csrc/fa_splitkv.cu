@@ -92,37 +92,45 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
 // tile of MMAs and exponentials per key block on one useful row; here the work is
 // the K/V stream itself: 2d fp32 FMAs per key against 4d bytes read.
 //
-// One CTA of 4 warps per (head, split); warp w takes the split's chunks of KC keys
-// (32 at d = 64, 16 at d = 128, so that a chunk's rows fit in registers) w, w + 4,
-// ...  Lane l holds the d/32 consecutive columns c = l d/32 .. of every row, so
-// each row of K or V is one coalesced warp load; all of a chunk's loads are issued
-// before its arithmetic.  Per chunk:
-//  * partial dots: lane l forms q[c] k_j[c] summed over its columns for every key j;
-//  * a butterfly of shuffles (widths KC/2, ..., 2, 1; at each step a lane keeps the
-//    half of its values whose key index has its bit of the width and adds the
-//    partner's copy of that half; for KC = 16 one more exchange adds the two
-//    half-warps) leaves the full q . k_j in lane j (and j + 16);
+// One CTA of 4 warps per (head, split).  A row of K or V is read by L = d/8 lanes,
+// 16 bytes (8 columns) each, so one warp load instruction covers R = 32/L rows
+// (4 at d = 64, 2 at d = 128): lane l takes columns 8 (l mod L) .. +7 of row
+// group g = l / L.  A chunk is 8 such loads per tensor, KC = 8 R keys (32 or 16);
+// warp w takes the split's chunks w, w + 4, ...  Chunk row rho = 8-slot index i
+// times R plus g.  All of a chunk's loads are issued before its arithmetic and
+// none sits behind a branch (rows past the split re-read its last row; their
+// scores are masked to -inf).  Per chunk:
+//  * partial dots: for each of its 8 rows, q . k over the lane's 8 columns;
+//  * a butterfly over the 8 lanes of an aligned group (widths 4, 2, 1: a lane keeps
+//    the half of its values whose slot index has its bit of the width and adds the
+//    partner's copy of that half; at d = 128 one more exchange adds the two 8-lane
+//    halves of a row) leaves the score of slot i = l mod 8 in lane l;
 //  * online softmax in base 2 (the scale and log2 e are folded into q): chunk
-//    maximum, the running reference, p_j = 2^(s_j - m), O and the lane's row sum
-//    rescaled by 2^(m_old - m);
-//  * O[c] += p_j v_j[c] for the 32 keys, p_j broadcast from lane j.
-// The four warps' (m, l, O) are merged through shared memory exactly as the split
-// merge does; the partial is O / l in fp32 and LSE = ln 2 (m + log2 l), -inf for an
-// empty split.  All arithmetic is fp32 (the inputs bf16).  Only d = 64 is built:
-// at d = 128 this kernel streamed 0.90 of HBM bandwidth against the tensor-core
-// kernel's 0.92, which therefore keeps that case.
-template <int D, int KC>  // KC keys per chunk: 32 at d = 64, 16 at d = 128 (registers for the chunk's rows)
+//    maximum, the running reference, p = 2^(s - m), O and the row sum rescaled by
+//    2^(m_old - m);
+//  * O[c] += p_i v_i[c] over the lane's 8 rows, p_i taken from lane g L + i.
+// At the end the R row groups' O are summed with shuffles, and the four warps'
+// (m, l, O) are merged through shared memory exactly as the split merge does; the
+// partial is O / l in fp32 and LSE = ln 2 (m + log2 l), -inf for an empty split.
+// All arithmetic is fp32 (the inputs bf16).  Only d = 64 is built: at d = 128 this
+// kernel streamed 0.93 of HBM bandwidth at B = 8, H = 16, Nk = 32768 but 0.79 at
+// B = 1, H = 16, Nk = 131072, against 0.92 and 0.85 for the tensor-core kernel,
+// which keeps that case.
+template <int D>
 __global__ void __launch_bounds__(128) decode_partial_kernel(const __nv_bfloat16* __restrict__ q,
                                                              const __nv_bfloat16* __restrict__ k,
                                                              const __nv_bfloat16* __restrict__ v, Strides sq,
                                                              Strides sk, Strides sv, float* __restrict__ o_part,
                                                              float* __restrict__ lse_part, int H, int BH, int Nk,
                                                              int n_split, int kbps, float scale_log2) {
-  constexpr int E = D / 32;  // columns per lane: 4 (d = 128) or 2 (d = 64)
+  constexpr int L = D / 8;    // lanes per row
+  constexpr int R = 32 / L;   // rows per warp load
+  constexpr int KC = 8 * R;   // keys per chunk
   constexpr int kWarps = 4;
   __shared__ float s_m[kWarps], s_l[kWarps];
-  __shared__ float s_o[kWarps][D];
+  __shared__ __align__(16) float s_o[kWarps][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane / L, cg = lane % L;  // row group, column group (columns 8 cg .. 8 cg + 7)
   const int bh = blockIdx.x / n_split, sp = blockIdx.x % n_split;
   const int b = bh / H, h = bh % H;
   const int k0 = min(sp * kbps * 128, Nk), k1 = min((sp + 1) * kbps * 128, Nk);
@@ -131,53 +139,48 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(const __nv_bfloat16
     if (threadIdx.x == 0) lse_part[rows] = -INFINITY;
     return;
   }
-  const __nv_bfloat16* qh = q + b * sq.s[2] + h * sq.s[1] + E * lane;
-  const __nv_bfloat16* kh = k + b * sk.s[2] + h * sk.s[1] + E * lane;
-  const __nv_bfloat16* vh = v + b * sv.s[2] + h * sv.s[1] + E * lane;
-  float qf[E];
+  const __nv_bfloat16* kh = k + b * sk.s[2] + h * sk.s[1] + 8 * cg;
+  const __nv_bfloat16* vh = v + b * sv.s[2] + h * sv.s[1] + 8 * cg;
+  float qf[8];
+  {
+    const uint4 qv = *reinterpret_cast<const uint4*>(q + b * sq.s[2] + h * sq.s[1] + 8 * cg);
+    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-  for (int e = 0; e < E; ++e) qf[e] = __bfloat162float(qh[e]) * scale_log2;
-  float m = -INFINITY, lsum = 0.f, o[E];
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw[e]));
+      qf[2 * e] = f.x * scale_log2;
+      qf[2 * e + 1] = f.y * scale_log2;
+    }
+  }
+  float m = -INFINITY, lsum = 0.f, o[8];
 #pragma unroll
-  for (int e = 0; e < E; ++e) o[e] = 0.f;
+  for (int e = 0; e < 8; ++e) o[e] = 0.f;
+  const bool counts = L == 8 || (lane & 8) == 0;  // d = 128: lanes l and l ^ 8 hold the same row
 
   for (int c0 = k0 + KC * warp; c0 < k1; c0 += KC * kWarps) {
-    const int nkeys = min(KC, k1 - c0);
-    // The chunk's K and V rows, every load issued before any arithmetic and none
-    // behind a branch (a ragged last chunk re-reads its last row; those scores are
-    // masked to -inf below, so their P is 0).
-    uint32_t kr[KC][E / 2], vr[KC][E / 2];
+    const int last = k1 - 1 - c0;  // chunk rows past this are re-reads of the split's last row
+    uint4 kr[8], vr[8];
 #pragma unroll
-    for (int j = 0; j < KC; ++j) {
-      const int jr = c0 + (j < nkeys ? j : nkeys - 1);
-      const __nv_bfloat16* kp = kh + static_cast<size_t>(jr) * sk.s[0];
-      const __nv_bfloat16* vp = vh + static_cast<size_t>(jr) * sv.s[0];
-      if constexpr (E == 4) {
-        const uint2 a = __ldg(reinterpret_cast<const uint2*>(kp)), c = __ldg(reinterpret_cast<const uint2*>(vp));
-        kr[j][0] = a.x;
-        kr[j][1] = a.y;
-        vr[j][0] = c.x;
-        vr[j][1] = c.y;
-      } else {
-        kr[j][0] = __ldg(reinterpret_cast<const uint32_t*>(kp));
-        vr[j][0] = __ldg(reinterpret_cast<const uint32_t*>(vp));
-      }
+    for (int i = 0; i < 8; ++i) {
+      const int rho = min(i * R + grp, last);
+      kr[i] = __ldg(reinterpret_cast<const uint4*>(kh + static_cast<size_t>(c0 + rho) * sk.s[0]));
+      vr[i] = __ldg(reinterpret_cast<const uint4*>(vh + static_cast<size_t>(c0 + rho) * sv.s[0]));
     }
-    // Partial dots of the lane's columns, then the butterfly: lane j ends with q . k_j.
-    float t[KC];
+    float t[8];
 #pragma unroll
-    for (int j = 0; j < KC; ++j) {
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t kw[4] = {kr[i].x, kr[i].y, kr[i].z, kr[i].w};
       float acc = 0.f;
 #pragma unroll
-      for (int e = 0; e < E / 2; ++e) {
-        const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kr[j][e]));
+      for (int e = 0; e < 4; ++e) {
+        const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw[e]));
         acc = fmaf(qf[2 * e], kf.x, acc);
         acc = fmaf(qf[2 * e + 1], kf.y, acc);
       }
-      t[j] = acc;
+      t[i] = acc;
     }
 #pragma unroll
-    for (int w = KC / 2; w >= 1; w >>= 1) {
+    for (int w = 4; w >= 1; w >>= 1) {
       const bool upper = (lane & w) != 0;
 #pragma unroll
       for (int i = 0; i < w; ++i) {
@@ -186,59 +189,68 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(const __nv_bfloat16
         t[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
       }
     }
-    // 16-key chunks: lanes l and l + 16 hold the two half-warps' sums of key l % 16.
-    if (KC == 16) t[0] += __shfl_xor_sync(0xffffffffu, t[0], 16);
-    const int kj = lane % KC;
-    const float sj = kj < nkeys ? t[0] : -INFINITY;  // score of key c0 + lane % KC (base 2)
+    if (L == 16) t[0] += __shfl_xor_sync(0xffffffffu, t[0], 8);
+    const int my_rho = (lane & 7) * R + grp;  // the chunk row whose score this lane now holds
+    const float sj = my_rho <= last ? t[0] : -INFINITY;
     float cm = sj;
 #pragma unroll
     for (int w = 16; w >= 1; w >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, w));
     const float m_new = fmaxf(m, cm);  // finite: the chunk has at least one key
     const float alpha = ex2_approx(m - m_new);  // 0 on the first chunk (m = -inf)
     const float p = ex2_approx(sj - m_new);
-    lsum = lsum * alpha + (lane < KC ? p : 0.f);  // 16-key chunks: each key once
+    lsum = lsum * alpha + (counts ? p : 0.f);
 #pragma unroll
-    for (int e = 0; e < E; ++e) o[e] *= alpha;
+    for (int e = 0; e < 8; ++e) o[e] *= alpha;
 #pragma unroll
-    for (int j = 0; j < KC; ++j) {
-      const float pj = __shfl_sync(0xffffffffu, p, j);
+    for (int i = 0; i < 8; ++i) {
+      const float pi = __shfl_sync(0xffffffffu, p, grp * L + i);  // p of chunk row i R + grp
+      const uint32_t vw[4] = {vr[i].x, vr[i].y, vr[i].z, vr[i].w};
 #pragma unroll
-      for (int e = 0; e < E / 2; ++e) {
-        const float2 vf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vr[j][e]));
-        o[2 * e] = fmaf(pj, vf.x, o[2 * e]);
-        o[2 * e + 1] = fmaf(pj, vf.y, o[2 * e + 1]);
+      for (int e = 0; e < 4; ++e) {
+        const float2 vf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vw[e]));
+        o[2 * e] = fmaf(pi, vf.x, o[2 * e]);
+        o[2 * e + 1] = fmaf(pi, vf.y, o[2 * e + 1]);
       }
     }
     m = m_new;
   }
+  // Sum the R row groups' O (lanes with the same column group), then the row sums.
+#pragma unroll
+  for (int w = L; w < 32; w <<= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] += __shfl_xor_sync(0xffffffffu, o[e], w);
 #pragma unroll
   for (int w = 16; w >= 1; w >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, w);
   if (lane == 0) {
     s_m[warp] = m;
     s_l[warp] = lsum;
   }
-#pragma unroll
-  for (int e = 0; e < E; ++e) s_o[warp][E * lane + e] = o[e];
+  if (grp == 0) {
+    float4* dst = reinterpret_cast<float4*>(&s_o[warp][8 * cg]);
+    dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+  }
   __syncthreads();
   if (warp == 0) {
+    constexpr int E = D / 32;  // output columns per lane
     float M = s_m[0];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) M = fmaxf(M, s_m[w]);
-    float L = 0.f, acc[E];
+    float Lw = 0.f, acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
       const float a = s_m[w] == -INFINITY ? 0.f : ex2_approx(s_m[w] - M);  // a warp with no chunk weighs 0
-      L += s_l[w] * a;
+      Lw += s_l[w] * a;
 #pragma unroll
       for (int e = 0; e < E; ++e) acc[e] += s_o[w][E * lane + e] * a;
     }
-    const float inv = 1.f / L;
+    const float inv = 1.f / Lw;
     float* dst = o_part + rows * D + E * lane;
 #pragma unroll
     for (int e = 0; e < E; ++e) dst[e] = acc[e] * inv;
-    if (lane == 0) lse_part[rows] = (M + log2f(L)) * 0.69314718055994530942f;
+    if (lane == 0) lse_part[rows] = (M + log2f(Lw)) * 0.69314718055994530942f;
   }
 }
 
@@ -246,7 +258,7 @@ __global__ void __launch_bounds__(128) decode_partial_kernel(const __nv_bfloat16
 
 int decode_ctas_per_sm(int d) {
   int n = 0;
-  if (d != 64 || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partial_kernel<64, 32>, 128, 0) != cudaSuccess ||
+  if (d != 64 || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_partial_kernel<64>, 128, 0) != cudaSuccess ||
       n < 1)
     n = 4;
   return n;
@@ -258,7 +270,7 @@ cudaError_t launch_decode_partial(const SplitKvArgs& a, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>(BH) * static_cast<unsigned>(a.n_split);
   const float scale_log2 = a.scale * 1.4426950408889634f;
   const int kbps = splitkv_kbps(a.Nk, a.n_split);
-  decode_partial_kernel<64, 32><<<grid, 128, 0, stream>>>(
+  decode_partial_kernel<64><<<grid, 128, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
       static_cast<const __nv_bfloat16*>(a.v), a.sq, a.sk, a.sv, a.o_part, a.lse_part, a.H, BH, a.Nk, a.n_split, kbps,
       scale_log2);
