@@ -112,7 +112,9 @@ struct FwdCfg {
   // For bf16 at d = 128 the softmax warpgroups therefore check that V_j and K_{j+1}
   // have landed before signalling P, and the MMA thread waits on P alone.  With
   // FP8 or d = 64 the MMA bursts are shorter and the softmax chain is the longer
-  // one, so there the MMA thread keeps those waits (measured both ways).
+  // one, so there the MMA thread keeps those waits (measured both ways); so does
+  // the split-KV build (see fwd_kernel), whose decode-shaped launches are bound by
+  // HBM: there P_t V_j must not wait for K_{j+1} to land.
   static constexpr bool kRingWaitsInSoftmax = !FP8 && D == 128;
   static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * static_cast<uint32_t>(t); }
   static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + D * static_cast<uint32_t>(t); }
@@ -135,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(!(SPLIT && FP8), "the split-KV variant is bf16 only");
   static_assert(!(TAIL && (CAUSAL || SPLIT)), "shared tiles only for the non-causal, whole-key forward");
   using C = FwdCfg<D, FP8>;
+  constexpr bool kRingWaitsInSoftmax = C::kRingWaitsInSoftmax && !SPLIT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::kQOff;
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P_t covers them and this thread does one wait per tile and block.
         for (int j = 0; ok && j < n_max; ++j) {
           const int slot_v = item % C::kSlots;
-          if constexpr (!C::kRingWaitsInSoftmax) {
+          if constexpr (!kRingWaitsInSoftmax) {
             ok = mbar_wait(&bar_full[slot_v], (item / C::kSlots) & 1, wc, kSiteMmaV);
             if (!ok) break;
           }
@@ -366,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot_k = item % C::kSlots;
           const uint32_t par_k = (item / C::kSlots) & 1;
           if (has_next) ++item;
-          bool k_ready = C::kRingWaitsInSoftmax;
+          bool k_ready = kRingWaitsInSoftmax;
           for (int t = 0; ok && t < kTiles; ++t) {
             if (j >= nq[t]) continue;
             ok = mbar_wait(&bar_p[t], np[t] & 1, wc, kSiteMmaP);
@@ -475,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nkt = sw.count;
       // A whole unit takes 2 n_max ring items: K_0, then V_j and K_{j+1} per block j.
       int n_max = 0, ring_unit = 0;
-      if constexpr (C::kRingWaitsInSoftmax) {
+      if constexpr (kRingWaitsInSoftmax) {
         n_max = shared ? 0 : max(slot_work<CAUSAL>(itm, 0, N, ks).count, slot_work<CAUSAL>(itm, 1, N, ks).count);
         ring_unit = ring0;
         ring0 += 2 * n_max;
@@ -750,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // have landed, so the MMA thread waits on P_t alone before P_t V_j and
           // S_t = Q_t K_{j+1}^T.
           bool landed = true;
-          if (C::kRingWaitsInSoftmax && !shared) {
+          if (kRingWaitsInSoftmax && !shared) {
             const int iv = ring_unit + 1 + 2 * j;
             landed = mbar_wait(&bar_full[iv % C::kSlots], (iv / C::kSlots) & 1, wc, kSiteSoftKV);
             if (landed && j + 1 < n_max)
@@ -758,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (landed) mbar_arrive(&bar_p[t]);
         }
-        if (C::kRingWaitsInSoftmax && !__shfl_sync(0xffffffffu, static_cast<int>(*abort_flag == 0), 0)) {
+        if (kRingWaitsInSoftmax && !__shfl_sync(0xffffffffu, static_cast<int>(*abort_flag == 0), 0)) {
           ok = false;  // lane 0 gave up on the ring (the CTA is aborting)
           break;
         }
