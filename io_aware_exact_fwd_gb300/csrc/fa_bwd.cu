@@ -51,12 +51,13 @@ namespace {
 
 constexpr int kBkB = 128;       // keys per CTA
 constexpr int kBqB = 64;        // query rows per inner step
-constexpr int kThreads = 512;   // 0-7 compute, 8-11 dQ reduction, 12 TMA, 13-14 MMA issuers, 15 spare
+constexpr int kThreads = 512;   // 0-7 compute, 8-11 dQ reduction, 12 TMA, 13-15 MMA issuers (15: see kSplitSdp)
 constexpr int kWarpDq = 8;
 constexpr int kWarpCtl = 12;
 constexpr int kWarpLoad = 12;
 constexpr int kWarpMma = 13;     // issues dV, dK, dQ^T (and owns the TMEM allocation)
-constexpr int kWarpMmaS = 14;    // issues S^T, dP^T
+constexpr int kWarpMmaS = 14;    // issues S^T
+constexpr int kWarpMmaDP = 15;   // issues dP^T when the kernel splits that issue (kSplitSdp), else idle
 constexpr int kStages = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -202,6 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float* __restrict__ dq_bmax, const float* __restrict__ kv_max, int N, int Npad, int H,
                     int BH, int nkb, float scale, float scale_log2, unsigned int* err_word, unsigned long long wait_ns) {
   using C = BwdCfg<D>;
+  // Whether warps 14 and 15 split the S^T and dP^T issue (see the MMA issuers below).
+  // Measured faster with atomic dQ at d = 128 only: the deterministic dQ warps and
+  // the d = 64 kernel (where the chain is the elementwise work) do not gain from it.
+  constexpr bool kSplitSdp = D == 128 && !DET;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem + C::kKOff;
@@ -245,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
-    mbar_init(bar_sdp, 1);
+    mbar_init(bar_sdp, kSplitSdp ? 2 : 1);  // one commit per S^T / dP^T issuing thread
     mbar_init(bar_sde, 8);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_comp[b], 8);
@@ -254,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar_dkv, 1);
     mbar_init(bar_epi, 8);
-    mbar_init(bar_drain, 2);  // one commit per MMA-issuing thread
+    mbar_init(bar_drain, kSplitSdp ? 3 : 2);  // one commit per MMA-issuing thread
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -321,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kWarpMma || warp == kWarpMmaS) {
+  } else if (warp == kWarpMma || warp == kWarpMmaS || (kSplitSdp && warp == kWarpMmaDP)) {
     // ------------------------------------------------ MMA issuers (one thread each)
     // Two threads issue MMAs so that S^T/dP^T of a later query block never waits
     // behind dV/dK/dQ^T of an earlier one (or vice versa).  Each hazard between
@@ -346,31 +351,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t vaug = sdesc_sw32(smem_u32(smem + C::kVAugOff));
       const uint64_t ring_aug = sdesc_sw32(smem_u32(sRing + C::kStageAug));
       bool ok = mbar_wait(bar_kv, 0, wc, kSiteBMmaKV);
-      if (warp == kWarpMmaS) {
+      if (warp == kWarpMmaS || warp == kWarpMmaDP) {
         // S^T = K Q_i^T and dP^T = V dO_i^T for local step `it`, as soon as the
-        // compute warps have read the previous pair out of TMEM.
+        // compute warps have read the previous pair out of TMEM.  With
+        // kSplitSdp warp 14 issues S^T and warp 15 dP^T: one thread's chain of
+        // N = 64 MMAs runs at about half the tensor rate, two overlap, and this
+        // pair is the backward's critical path (issue, completion, the compute
+        // warps' TMEM loads, bar_sde).  Otherwise warp 14 issues both.
+        const bool issue_s = warp == kWarpMmaS;
+        const bool issue_dp = kSplitSdp ? warp == kWarpMmaDP : warp == kWarpMmaS;
         for (int it = 0; ok && it < n; ++it) {
           const int slot = it % kStages;
           if (!(ok = mbar_wait(&bar_full[slot], (it / kStages) & 1, wc, kSiteBMmaQ))) break;
           if (it >= 1 && !(ok = mbar_wait(bar_sde, (it - 1) & 1, wc, kSiteBMmaSd))) break;
           tc_fence_after();
           const uint32_t st = slot * C::kStageBytes;
+          if (issue_s) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
-            const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
-            mma_bf16_ss(tmem + C::kColS, sdesc_add(k_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageQ + offb),
-                        idesc_sdp, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
+              const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
+              mma_bf16_ss(tmem + C::kColS, sdesc_add(k_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageQ + offb),
+                          idesc_sdp, kk > 0 ? 1u : 0u);
+            }
+            mma_bf16_ss(tmem + C::kColS, kaug, sdesc_add(ring_aug, st), idesc_sdp, 1u);  // - LSE2 / (scale log2 e)
           }
-          mma_bf16_ss(tmem + C::kColS, kaug, sdesc_add(ring_aug, st), idesc_sdp, 1u);  // - LSE2 / (scale log2 e)
+          if (issue_dp) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
-            const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
-            mma_bf16_ss(tmem + C::kColDP, sdesc_add(v_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageDO + offb),
-                        idesc_sdp, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t offa = (kk / 4) * C::kKVBox + (kk % 4) * 32;
+              const uint32_t offb = (kk / 4) * C::kQBox + (kk % 4) * 32;
+              mma_bf16_ss(tmem + C::kColDP, sdesc_add(v_kmaj, offa), sdesc_add(ring_kmaj, st + C::kStageDO + offb),
+                          idesc_sdp, kk > 0 ? 1u : 0u);
+            }
+            mma_bf16_ss(tmem + C::kColDP, vaug, sdesc_add(ring_aug, st + C::kAugTile), idesc_sdp, 1u);  // - D
           }
-          mma_bf16_ss(tmem + C::kColDP, vaug, sdesc_add(ring_aug, st + C::kAugTile), idesc_sdp, 1u);  // - D
           mma_commit(bar_sdp);
         }
       } else {
