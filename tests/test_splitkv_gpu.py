@@ -161,10 +161,12 @@ def test_default_split_count(causal):
     assert max_abs(lse, lse_ref) <= FWD_LSE_ATOL
 
 
-def test_decode_workload_sampled_heads():
-    # The decode workload at full size (B=8, H=16, one query, Nk=32768, d=128) in the
-    # launch configuration the benchmark uses; heads sampled for the oracle.
-    B, H, Nq, Nk, d = 8, 16, 1, 32768, 128
+@pytest.mark.parametrize("H, d", [(16, 128), (32, 64)])
+def test_decode_workload_sampled_heads(H, d):
+    # The decode workloads at full size (B=8, one query, Nk=32768; H=16 at d=128 on the
+    # tensor cores, H=32 at d=64 on the CUDA cores) in the launch configuration the
+    # benchmark uses; heads sampled for the oracle.
+    B, Nq, Nk = 8, 1, 32768
     q, k, v = _inputs(B, H, Nq, Nk, d, 2024)
     o, lse = fa.fa_fwd_splitkv(q, k, v)
     fa.fa_sync_check()

@@ -142,8 +142,9 @@ def test_fp8_prepare_strided_equals_dense(layout, dtype, d):
 @pytest.mark.parametrize("layout", ["bnhd", "padded"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("d", [64, 128])
-def test_splitkv_strided_equals_dense(layout, causal, d):
-    B, H, Nq, Nk = 2, 3, 5, 1500
+@pytest.mark.parametrize("Nq", [5, 1])  # one query row at d = 64: the CUDA-core partials
+def test_splitkv_strided_equals_dense(layout, causal, d, Nq):
+    B, H, Nk = 2, 3, 1500
     kv = normal_qkv(B, H, Nk, d, 50)
     k, v = (kv[n].to(torch.bfloat16).cuda() for n in ("k", "v"))
     q = normal_qkv(B, H, Nq, d, 51)["q"].to(torch.bfloat16).cuda()
