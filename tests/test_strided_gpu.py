@@ -154,7 +154,10 @@ def test_splitkv_strided_equals_dense(layout, causal, d, Nq):
     o, lse = fa.fa_fwd_splitkv(q, k, v, n_split=4, causal=causal)
     o2, lse2 = fa.fa_fwd_splitkv(qv, kvv, vv, o=o_view, n_split=4, causal=causal)
     fa.fa_sync_check()
-    assert not o_view.is_contiguous()
+    # K and V are strided views in both layouts; with one query row a [B, 1, H, d]
+    # view of q or o is contiguous as far as torch is concerned.
+    assert not kvv.is_contiguous() and not vv.is_contiguous()
+    assert Nq == 1 or not o_view.is_contiguous()
     assert torch.equal(o, o2.contiguous())
     assert torch.equal(lse, lse2)
     # Sanity against the oracle on one head (queries are the last Nq positions).
