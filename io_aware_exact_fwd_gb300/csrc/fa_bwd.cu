@@ -22,7 +22,8 @@
 //     more K-step of 16 columns whose product is -LSE_i * log2(e) / (scale log2 e)
 //     (resp. -D_i) in every key row, so the accumulators hold scale^-1 log2 P
 //     and dP - D directly and the compute warps read no per-query value from
-//     shared memory.  Per query block, tcgen05 MMAs compute
+//     shared memory.  Per query block, tcgen05 MMAs (issued by two or three
+//     single threads, see kSplitSdp) compute
 //     S^T = K Q_i^T and dP^T = V dO_i^T into TMEM (keys on TMEM lanes, so a
 //     thread owns one key row; two warpgroups split the 64 query columns),
 //     eight warps form P^T and dS^T in registers and write them back to TMEM
@@ -416,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) mma_commit(bar_dkv);
       }
-      // Every issued MMA of both threads must finish before TMEM is released.
+      // Every issued MMA of every issuing thread must finish before TMEM is released.
       mma_commit(bar_drain);
       mbar_wait_drain(bar_drain, 0, wait_ns);
     }

@@ -1047,8 +1047,8 @@ int splitkv_kbps(int Nk, int n_split) {
 }
 
 cudaError_t launch_fwd_splitkv_partial(const SplitKvArgs& a, cudaStream_t stream) {
-  // One query row (causal or not: the last position sees every key): a stream over
-  // K and V, taken on the CUDA cores (fa_splitkv.cu).
+  // One query row (causal or not: the last position sees every key) is a stream over
+  // K and V; at d = 64 the CUDA-core kernel in fa_splitkv.cu takes it (decode_takes).
   if (decode_takes(a.Nq, a.d)) return launch_decode_partial(a, stream);
   if (a.d == 64) return a.causal ? launch_splitkv_impl<64, true>(a, stream) : launch_splitkv_impl<64, false>(a, stream);
   return a.causal ? launch_splitkv_impl<128, true>(a, stream) : launch_splitkv_impl<128, false>(a, stream);
