@@ -55,6 +55,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, with a suspend-time hint: a thread whose phase has not completed
+// may stay suspended (issuing nothing) for up to hint_ns nanoseconds, and resumes
+// when the phase completes.  For warps that wait long and share their SM
+// sub-partition with a latency-critical warp.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared state every bounded wait of a CTA consults.
 struct WaitCtl {
   volatile int* abort_flag;   // shared memory; nonzero once any thread of the CTA gave up
@@ -77,6 +93,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
+    if (*w.abort_flag) return false;
+    if (globaltimer_ns() - t0 > w.limit_ns) {
+      record_timeout(w, site);
+      return false;
+    }
+  }
+}
+
+// mbar_wait whose polls suspend the thread (see mbar_try_wait_suspend) instead of
+// spinning; the deadline and the abort flag are checked between polls.
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity, const WaitCtl& w, uint32_t site,
+                                                  uint32_t hint_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_suspend(bar, parity, hint_ns)) return true;
     if (*w.abort_flag) return false;
     if (globaltimer_ns() - t0 > w.limit_ns) {
       record_timeout(w, site);

@@ -124,6 +124,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   const bool ok = mbar_wait(bar, parity, wc, site);
   return __all_sync(0xffffffffu, ok);
 }
+// The softmax warpgroups' wait for S: they wait more than half of each block, on
+// the same SM sub-partitions as the MMA-issuing warp, so their polls suspend.
+__device__ __forceinline__ bool warp_wait_suspend(uint64_t* bar, uint32_t parity, const WaitCtl& wc, uint32_t site) {
+  const bool ok = mbar_wait_suspend(bar, parity, wc, site, 20000u);
+  return __all_sync(0xffffffffu, ok);
+}
 
 // TAIL: the build for launches whose last pass is dealt out as shared tiles
 // (item_at); only the non-causal, whole-key forward has one.  Every other launch
@@ -536,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fetch_scales(0);
 
       for (int j = 0; j < nkt; ++j, ++scnt) {
-        if (!warp_wait(&bar_s[t], scnt & 1, wc, kSiteSoftS)) {
+        if (!warp_wait_suspend(&bar_s[t], scnt & 1, wc, kSiteSoftS)) {
           ok = false;
           break;
         }
