@@ -131,6 +131,12 @@ __device__ __forceinline__ bool warp_wait_b(uint64_t* bar, uint32_t parity, cons
   const bool ok = mbar_wait(bar, parity, wc, site);
   return __all_sync(0xffffffffu, ok);
 }
+// For the compute and dQ warps' long waits (S^T, dP^T ready; dQ^T ready): their polls
+// suspend instead of spinning beside the MMA-issuing warps.
+__device__ __forceinline__ bool warp_wait_b_suspend(uint64_t* bar, uint32_t parity, const WaitCtl& wc, uint32_t site) {
+  const bool ok = mbar_wait_suspend(bar, parity, wc, site, 20000u);
+  return __all_sync(0xffffffffu, ok);
+}
 
 // Deterministic dQ: fixed-point accumulation.  Every contribution of a key block
 // to dQacc[i, c] is sum_j dS_ij k_jc, and the whole sum over all key blocks obeys
@@ -439,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; it < n; ++it) {
       const int b = it & 1;
       const int i = i0 + it;
-      if (!(ok = warp_wait_b(bar_sdp, it & 1, wc, kSiteBComp))) break;
+      if (!(ok = warp_wait_b_suspend(bar_sdp, it & 1, wc, kSiteBComp))) break;
       tc_fence_after();
       uint32_t s[32], dp[32];
       tmem_ld32(trow + C::kColS + 32 * g, s);
@@ -508,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     for (int it = 0; it < n; ++it) {
       const int b = it & 1;
-      if (!warp_wait_b(&bar_dqf[b], (it >> 1) & 1, wc, kSiteBDq)) break;
+      if (!warp_wait_b_suspend(&bar_dqf[b], (it >> 1) & 1, wc, kSiteBDq)) break;
       if (D == 64 && dcol >= D) {  // the zero-padded rows of dQ^T: nothing to read or add
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_dqe[b]);
