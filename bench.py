@@ -447,7 +447,57 @@ def run_ours(args):
     return line
 
 
+def gpu_local_cpus(cuda_index):
+    """The host CPUs NVML names as closest to this GPU (nvmlDeviceGetCpuAffinity), or None.
+
+    Pinned host buffers are placed on the NUMA node of the thread that first touches
+    them; allocated from one of these CPUs they sit next to the GPU's host link.
+    """
+    import ctypes
+
+    try:
+        import torch
+
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            return None
+        try:
+            props = torch.cuda.get_device_properties(cuda_index)
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+            dev = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(dev)) != 0:
+                return None
+            words = 64
+            mask = (ctypes.c_ulong * words)()
+            if nv.nvmlDeviceGetCpuAffinity(dev, ctypes.c_uint(words), mask) != 0:
+                return None
+            bits = ctypes.sizeof(ctypes.c_ulong) * 8
+            cpus = {w * bits + b for w in range(words) for b in range(bits) if (mask[w] >> b) & 1}
+            return cpus or None
+        finally:
+            nv.nvmlShutdown()
+    except Exception:
+        return None
+
+
 def run_e2e(fa, args, q, k, v, g, lse, ws, causal, scale, flops_step, world):
+    import torch
+
+    # Allocate and drive the pinned host buffers from CPUs next to the GPU (restored after).
+    saved_affinity = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    local = gpu_local_cpus(torch.cuda.current_device())
+    host_cpus = None
+    if saved_affinity and local and (local & saved_affinity):
+        host_cpus = sorted(local & saved_affinity)
+        os.sched_setaffinity(0, host_cpus)
+    try:
+        return _run_e2e(fa, args, q, k, v, g, lse, ws, causal, scale, flops_step, world, host_cpus)
+    finally:
+        if host_cpus is not None:
+            os.sched_setaffinity(0, saved_affinity)
+
+
+def _run_e2e(fa, args, q, k, v, g, lse, ws, causal, scale, flops_step, world, host_cpus):
     import torch
 
     hq, hk, hv, hg = (t.cpu().pin_memory() for t in (q, k, v, g))
@@ -503,7 +553,9 @@ def run_e2e(fa, args, q, k, v, g, lse, ws, causal, scale, flops_step, world):
             "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "calls": "fa_fwd + fa_bwd per step; H2D of q, k, v, dO and D2H of o, lse, dq, dk, dv inside the "
-                     "timed region, overlapped with the neighbouring steps' kernels"}
+                     "timed region, overlapped with the neighbouring steps' kernels",
+            "host_cpus": (f"{len(host_cpus)} CPUs local to the GPU (NVML affinity)" if host_cpus
+                          else "process affinity unchanged")}
 
 
 # Rows past the headline, timed after it (not part of `value`): the causal step
