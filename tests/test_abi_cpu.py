@@ -120,6 +120,35 @@ def test_splitkv_validation_statuses(lib):
     assert lib.fa_splitkv_workspace_size(1, 1, 1, 96, 1) == 0
 
 
+def test_splitkv_default_split_rule(lib):
+    # fa_splitkv_default_splits (include/fa.h): the fewest splits n in 1 .. min(64, max(1,
+    # nkb / 4)) whose busiest-slot load ceil(units n / slots) / n is within 2 % of the
+    # best; 1 when Nq > 128 and the units already cover the SMs; slots = SMs, times the
+    # one-row kernel's resident CTAs for Nq == 1 at d == 64.  Without a GPU the library
+    # assumes 148 SMs and 4 resident CTAs.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("checked on the device by the GPU tests")
+    sms = 148
+
+    def expected(B, H, Nq, Nk, d):
+        units = B * H * ((Nq + 255) // 256)
+        nkb = (Nk + 127) // 128
+        if Nq > 128 and units >= sms:
+            return 1
+        slots = sms * 4 if (Nq == 1 and d == 64) else sms
+        n_max = min(max(1, nkb // 4), 64)
+        cost = lambda n: ((units * n + slots - 1) // slots) / n
+        best = min(cost(n) for n in range(1, n_max + 1))
+        return next(n for n in range(1, n_max + 1) if cost(n) <= best * 1.02)
+
+    for B, H, Nq, Nk, d in [(8, 16, 1, 32768, 128), (1, 16, 1, 131072, 128), (8, 32, 1, 32768, 64),
+                            (4, 16, 16, 32768, 128), (1, 16, 128, 65536, 128), (1, 2, 1, 300, 64),
+                            (2, 3, 5, 1500, 64), (4, 16, 2048, 2048, 128), (1, 1, 200, 100000, 128)]:
+        assert lib.fa_splitkv_default_splits(B, H, Nq, Nk, d) == expected(B, H, Nq, Nk, d), (B, H, Nq, Nk, d)
+    assert lib.fa_splitkv_default_splits(1, 1, 1, 1000, 96) == 0
+
+
 def test_strided_validation_statuses(lib):
     vp = ctypes.c_void_p
     good = (ctypes.c_int64 * 3)(128, 128 * 64, 128 * 64 * 2)
