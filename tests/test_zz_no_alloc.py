@@ -3,9 +3,9 @@
 Such callers (a plugin inside a framework that owns all device memory, or a
 loop where cudaMalloc's possible device-wide synchronisation is not allowed)
 pass inputs and outputs only; the library supplies the scratch from a fixed
-per-device buffer.  This test calls the new entry point through the C ABI and
-checks it against fa_bwd, the entry point with a caller workspace, on two calls
-in a row (the buffer keeps the previous call's contents, so the second call
+per-device buffer.  These tests call the entry point through the C ABI and
+check it against the float64 oracle, and against fa_bwd (the entry point with a
+caller workspace) on two calls in a row (the buffer keeps the previous call's contents, so the second call
 also shows that everything that must start at zero is cleared).  This file is
 collected last so that a run stopping at its first failure has already run
 every other test; it also passes alone in a fresh process.
@@ -50,6 +50,28 @@ def test_noalloc_backward_matches_fa_bwd_on_two_calls():
             assert _rel(a, b) <= BWD_REL, (call, name, _rel(a, b))
         # dK and dV involve no atomics: identical to the workspace entry point.
         assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_noalloc_backward_matches_the_oracle(d):
+    # The same entry point against the float64 oracle directly (ragged N, causal),
+    # every head, at the backward's bar: max|dX - dX_ref| <= 2e-2 max|dX_ref|.
+    from oracle import attention_backward
+
+    fa.load_library()
+    fa.fa_debug_set_fault(0)
+    fa.fa_debug_set_wait_limit_ns(0)
+    B, H, N = 1, 2, 333
+    x = normal_qkv(B, H, N, d, 311, with_do=True)
+    q, k, v, g = (x[n].to(torch.bfloat16).cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.fa_fwd(q, k, v, causal=True)
+    got = tuple(torch.empty_like(q) for _ in range(3))
+    fa.fa_bwd_noalloc(q, k, v, o, g, lse, *got, causal=True)
+    fa.fa_sync_check()
+    ref = attention_backward(q, k, v, g, d ** -0.5, True)
+    for name, a, r in zip(("dq", "dk", "dv"), got, ref):
+        err = float(np.abs(a.double().cpu().numpy() - r).max() / max(np.abs(r).max(), 1e-4))
+        assert err <= BWD_REL, (d, name, err)
 
 
 def test_noalloc_rejects_problems_beyond_its_buffer():
