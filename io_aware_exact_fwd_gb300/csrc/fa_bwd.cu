@@ -367,12 +367,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // warps' TMEM loads, bar_sde).  Otherwise warp 14 issues both.
         const bool issue_s = warp == kWarpMmaS;
         const bool issue_dp = kSplitSdp ? warp == kWarpMmaDP : warp == kWarpMmaS;
+        // Ring slot, its phase and byte offset, stepped instead of recomputed (these
+        // threads' instructions pace the step).
+        int slot = 0;
+        uint32_t ring_ph = 0, st = 0;
         for (int it = 0; ok && it < n; ++it) {
-          const int slot = it % kStages;
-          if (!(ok = mbar_wait(&bar_full[slot], (it / kStages) & 1, wc, kSiteBMmaQ))) break;
+          if (!(ok = mbar_wait(&bar_full[slot], ring_ph, wc, kSiteBMmaQ))) break;
           if (it >= 1 && !(ok = mbar_wait(bar_sde, (it - 1) & 1, wc, kSiteBMmaSd))) break;
           tc_fence_after();
-          const uint32_t st = slot * C::kStageBytes;
           if (issue_s) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -394,14 +396,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ss(tmem + C::kColDP, vaug, sdesc_add(ring_aug, st + C::kAugTile), idesc_sdp, 1u);  // - D
           }
           mma_commit(bar_sdp);
+          if (++slot == kStages) {
+            slot = 0;
+            ring_ph ^= 1u;
+            st = 0;
+          } else {
+            st += C::kStageBytes;
+          }
         }
       } else {
+        int slot = 0;  // ring slot and byte offset, stepped (see the S^T / dP^T issuers)
+        uint32_t st = 0;
         for (int it = 0; ok && it < n; ++it) {
           const int b = it & 1;
-          const int slot = it % kStages;
           if (!(ok = mbar_wait(&bar_comp[b], (it >> 1) & 1, wc, kSiteBMmaC))) break;
           tc_fence_after();
-          const uint32_t st = slot * C::kStageBytes;
           // dV += P^T dO_i ; dK += dS^T Q_i   (A from TMEM, B MN-major: 16 query rows per MMA)
 #pragma unroll
           for (int kk = 0; kk < kBqB / 16; ++kk)
@@ -420,6 +429,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ss(tmem + C::col_pdq(b), sdesc_add(k_mn, kk * 2048),
                         sdesc_add(ds_mn, b * C::kDsBytes + kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
           mma_commit(&bar_dqf[b]);
+          if (++slot == kStages) {
+            slot = 0;
+            st = 0;
+          } else {
+            st += C::kStageBytes;
+          }
         }
         if (ok) mma_commit(bar_dkv);
       }
